@@ -1,0 +1,106 @@
+"""Seeded synthetic KDA forward inputs (the workload recipe, no method arithmetic).
+
+This module is the one piece shared by the oracle-side tests and the CUDA
+path's tests and benchmark: it only draws random tensors.  It imports nothing
+else from this package, so importing it never loads the CUDA library.
+
+Recipe (for every named workload): a torch CPU ``Generator`` seeded with the
+workload's seed draws, in this order and in fp32,
+  q ~ N(0,1) [B,T,H,K], L2-normalised over K per (token, head), cast to bf16;
+  k ~ N(0,1) [B,T,H,K], L2-normalised the same way, cast to bf16;
+  v ~ N(0,1) [B,T,H,V], cast to bf16;
+  g = logsigmoid(N(0,1)) / 16 per dimension [B,T,H,K], fp32 (so g <= 0);
+  beta = sigmoid(N(0,1)) [B,T,H], fp32;
+  h0 = 0.1 * N(0,1) [N,H,V,K], fp32, for the workloads that carry one.
+This follows the operator page's "stable inputs" convention (log-sigmoid
+gates, sigmoid beta) with the scalings that the five named workloads fix.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+import torch
+import torch.nn.functional as F
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    T: int
+    H: int
+    K: int = 128
+    V: int = 128
+    seqlens: Optional[Sequence[int]] = None   # varlen packing (B == 1)
+    with_h0: bool = False
+    seed: int = 0
+    gate_div: float = 16.0
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def N(self) -> int:
+        return len(self.seqlens) if self.seqlens is not None else self.B
+
+    @property
+    def cu_seqlens(self) -> Optional[list]:
+        if self.seqlens is None:
+            return None
+        cu = [0]
+        for s in self.seqlens:
+            cu.append(cu[-1] + int(s))
+        return cu
+
+    @property
+    def token_heads(self) -> int:
+        return self.B * self.T * self.H
+
+
+# The five named workloads.
+WORKLOADS = {
+    "tiny": Workload("tiny", B=1, T=256, H=1, seed=0),
+    "b2_t2048_h8": Workload("b2_t2048_h8", B=2, T=2048, H=8, with_h0=True, seed=1),
+    "b4_t8192_h16": Workload("b4_t8192_h16", B=4, T=8192, H=16, seed=2),
+    "varlen6_t9192_h32": Workload("varlen6_t9192_h32", B=1, T=9192, H=32,
+                                  seqlens=(400, 624, 1000, 3000, 129, 4039),
+                                  with_h0=True, seed=3),
+    "t65536_h32": Workload("t65536_h32", B=1, T=65536, H=32, seed=4),
+}
+
+
+def make_inputs(w: Workload, device: str = "cpu"):
+    """Draw the workload's tensors.  Returns a dict with q, k, v (bf16), g, beta,
+    h0 (fp32 or None), cu_seqlens (int32 tensor or None), scale (None), N."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(w.seed))
+    B, T, H, K, V = w.B, w.T, w.H, w.K, w.V
+
+    def unit_rows(shape):
+        x = torch.randn(shape, generator=gen, dtype=torch.float32)
+        x = x / x.norm(dim=-1, keepdim=True)
+        return x.to(torch.bfloat16)
+
+    q = unit_rows((B, T, H, K))
+    k = unit_rows((B, T, H, K))
+    v = torch.randn((B, T, H, V), generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    g = F.logsigmoid(torch.randn((B, T, H, K), generator=gen, dtype=torch.float32)) / w.gate_div
+    beta = torch.sigmoid(torch.randn((B, T, H), generator=gen, dtype=torch.float32))
+    h0 = None
+    if w.with_h0:
+        h0 = 0.1 * torch.randn((w.N, H, V, K), generator=gen, dtype=torch.float32)
+    cu = None
+    if w.seqlens is not None:
+        assert B == 1 and sum(w.seqlens) == T
+        cu = torch.tensor(w.cu_seqlens, dtype=torch.int32)
+    out = dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, cu_seqlens=cu, scale=None, N=w.N)
+    if device != "cpu":
+        out = {kk: (vv.to(device) if isinstance(vv, torch.Tensor) else vv) for kk, vv in out.items()}
+    return out
+
+
+def custom(name: str, B: int, T: int, H: int, seqlens=None, with_h0=False, seed=0,
+           gate_div=16.0) -> Workload:
+    """A workload with the same distributions and other sizes (tests use these)."""
+    return Workload(name, B=B, T=T, H=H, seqlens=tuple(seqlens) if seqlens else None,
+                    with_h0=with_h0, seed=seed, gate_div=gate_div)
