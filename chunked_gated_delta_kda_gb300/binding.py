@@ -1,0 +1,148 @@
+"""Python binding of ``libkda.so`` (argument marshalling only).
+
+Every step of the forward runs in the library's CUDA kernels; this module
+checks torch tensors, allocates outputs and the workspace with torch on the
+tensors' device, and passes raw device pointers and torch's current stream to
+the C entry points declared in ``include/kda.h``.  If the library is missing
+or fails to load, every call raises: there is no fallback path.
+
+``fwd`` mirrors the operator page's host wrapper signature
+(``chunk_kda_wrapper(q, k, v, g, beta, scale=None, initial_state=None,
+output_final_state=False, use_qk_l2norm_in_kernel=False, cu_seqlens=None)``,
+page "PyPTO-Gym chunk_kda operator", section "算子签名与 I/O 规格").
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+KDA_FLAG_QK_L2NORM = 1
+
+_STATUS = {
+    0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
+    4: "invalid cu_seqlens", 5: "device wait timed out",
+}
+
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {_STATUS.get(code, 'unknown')} ({code})")
+
+
+def load_library(path: Optional[str] = None):
+    """Load (building first if needed) and return the ctypes handle."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if path is None:
+        path = _build.LIB if _build.up_to_date() else _build.build()
+    lib = ctypes.CDLL(path)
+    vp, i, f, sz, u = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint
+    lib.kda_fwd.restype = ctypes.c_int
+    lib.kda_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, u, vp, sz, vp]
+    lib.kda_fwd_workspace_bytes.restype = sz
+    lib.kda_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    lib.kda_get_status.restype = ctypes.c_int
+    lib.kda_get_status.argtypes = [vp, vp]
+    lib.kda_status_str.restype = ctypes.c_char_p
+    lib.kda_status_str.argtypes = [i]
+    _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def workspace_bytes(B: int, T: int, H: int, N: int, K: int = 128, V: int = 128) -> int:
+    return int(load_library().kda_fwd_workspace_bytes(B, T, H, K, V, N))
+
+
+def kda_fwd(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, N: int, flags: int,
+            workspace: torch.Tensor) -> None:
+    """Direct call of the C entry point on caller-provided tensors (all on one
+    CUDA device, contiguous).  Raises KdaError on a non-zero status."""
+    lib = load_library()
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    rc = lib.kda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                     float(scale if scale is not None else -1.0), _ptr(h0), _ptr(cu_seqlens),
+                     _ptr(o), _ptr(ht), B, T, H, K, V, N, flags, _ptr(workspace),
+                     workspace.numel() * workspace.element_size(), _stream_handle(q.device))
+    if rc != 0:
+        raise KdaError(rc, "kda_fwd")
+
+
+def get_status(workspace: torch.Tensor) -> int:
+    """Synchronise torch's current stream and return the device status code."""
+    lib = load_library()
+    return int(lib.kda_get_status(_ptr(workspace), _stream_handle(workspace.device)))
+
+
+def _check(name, t, dtype, ndim):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+        scale: Optional[float] = None, initial_state: Optional[torch.Tensor] = None,
+        output_final_state: bool = False, use_qk_l2norm_in_kernel: bool = False,
+        cu_seqlens: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None
+        ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunked KDA forward.  q, k: bf16 [B,T,H,K]; v: bf16 [B,T,H,V]; g: fp32
+    [B,T,H,K]; beta: fp32 [B,T,H]; initial_state: fp32 [N,H,V,K] or None;
+    cu_seqlens: int32 [N+1] on the device (varlen, B == 1) or None (fixed
+    length, T % 128 == 0).  Returns (o bf16 [B,T,H,V], final state fp32
+    [N,H,V,K] or None)."""
+    _check("q", q, torch.bfloat16, 4)
+    _check("k", k, torch.bfloat16, 4)
+    _check("v", v, torch.bfloat16, 4)
+    _check("g", g, torch.float32, 4)
+    _check("beta", beta, torch.float32, 3)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if k.shape != q.shape or g.shape != q.shape or v.shape[:3] != q.shape[:3] or beta.shape != q.shape[:3]:
+        raise ValueError("shape mismatch among q, k, v, g, beta")
+    if cu_seqlens is not None:
+        _check("cu_seqlens", cu_seqlens, torch.int32, 1)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    if initial_state is not None:
+        _check("initial_state", initial_state, torch.float32, 4)
+        if tuple(initial_state.shape) != (N, H, V, K):
+            raise ValueError(f"initial_state must be {(N, H, V, K)}, got {tuple(initial_state.shape)}")
+    dev = q.device
+    tensors = [q, k, v, g, beta] + [t for t in (initial_state, cu_seqlens) if t is not None]
+    if any(t.device != dev for t in tensors):
+        raise ValueError("all tensors must be on the same device")
+    q, k, v, g, beta = (t.contiguous() for t in (q, k, v, g, beta))
+    h0 = initial_state.contiguous() if initial_state is not None else None
+    o = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=dev)
+    ht = torch.empty((N, H, V, K), dtype=torch.float32, device=dev) if output_final_state else None
+    need = workspace_bytes(B, T, H, N, K, V)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    flags = KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0
+    with torch.cuda.device(dev):
+        kda_fwd(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, N, flags, workspace)
+    return o, ht

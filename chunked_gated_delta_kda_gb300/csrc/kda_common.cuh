@@ -1,0 +1,153 @@
+// Shared definitions for the chunked KDA forward kernels: sizes, the per-chunk
+// workspace tile layout, the chunk-slot map for fixed-length and varlen
+// packing, and the device status word.
+//
+// Method (page "PyPTO-Gym chunk_kda operator: an NPU forward of chunked gated
+// delta-rule linear attention", section "算法原理", steps M1-M4): split each
+// sequence into chunks of BT = 128 tokens; inside a chunk build the gated
+// k-k matrix A and the q-k matrix A2, invert (I + A), form the WY projections
+// w and u, then walk the chunks in order carrying the K x V state S.
+//
+// This implementation re-associates step M4 exactly (no approximation):
+//   v_new = u - w S,  o = qg S + A2 v_new,  S' = D S + kg^T v_new
+// becomes
+//   S' = D S + N S + Bc   with N = -kg^T w (K x K), Bc = kg^T u (K x V)
+//   o  = Qe S + Oi        with Qe = qg - A2 w (BT x K), Oi = A2 u (BT x V)
+// where qg = (scale q) * exp(G), kg = k * exp(G_last - G), D = diag(exp(G_last)).
+// Everything except the S recurrence is chunk-parallel (the "prep" kernel);
+// the recurrence is one K x K by K x V product per chunk (the "scan" kernel).
+#pragma once
+
+#include <cstdint>
+
+namespace kda {
+
+constexpr int BT = 128;   // chunk length (tokens)
+constexpr int KD = 128;   // key / query head dimension
+constexpr int VD = 128;   // value head dimension
+constexpr int BV = 32;    // value-dimension tile of one scan CTA
+constexpr int NVT = VD / BV;
+
+// ---------------------------------------------------------------------------
+// Per-(slot, head) workspace tile, written by the prep kernel and read by the
+// scan kernel with 1-D bulk copies.  Each piece is stored byte-for-byte in the
+// shared-memory layout the scan kernel's MMAs and threads expect.
+//   Nm  : fp16 K x K, K-major 128B-swizzled (A operand: rows d_out, cols d_in)
+//   Qe  : fp16 BT x K, K-major 128B-swizzled (A operand: rows t, cols d)
+//   Bc  : fp16 [NVT][K][BV], each [K][BV] piece 64B-swizzled (row d)
+//   Oi  : fp16 [NVT][BT][BV], each piece 64B-swizzled (row t)
+//   Dg  : fp32 [K] = exp(G_last)
+// ---------------------------------------------------------------------------
+constexpr uint32_t TILE_NM = 0;
+constexpr uint32_t TILE_QE = TILE_NM + KD * KD * 2;          // 32768
+constexpr uint32_t TILE_BC = TILE_QE + BT * KD * 2;          // 65536
+constexpr uint32_t BC_PIECE = KD * BV * 2;                   // 8192
+constexpr uint32_t TILE_OI = TILE_BC + NVT * BC_PIECE;       // 98304
+constexpr uint32_t OI_PIECE = BT * BV * 2;                   // 8192
+constexpr uint32_t TILE_DG = TILE_OI + NVT * OI_PIECE;       // 131072
+constexpr uint32_t TILE_BYTES = TILE_DG + KD * 4;            // 131584
+
+// Device status word bits (first 16 bytes of the workspace).
+constexpr uint32_t STATUS_BAD_CU = 1u;
+constexpr uint32_t STATUS_TIMEOUT = 2u;
+constexpr uint32_t WS_HEADER = 256;
+
+// Poll limit for mbarrier waits (MMA / bulk-copy completion inside one CTA).
+constexpr uint32_t WAIT_LIMIT = 1u << 24;
+
+struct FwdParams {
+    const uint16_t* q;      // bf16 [B*T, H, K]
+    const uint16_t* k;      // bf16 [B*T, H, K]
+    const uint16_t* v;      // bf16 [B*T, H, V]
+    const float* g;         // fp32 [B*T, H, K]
+    const float* beta;      // fp32 [B*T, H]
+    const float* h0;        // fp32 [N, H, V, K] or null
+    const int32_t* cu;      // int32 [N+1] or null (fixed length)
+    uint16_t* o;            // bf16 [B*T, H, V]
+    float* ht;              // fp32 [N, H, V, K] or null
+    uint8_t* tiles;         // workspace tiles, [nslots][H][TILE_BYTES]
+    uint32_t* status;       // workspace status word
+    float scale;
+    int T;                  // per-sequence length (fixed) or packed length (varlen)
+    int H;
+    int N;
+    int NT;                 // chunks per sequence (fixed length), else 0
+    int nslots;             // number of chunk slots the workspace holds
+};
+
+// A chunk: sequence n, chunk j inside it, first token (packed index), rows.
+struct ChunkRef {
+    int n;
+    int j;
+    long long tok0;
+    int len;
+    int slot;
+};
+
+__device__ __forceinline__ int cdiv128(int x) { return (x + BT - 1) / BT; }
+
+// Slot of chunk 0 of sequence n (varlen): floor(cu[n]/BT) + n.  Strictly
+// increasing in n and injective over (n, j) for j < ceil(len_n / BT), so a
+// workspace of floor(T/BT) + N + 1 slots per head holds every chunk.
+__device__ __forceinline__ int varlen_base(const int32_t* cu, int n) { return cu[n] / BT + n; }
+
+// Sequence bounds with validation: returns false (and flags the status word)
+// if cu is not a valid non-decreasing offset list into [0, T].
+__device__ __forceinline__ bool seq_bounds(const FwdParams& p, int n, long long& bos, int& len) {
+    if (p.cu == nullptr) {
+        bos = (long long)n * p.T;
+        len = p.T;
+        return true;
+    }
+    const int a = p.cu[n];
+    const int b = p.cu[n + 1];
+    if (a < 0 || b < a || b > p.T || (n == 0 && a != 0) || (n == p.N - 1 && b != p.T)) {
+        atomicOr(p.status, STATUS_BAD_CU);
+        return false;
+    }
+    bos = a;
+    len = b - a;
+    return true;
+}
+
+__device__ __forceinline__ int chunk_slot(const FwdParams& p, int n, int j) {
+    return p.cu == nullptr ? n * p.NT + j : varlen_base(p.cu, n) + j;
+}
+
+// Map a slot back to its chunk (prep kernel).  Returns false for slots that
+// hold no chunk (gaps in the varlen map, or slots past the end).
+__device__ __forceinline__ bool slot_chunk(const FwdParams& p, int slot, ChunkRef& c) {
+    int n, j;
+    if (p.cu == nullptr) {
+        if (slot >= p.N * p.NT) return false;
+        n = slot / p.NT;
+        j = slot % p.NT;
+    } else {
+        // largest n in [0, N) with base(n) <= slot
+        int lo = 0, hi = p.N - 1;
+        if (p.N <= 0 || varlen_base(p.cu, 0) > slot) return false;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (varlen_base(p.cu, mid) <= slot) lo = mid;
+            else hi = mid - 1;
+        }
+        n = lo;
+        j = slot - varlen_base(p.cu, n);
+    }
+    long long bos;
+    int len;
+    if (!seq_bounds(p, n, bos, len)) return false;
+    if (j * BT >= len) return false;
+    c.n = n;
+    c.j = j;
+    c.tok0 = bos + (long long)j * BT;
+    c.len = len - j * BT < BT ? len - j * BT : BT;
+    c.slot = slot;
+    return true;
+}
+
+__device__ __forceinline__ uint8_t* tile_ptr(const FwdParams& p, int slot, int h) {
+    return p.tiles + ((size_t)slot * p.H + h) * TILE_BYTES;
+}
+
+}  // namespace kda

@@ -1,0 +1,112 @@
+/*
+ * kda.h -- C ABI of the chunked Kimi Delta Attention (KDA) forward for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (page "PyPTO-Gym chunk_kda operator: an NPU forward of chunked
+ * gated delta-rule linear attention", lpnh.cn/news/2283126):
+ *   per sequence n and head h, with the K x V state S starting at h0[n,h]^T
+ *   (or zero) and, for every token t in order,
+ *       S <- diag(exp(g_t)) S                       (per-dimension gate decay)
+ *       S <- S + beta_t k_t (v_t - S^T k_t)^T       (delta update)
+ *       o_t = S^T (scale q_t)                       (read-out)
+ *   and finally ht[n,h] = S^T.  Section "算子定位与算法背景" gives the update
+ *   rule; section "算法原理" (M1-M4) gives the chunked evaluation with 128-token
+ *   chunks that the library runs; section "算子签名与 I/O 规格" gives the
+ *   tensors, dtypes and the [N, H, V, K] state layout; section "主机侧 wrapper
+ *   与输入校验" gives fixed-length vs varlen packing and the rule that the
+ *   host never reads cu_seqlens.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates nothing and keeps no pointer after the call returns.
+ *   - Calls are asynchronous on `stream`.  Argument checks happen on the host
+ *     before anything is enqueued; a failed check enqueues nothing.
+ *   - Errors are returned as kda_status; nothing is printed, nothing throws,
+ *     the process is never terminated.  Faults the device detects (an invalid
+ *     cu_seqlens, a wait that ran out) are recorded in the workspace status
+ *     word and read with kda_get_status().
+ *   - Tensor pointers must be 16-byte aligned; the tensors are contiguous in
+ *     the stated layout.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,     /* bad pointer, size, alignment or packing */
+    KDA_ERR_UNSUPPORTED = 2,     /* K != 128 or V != 128 */
+    KDA_ERR_CUDA = 3,            /* a CUDA runtime call failed */
+    KDA_ERR_BAD_CU_SEQLENS = 4,  /* device found cu_seqlens invalid (via kda_get_status) */
+    KDA_ERR_TIMEOUT = 5          /* a bounded device wait ran out (via kda_get_status) */
+} kda_status;
+
+/* Apply the per-token L2 normalisation x / sqrt(sum(x^2) + 1e-6) to q and k
+ * inside the kernel, before the scale (section "测试与验证体系" of the page). */
+#define KDA_FLAG_QK_L2NORM 1u
+
+/*
+ * Bytes of device workspace kda_fwd needs for these sizes (an upper bound
+ * that covers both fixed-length and varlen packing).  0 on invalid sizes.
+ * Layout: a 256-byte status header, then one 131584-byte tile per
+ * (128-token chunk slot, head).
+ */
+size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int N);
+
+/*
+ * Chunked KDA forward.
+ *
+ *   q, k        bf16 [B, T, H, K]   queries / keys (row-major, contiguous)
+ *   v           bf16 [B, T, H, V]
+ *   g           fp32 [B, T, H, K]   log-domain forget gate, expected <= 0
+ *   beta        fp32 [B, T, H]      delta-rule write strength
+ *   scale       multiplier for q; <= 0 or NaN means K^-0.5
+ *   h0          fp32 [N, H, V, K] initial state (transposed), or NULL for zero
+ *   cu_seqlens  int32 [N+1] device offsets of N packed sequences (varlen,
+ *               requires B == 1, cu[0] == 0, non-decreasing, cu[N] == T), or
+ *               NULL for fixed length (N == B sequences of T tokens,
+ *               T % 128 == 0).  Never read by the host.
+ *   o           bf16 [B, T, H, V]   output (written for every valid token)
+ *   ht          fp32 [N, H, V, K] final state, or NULL to skip it
+ *   B, T, H, K, V, N  sizes (K == V == 128)
+ *   flags       0 or KDA_FLAG_QK_L2NORM
+ *   workspace   device scratch of at least kda_fwd_workspace_bytes(...)
+ *               bytes, 256-byte aligned; its contents need not be
+ *               initialised.  Two calls that share a workspace must not
+ *               overlap in time.
+ *   stream      CUDA stream for every launch
+ *
+ * Precision: bf16 inputs, fp32 gate prefix sums, fp32 (I+A)^-1 and fp32
+ * state; tensor-core products use bf16 operands for the gated q.k / k.k
+ * matrices and fp16 operands for the rest, always with fp32 accumulation.
+ * The gated products are factored around the chunk's middle row; factors are
+ * capped at e^80, so results are exact (up to rounding) while the gate decay
+ * over any 64 tokens of a chunk stays below 80 in each dimension.
+ */
+kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                   float scale, const float* h0, const int32_t* cu_seqlens, void* o, float* ht, int B,
+                   int T, int H, int K, int V, int N, unsigned flags, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronise `stream`, then read the device status word that the last
+ * kda_fwd on this workspace wrote.  Returns KDA_OK, KDA_ERR_BAD_CU_SEQLENS,
+ * KDA_ERR_TIMEOUT, or KDA_ERR_CUDA if synchronising or reading failed.
+ */
+kda_status kda_get_status(const void* workspace, cudaStream_t stream);
+
+/* Static English description of a status code. */
+const char* kda_status_str(kda_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

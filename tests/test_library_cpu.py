@@ -1,0 +1,78 @@
+"""CPU-side checks of the C-ABI library: it builds, loads, exports every
+function include/kda.h declares, sizes the workspace, and rejects invalid
+arguments on the host before any CUDA call.  No compute runs here."""
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    from chunked_gated_delta_kda_gb300 import binding
+    lib = binding.load_library()
+    names = _declared_functions()
+    assert {"kda_fwd", "kda_fwd_workspace_bytes", "kda_get_status", "kda_status_str"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"libkda.so does not export {n}"
+
+
+def test_workspace_bytes():
+    from chunked_gated_delta_kda_gb300 import binding
+    lib = binding.load_library()
+    tile = 131584
+    # fixed length: B * T/128 slots; varlen bound: T/128 + N + 1
+    assert lib.kda_fwd_workspace_bytes(1, 65536, 32, 128, 128, 1) == 256 + 514 * 32 * tile
+    assert lib.kda_fwd_workspace_bytes(4, 8192, 16, 128, 128, 4) == 256 + 256 * 16 * tile
+    assert lib.kda_fwd_workspace_bytes(1, 9192, 32, 128, 128, 6) == 256 + 78 * 32 * tile
+    assert lib.kda_fwd_workspace_bytes(1, 256, 1, 64, 128, 1) == 0
+
+
+def test_status_strings():
+    from chunked_gated_delta_kda_gb300 import binding
+    lib = binding.load_library()
+    for code in range(6):
+        assert lib.kda_status_str(code)
+    assert b"unknown" in lib.kda_status_str(99)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-pointer validation cases run on CPU-only hosts")
+def test_host_validation_rejects_before_any_cuda_call():
+    """Every case below fails a host check, so no pointer is ever used."""
+    from chunked_gated_delta_kda_gb300 import binding
+    lib = binding.load_library()
+    buf = (ctypes.c_uint8 * 4096)()
+    p = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf) % 256), ctypes.c_void_p)
+    ws = lib.kda_fwd_workspace_bytes(1, 256, 1, 128, 128, 1)
+
+    def call(**kw):
+        a = dict(q=p, k=p, v=p, g=p, beta=p, scale=0.0, h0=None, cu=None, o=p, ht=None, B=1, T=256,
+                 H=1, K=128, V=128, N=1, flags=0, ws=p, wsb=ws)
+        a.update(kw)
+        return lib.kda_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["h0"], a["cu"], a["o"],
+                           a["ht"], a["B"], a["T"], a["H"], a["K"], a["V"], a["N"], a["flags"], a["ws"],
+                           a["wsb"], None)
+
+    assert call(K=64) == 2                  # unsupported head size
+    assert call(V=256) == 2
+    assert call(q=None) == 1                # null tensor
+    assert call(ws=None) == 1
+    assert call(T=200) == 1                 # fixed length needs T % 128 == 0
+    assert call(N=2) == 1                   # fixed length needs N == B
+    assert call(B=2, N=2, cu=p) == 1        # varlen needs B == 1
+    assert call(wsb=ws - 1) == 1            # workspace too small
+    assert call(flags=4) == 1               # unknown flag
+    assert call(H=0) == 1
+    misaligned = ctypes.c_void_p(p.value + 8)
+    assert call(o=misaligned) == 1          # 16-byte alignment
+    assert call(ws=misaligned) == 1         # 256-byte workspace alignment
