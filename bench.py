@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Benchmark of the chunked KDA forward on GB300.
+
+One step = one full forward (every stage of the hot path) over the workload's
+synthetic inputs, already resident in HBM.  Default workload: B=1, T=65536,
+H=32, K=V=128 (the large named workload), whose 2.7 GB of inputs per step
+exceed the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 oracle
+on the host cores instead (the reference arm; no public implementation of
+this method exists to run).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from chunked_gated_delta_kda_gb300.inputs import WORKLOADS, custom, make_inputs  # noqa: E402
+
+METRIC = "KDA fwd tokens*heads/s and TFLOP/s, % of roofline, at T=64K H=32 K=V=128"
+UNIT = "token*heads/s"
+N128 = 128
+# Algorithmic work per token-head (n = 128, triangular products at their
+# triangular size): 11 1/3 n^2 flop; dense-tile count 16 1/3 n^2.
+ALG_FLOP_PER_TH = (34.0 / 3.0) * N128 * N128
+DENSE_FLOP_PER_TH = (49.0 / 3.0) * N128 * N128
+# Algorithmic HBM bytes per token-head: q, k, v bf16 (3 x 256) + g fp32 512
+# + beta 4 + o bf16 256.  The chunk-parallel kernel's share is the inputs
+# (1284 B), the scan kernel's share the output (256 B) plus state I/O.
+BYTES_PER_TH = 1540
+PREP_BYTES_PER_TH = 1284
+SCAN_BYTES_PER_TH = 256
+STATE_BYTES = N128 * N128 * 4
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def load_traffic():
+    """Per-kernel DRAM traffic (bytes per token-head) from the committed ncu
+    summary, keyed by the source hash it was captured on; a kernel whose
+    source changed since reads as None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    out = {}
+    if not os.path.exists(path):
+        return out
+    src_dir = os.path.join(ROOT, "chunked_gated_delta_kda_gb300", "csrc")
+    with open(path) as f:
+        for line in f:
+            parts = [p.strip() for p in line.strip().strip("|").split("|")]
+            if len(parts) >= 4 and parts[0].startswith("kda_"):
+                kernel, fname, sha, per_th = parts[0], parts[1], parts[2], parts[3]
+                fp = os.path.join(src_dir, fname)
+                if not os.path.exists(fp):
+                    continue
+                cur = hashlib.sha256(open(fp, "rb").read()).hexdigest()[:12]
+                try:
+                    out[kernel] = float(per_th) if cur == sha else None
+                except ValueError:
+                    out[kernel] = None
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t_start, t_end):
+        rows = []
+        for ts, line in self.lines:
+            if t_start <= ts <= t_end + 0.05:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 7:
+                    rows.append(parts)
+        if not rows:
+            rows = [[p.strip() for p in l.split(",")] for _, l in self.lines[-3:] if l.count(",") >= 6]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def algorithmic(w, N):
+    th = w.B * w.T * w.H
+    state_io = (STATE_BYTES * N * w.H) * (2 if w.with_h0 else 1)
+    return th, th * BYTES_PER_TH + state_io, th * ALG_FLOP_PER_TH, th * DENSE_FLOP_PER_TH
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline / reference arm: the fp64 oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_rate(w, target_s=10.0, max_tokens=None):
+    """Time the oracle (as it stands) on the first T_s tokens of the workload,
+    all heads; T_s sized so the run takes about ``target_s`` seconds."""
+    import oracle
+    threads = oracle.max_threads()
+    H = w.H
+
+    def run(Ts):
+        x = make_inputs(custom("sample", B=1, T=Ts, H=H, seed=w.seed))
+        args = [x[n].float().numpy() for n in ("q", "k", "v", "g", "beta")]
+        t0 = time.perf_counter()
+        oracle.kda_recurrent(*args)
+        return time.perf_counter() - t0
+
+    Ts = 128
+    dt = run(Ts)
+    while dt < target_s / 8 and Ts < (max_tokens or w.T):
+        Ts = min(Ts * 4, max_tokens or w.T)
+        dt = run(Ts)
+    if dt < target_s / 2 and Ts < (max_tokens or w.T):
+        Ts = min(int(Ts * target_s / max(dt, 1e-3)), max_tokens or w.T)
+        dt = run(Ts)
+    return {"value": Ts * H / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"fp64 per-token recurrence (C, OpenMP over heads) on the first {Ts} tokens x {H} heads "
+                      f"of the {w.name} workload ({Ts * H} token-heads, {dt:.1f} s)",
+            "seconds": dt, "tokens": Ts}
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    cal = oracle_rate(w, target_s=2.0)
+    per_step_s = max(0.05, min(1.0, 120.0 / max(1, args.steps + args.warmup)))
+    Ts = max(8, min(w.T, int(cal["tokens"] * per_step_s / max(cal["seconds"], 1e-3))))
+    x = make_inputs(custom("ref", B=1, T=Ts, H=w.H, seed=w.seed))
+    a = [x[n].float().numpy() for n in ("q", "k", "v", "g", "beta")]
+    for _ in range(args.warmup):
+        oracle.kda_recurrent(*a)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.kda_recurrent(*a)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = Ts * w.H / dt
+    th, _, _, _ = algorithmic(w, w.N)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V,
+                       "step": f"bounded sample: first {Ts} tokens x {w.H} heads of the workload"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cal["cores"], "kind": "oracle",
+                             "sample": f"first {Ts} tokens x {w.H} heads per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="t65536_h32", choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+
+    import torch.distributed as dist
+    from chunked_gated_delta_kda_gb300 import binding
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load_library()
+
+    # Weak scaling: every rank runs the full workload on its own GPU (the
+    # (sequence, head) units are independent; no data-path collective).
+    x = make_inputs(w, device=str(dev), draw_on_device=True, seed_offset=rank)
+    q, k, v, g, beta, h0, cu = (x[n] for n in ("q", "k", "v", "g", "beta", "h0", "cu_seqlens"))
+    N, H, B, T = w.N, w.H, w.B, w.T
+    o = torch.empty((B, T, H, w.V), dtype=torch.bfloat16, device=dev)
+    ht = torch.empty((N, H, w.V, w.K), dtype=torch.float32, device=dev)
+    ws = torch.empty(binding.workspace_bytes(B, T, H, N), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        binding.kda_fwd(q, k, v, g, beta, None, h0, cu, o, ht, N, 0, ws)
+
+    for _ in range(args.warmup):
+        step()
+    st = binding.get_status(ws)
+    assert st == 0, f"device status {st}"
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for trio in ev:            # torch creates the CUDA event on first record
+        for e in trio:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        binding.kda_fwd_timed(q, k, v, g, beta, None, h0, cu, o, ht, N, 0, ws, ev[i])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_end = time.time()
+    if world > 1:
+        dist.barrier()
+    clocks.stop()
+    total_ms = e0.elapsed_time(e1)
+    prep_ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)) / args.steps
+    scan_ms = sum(ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)) / args.steps
+    st = binding.get_status(ws)
+    assert st == 0, f"device status {st}"
+
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_per_step = float(t.item()) / args.steps
+
+    th, alg_bytes, alg_flop, dense_flop = algorithmic(w, N)
+    value = world * th / (ms_per_step * 1e-3)
+    peaks = load_peaks()
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg_flop / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_roof = max(t_hbm, t_tc)
+    traffic = load_traffic()
+
+    stages = {
+        "kda_prep_kernel": {"ms": prep_ms, "alg_bytes": th * PREP_BYTES_PER_TH},
+        "kda_scan_kernel": {"ms": scan_ms, "alg_bytes": th * SCAN_BYTES_PER_TH + STATE_BYTES * N * H * (2 if h0 is not None else 1)},
+    }
+    dom = max(stages, key=lambda s: stages[s]["ms"])
+    d = stages[dom]
+    achieved = d["alg_bytes"] / (d["ms"] * 1e-3) / 1e9
+    tr = traffic.get(dom)
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"],
+                "traffic": (tr * th if tr is not None else None),
+                "peak_source": f"{peaks['source']} (hbm_gbs, MEASURED_PEAKS.json)" if peaks["source"] == "measured"
+                else "fallback 6.8 TB/s",
+                "alg_bytes_per_launch": d["alg_bytes"], "ms_per_launch": d["ms"]}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "T": T, "H": H, "K": w.K, "V": w.V, "chunk": 128,
+                   "h0": h0 is not None, "output_final_state": True,
+                   "l2_between_steps": "inputs (2.7 GB per step) larger than L2 (129 MB); no flush",
+                   "inputs": "seeded synthetic, drawn on device with the workload's recipe"},
+        "tflops_alg": alg_flop / (ms_per_step * 1e-3) / 1e12,
+        "tflops_dense": dense_flop / (ms_per_step * 1e-3) / 1e12,
+        "gbs_alg": alg_bytes / (ms_per_step * 1e-3) / 1e9,
+        "path_roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor", "t_roof_us": t_roof * 1e6,
+                          "t_hbm_us": t_hbm * 1e6, "t_tensor_us": t_tc * 1e6,
+                          "frac": t_roof / (ms_per_step * 1e-3)},
+        "stages_ms": {"kda_prep_kernel": prep_ms, "kda_scan_kernel": scan_ms},
+        "roofline": roofline,
+        "gpu_launches": 2 * args.steps,
+    }
+
+    # End to end through the public API: pinned host inputs -> device, forward,
+    # output and final state -> pinned host, all inside the timed region.
+    if args.e2e_steps > 0:
+        host = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta") if x[n] is not None}
+        if h0 is not None:
+            host["h0"] = h0.cpu().pin_memory()
+        o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        ht_host = torch.empty(ht.shape, dtype=ht.dtype).pin_memory()
+        dbuf = {n: torch.empty_like(x[n] if n != "h0" else h0) for n in host}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = o_host.numel() * o_host.element_size() + ht_host.numel() * ht_host.element_size()
+
+        def e2e_step():
+            for n, t in host.items():
+                dbuf[n].copy_(t, non_blocking=True)
+            binding.kda_fwd(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], None, dbuf.get("h0"), cu,
+                            o, ht, N, 0, ws)
+            o_host.copy_(o, non_blocking=True)
+            ht_host.copy_(ht, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        te = torch.tensor([f0.elapsed_time(f1) / args.e2e_steps], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        line["e2e"] = {"value": world * th / (float(te.item()) * 1e-3), "unit": UNIT,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": float(te.item())}
+        line["gpu_launches_e2e"] = 2 * args.e2e_steps
+
+    line["clocks"] = clocks.summary(t_start, t_end)
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_rate(w, target_s=args.cpu_seconds)
+        for kk in ("seconds", "tokens"):
+            line["cpu_baseline"].pop(kk, None)
+
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

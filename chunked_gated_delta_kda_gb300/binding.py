@@ -49,6 +49,8 @@ def load_library(path: Optional[str] = None):
     vp, i, f, sz, u = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint
     lib.kda_fwd.restype = ctypes.c_int
     lib.kda_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, u, vp, sz, vp]
+    lib.kda_fwd_timed.restype = ctypes.c_int
+    lib.kda_fwd_timed.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, u, vp, sz, vp, vp]
     lib.kda_fwd_workspace_bytes.restype = sz
     lib.kda_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i]
     lib.kda_get_status.restype = ctypes.c_int
@@ -84,6 +86,22 @@ def kda_fwd(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, N: int, flags: int,
                      workspace.numel() * workspace.element_size(), _stream_handle(q.device))
     if rc != 0:
         raise KdaError(rc, "kda_fwd")
+
+
+def kda_fwd_timed(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, N: int, flags: int,
+                  workspace: torch.Tensor, events) -> None:
+    """kda_fwd that also records three torch.cuda.Event objects (created with
+    enable_timing=True) around the two stages on torch's current stream."""
+    lib = load_library()
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    ev = (ctypes.c_void_p * 3)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    rc = lib.kda_fwd_timed(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                           float(scale if scale is not None else -1.0), _ptr(h0), _ptr(cu_seqlens),
+                           _ptr(o), _ptr(ht), B, T, H, K, V, N, flags, _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _stream_handle(q.device), ev)
+    if rc != 0:
+        raise KdaError(rc, "kda_fwd_timed")
 
 
 def get_status(workspace: torch.Tensor) -> int:

@@ -33,9 +33,10 @@ size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int N) {
     return (size_t)kda::WS_HEADER + (size_t)max_slots(B, T, N) * (size_t)H * kda::TILE_BYTES;
 }
 
-kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
-                   const float* h0, const int32_t* cu_seqlens, void* o, float* ht, int B, int T, int H, int K, int V,
-                   int N, unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+static kda_status fwd_impl(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                           float scale, const float* h0, const int32_t* cu_seqlens, void* o, float* ht, int B, int T,
+                           int H, int K, int V, int N, unsigned flags, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream, cudaEvent_t* ev) {
     if (K != kda::KD || V != kda::VD) return KDA_ERR_UNSUPPORTED;
     // With T == 0 there is nothing to read or write (frameworks hand out null
     // pointers for empty tensors); only the state tensors and workspace are used.
@@ -81,11 +82,30 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, 
     }
 
     if (cudaMemsetAsync(workspace, 0, 16, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (p.nslots > 0) {
         if (kda::launch_prep(p, (flags & KDA_FLAG_QK_L2NORM) != 0u, stream) != cudaSuccess) return KDA_ERR_CUDA;
     }
+    if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::launch_scan(p, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
+}
+
+kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
+                   const float* h0, const int32_t* cu_seqlens, void* o, float* ht, int B, int T, int H, int K, int V,
+                   int N, unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return fwd_impl(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, B, T, H, K, V, N, flags, workspace,
+                    workspace_bytes, stream, nullptr);
+}
+
+kda_status kda_fwd_timed(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         float scale, const float* h0, const int32_t* cu_seqlens, void* o, float* ht, int B, int T,
+                         int H, int K, int V, int N, unsigned flags, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream, cudaEvent_t* stage_events) {
+    if (!stage_events || !stage_events[0] || !stage_events[1] || !stage_events[2]) return KDA_ERR_INVALID_ARG;
+    return fwd_impl(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, B, T, H, K, V, N, flags, workspace,
+                    workspace_bytes, stream, stage_events);
 }
 
 kda_status kda_get_status(const void* workspace, cudaStream_t stream) {

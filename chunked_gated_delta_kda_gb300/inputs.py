@@ -69,32 +69,42 @@ WORKLOADS = {
 }
 
 
-def make_inputs(w: Workload, device: str = "cpu"):
+def make_inputs(w: Workload, device: str = "cpu", draw_on_device: bool = False, seed_offset: int = 0):
     """Draw the workload's tensors.  Returns a dict with q, k, v (bf16), g, beta,
-    h0 (fp32 or None), cu_seqlens (int32 tensor or None), scale (None), N."""
-    gen = torch.Generator(device="cpu")
-    gen.manual_seed(int(w.seed))
+    h0 (fp32 or None), cu_seqlens (int32 tensor or None), scale (None), N.
+
+    By default the draws come from a CPU generator (the values the oracle
+    tests use) and are then moved to ``device``.  ``draw_on_device=True``
+    draws the same distributions with a generator on ``device`` instead (a
+    different, equally seeded stream of numbers; used where only timing
+    matters and the workload is too large to draw quickly on the host)."""
+    gdev = device if draw_on_device else "cpu"
+    gen = torch.Generator(device=gdev)
+    gen.manual_seed(int(w.seed) + int(seed_offset))
     B, T, H, K, V = w.B, w.T, w.H, w.K, w.V
 
+    def randn(shape):
+        return torch.randn(shape, generator=gen, dtype=torch.float32, device=gdev)
+
     def unit_rows(shape):
-        x = torch.randn(shape, generator=gen, dtype=torch.float32)
+        x = randn(shape)
         x = x / x.norm(dim=-1, keepdim=True)
         return x.to(torch.bfloat16)
 
     q = unit_rows((B, T, H, K))
     k = unit_rows((B, T, H, K))
-    v = torch.randn((B, T, H, V), generator=gen, dtype=torch.float32).to(torch.bfloat16)
-    g = F.logsigmoid(torch.randn((B, T, H, K), generator=gen, dtype=torch.float32)) / w.gate_div
-    beta = torch.sigmoid(torch.randn((B, T, H), generator=gen, dtype=torch.float32))
+    v = randn((B, T, H, V)).to(torch.bfloat16)
+    g = F.logsigmoid(randn((B, T, H, K))) / w.gate_div
+    beta = torch.sigmoid(randn((B, T, H)))
     h0 = None
     if w.with_h0:
-        h0 = 0.1 * torch.randn((w.N, H, V, K), generator=gen, dtype=torch.float32)
+        h0 = 0.1 * randn((w.N, H, V, K))
     cu = None
     if w.seqlens is not None:
         assert B == 1 and sum(w.seqlens) == T
-        cu = torch.tensor(w.cu_seqlens, dtype=torch.int32)
+        cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=gdev)
     out = dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, cu_seqlens=cu, scale=None, N=w.N)
-    if device != "cpu":
+    if device != gdev:
         out = {kk: (vv.to(device) if isinstance(vv, torch.Tensor) else vv) for kk, vv in out.items()}
     return out
 

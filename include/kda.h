@@ -96,6 +96,19 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, 
                    size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * kda_fwd, additionally recording three caller-created CUDA events on
+ * `stream`: stage_events[0] before the chunk-parallel kernel, [1] between it
+ * and the sequential scan kernel, [2] after the scan.  Elapsed times between
+ * them give each stage's device time inside a running sequence of calls.
+ * Same arguments, contract and errors as kda_fwd; INVALID_ARG if any event
+ * is null.
+ */
+kda_status kda_fwd_timed(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         float scale, const float* h0, const int32_t* cu_seqlens, void* o, float* ht, int B,
+                         int T, int H, int K, int V, int N, unsigned flags, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream, cudaEvent_t* stage_events);
+
+/*
  * Synchronise `stream`, then read the device status word that the last
  * kda_fwd on this workspace wrote.  Returns KDA_OK, KDA_ERR_BAD_CU_SEQLENS,
  * KDA_ERR_TIMEOUT, or KDA_ERR_CUDA if synchronising or reading failed.
