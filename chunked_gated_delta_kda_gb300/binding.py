@@ -26,7 +26,7 @@ KDA_FLAG_QK_L2NORM = 1
 
 _STATUS = {
     0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
-    4: "invalid cu_seqlens", 5: "device wait timed out",
+    4: "invalid cu_seqlens", 5: "device wait timed out", 6: "too large for the no-alloc scratch",
 }
 
 _lib = None
@@ -51,6 +51,8 @@ def load_library(path: Optional[str] = None):
     lib.kda_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, u, vp, sz, vp]
     lib.kda_fwd_timed.restype = ctypes.c_int
     lib.kda_fwd_timed.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, u, vp, sz, vp, vp]
+    lib.kda_fwd_noalloc.restype = ctypes.c_int
+    lib.kda_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, u, vp]
     lib.kda_fwd_workspace_bytes.restype = sz
     lib.kda_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i]
     lib.kda_get_status.restype = ctypes.c_int
@@ -102,6 +104,21 @@ def kda_fwd_timed(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, N: int, flags:
                            workspace.numel() * workspace.element_size(), _stream_handle(q.device), ev)
     if rc != 0:
         raise KdaError(rc, "kda_fwd_timed")
+
+
+def kda_fwd_noalloc(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, N: int, flags: int) -> None:
+    """The no-allocation entry point: like kda_fwd but the library supplies
+    the workspace from its static device scratch (for callers that cannot
+    allocate device memory).  Raises KdaError (code 6) if the problem does
+    not fit the scratch."""
+    lib = load_library()
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    rc = lib.kda_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                             float(scale if scale is not None else -1.0), _ptr(h0), _ptr(cu_seqlens),
+                             _ptr(o), _ptr(ht), B, T, H, K, V, N, flags, _stream_handle(q.device))
+    if rc != 0:
+        raise KdaError(rc, "kda_fwd_noalloc")
 
 
 def get_status(workspace: torch.Tensor) -> int:

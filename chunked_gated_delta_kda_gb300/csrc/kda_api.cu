@@ -126,6 +126,7 @@ const char* kda_status_str(kda_status status) {
         case KDA_ERR_CUDA: return "CUDA runtime error";
         case KDA_ERR_BAD_CU_SEQLENS: return "device found cu_seqlens invalid";
         case KDA_ERR_TIMEOUT: return "a bounded device wait ran out";
+        case KDA_ERR_TOO_LARGE: return "problem too large for the static no-alloc scratch";
     }
     return "unknown status";
 }

@@ -45,7 +45,9 @@ typedef enum {
     KDA_ERR_UNSUPPORTED = 2,     /* K != 128 or V != 128 */
     KDA_ERR_CUDA = 3,            /* a CUDA runtime call failed */
     KDA_ERR_BAD_CU_SEQLENS = 4,  /* device found cu_seqlens invalid (via kda_get_status) */
-    KDA_ERR_TIMEOUT = 5          /* a bounded device wait ran out (via kda_get_status) */
+    KDA_ERR_TIMEOUT = 5,         /* a bounded device wait ran out (via kda_get_status) */
+    KDA_ERR_TOO_LARGE = 6        /* kda_fwd_noalloc: the problem needs more workspace than
+                                    the library's static scratch holds */
 } kda_status;
 
 /* Apply the per-token L2 normalisation x / sqrt(sum(x^2) + 1e-6) to q and k
@@ -114,6 +116,37 @@ kda_status kda_fwd_timed(const void* q, const void* k, const void* v, const floa
  * KDA_ERR_TIMEOUT, or KDA_ERR_CUDA if synchronising or reading failed.
  */
 kda_status kda_get_status(const void* workspace, cudaStream_t stream);
+
+/*
+ * Size of the static device scratch array behind kda_fwd_noalloc (64 MiB).
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * kda_fwd for callers that cannot allocate device memory (code running while
+ * a stream is being captured into a CUDA graph, inside an allocator callback,
+ * or under a host application that owns every allocation).  No counterpart
+ * on the method's pages: it is a deployment convenience of this library.
+ *
+ * Same arguments, layouts and precision as kda_fwd, minus the workspace: the
+ * library uses a static __device__ array of KDA_NOALLOC_SCRATCH_BYTES that
+ * every GPU which loads the library holds until the process exits.  Problems
+ * with kda_fwd_workspace_bytes(...) > KDA_NOALLOC_SCRATCH_BYTES return
+ * KDA_ERR_TOO_LARGE and enqueue nothing (at B=1 and H=8 that is T above about
+ * 7,800 tokens).  The call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *
+ * The first call on each device looks up the array's device address with
+ * cudaGetSymbolAddress (with that device current); make that first call
+ * before any stream capture begins.  Every call on a device shares the one
+ * array: calls whose GPU work overlaps in time (on different streams, or
+ * from different host threads) race on it and give undefined results, so
+ * serialise them.  kda_get_status() is not available for this entry point
+ * (the status word lives in the shared array).
+ */
+kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                           float scale, const float* h0, const int32_t* cu_seqlens, void* o, float* ht,
+                           int B, int T, int H, int K, int V, int N, unsigned flags, cudaStream_t stream);
 
 /* Static English description of a status code. */
 const char* kda_status_str(kda_status status);
