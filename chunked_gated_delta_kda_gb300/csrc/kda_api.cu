@@ -30,7 +30,8 @@ extern "C" {
 
 size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int N) {
     if (B < 1 || T < 0 || H < 1 || N < 1 || K != kda::KD || V != kda::VD) return 0;
-    return (size_t)kda::WS_HEADER + (size_t)max_slots(B, T, N) * (size_t)H * kda::TILE_BYTES;
+    const unsigned long long items = (unsigned long long)max_slots(B, T, N) * (unsigned long long)H;
+    return (size_t)(kda::ws_tiles_offset(items) + items * kda::TILE_BYTES);
 }
 
 static kda_status fwd_impl(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -67,8 +68,11 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const fl
     p.cu = cu_seqlens;
     p.o = static_cast<uint16_t*>(o);
     p.ht = ht;
+    const unsigned long long items = (unsigned long long)max_slots(B, T, N) * (unsigned long long)H;
     p.status = static_cast<uint32_t*>(workspace);
-    p.tiles = static_cast<uint8_t*>(workspace) + kda::WS_HEADER;
+    p.wide_count = static_cast<uint32_t*>(workspace) + 1;
+    p.wide_list = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + kda::WS_HEADER);
+    p.tiles = static_cast<uint8_t*>(workspace) + kda::ws_tiles_offset(items);
     p.scale = scale;
     p.T = T;
     p.H = H;
@@ -81,7 +85,7 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const fl
         p.nslots = T / kda::BT + N + 1;
     }
 
-    if (cudaMemsetAsync(workspace, 0, 16, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, kda::WS_CLEAR, stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (p.nslots > 0) {
         if (kda::launch_prep(p, (flags & KDA_FLAG_QK_L2NORM) != 0u, stream) != cudaSuccess) return KDA_ERR_CUDA;

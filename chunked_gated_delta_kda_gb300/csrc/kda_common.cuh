@@ -47,10 +47,19 @@ constexpr uint32_t OI_PIECE = BT * BV * 2;                   // 8192
 constexpr uint32_t TILE_DG = TILE_OI + NVT * OI_PIECE;       // 131072
 constexpr uint32_t TILE_BYTES = TILE_DG + KD * 4;            // 131584
 
-// Device status word bits (first 16 bytes of the workspace).
+// Workspace header: word 0 = device status bits, word 1 = number of entries
+// in the wide-range work list, then (from byte 256) the list itself (one
+// int32 work-item id per (chunk slot, head) at most), then the tiles.  The
+// first 16 bytes are cleared at the start of every call.
 constexpr uint32_t STATUS_BAD_CU = 1u;
 constexpr uint32_t STATUS_TIMEOUT = 2u;
 constexpr uint32_t WS_HEADER = 256;
+constexpr uint32_t WS_CLEAR = 16;
+
+// Bytes before the tiles for a workspace holding `items` (slot, head) tiles.
+__host__ __device__ constexpr unsigned long long ws_tiles_offset(unsigned long long items) {
+    return WS_HEADER + ((items * 4ull + 255ull) / 256ull) * 256ull;
+}
 
 // Poll limit for mbarrier waits (MMA / bulk-copy completion inside one CTA).
 constexpr uint32_t WAIT_LIMIT = 1u << 24;
@@ -67,6 +76,8 @@ struct FwdParams {
     float* ht;              // fp32 [N, H, V, K] or null
     uint8_t* tiles;         // workspace tiles, [nslots][H][TILE_BYTES]
     uint32_t* status;       // workspace status word
+    uint32_t* wide_count;   // number of work items queued for the wide-range path
+    int32_t* wide_list;     // their ids (slot * H + head)
     float scale;
     int T;                  // per-sequence length (fixed) or packed length (varlen)
     int H;

@@ -14,14 +14,28 @@
 // beta = 0 makes the rows inert), and "数值稳定性" (fp32 inverse; the gated
 // products are factored around a pivot row with the exponent capped at 80).
 //
-// GB300 mapping.  A persistent kernel: one 512-thread CTA per SM walks the
-// (chunk, head) work items.  The five 128-wide contractions run on tcgen05
-// tensor cores with fp32 accumulators in TMEM (A/A2 with bf16 operands for
-// range, everything downstream of the inverse with fp16 operands for
-// precision).  The prefix sum, the gated operands and the 16x16 / 32x32 /
-// 64x64 levels of the inverse run on CUDA cores in fp32; the 64 -> 128 level
-// of the inverse runs on the tensor cores.  While one chunk computes, its
-// successor's input rows are prefetched into L2.
+// Factoring.  With a pivot P (per dimension, the prefix sum at row 64),
+//   E = exp(G - P),  F = exp(P - G),
+//   Lk = k E, Lq = (scale q) E, R = k F,  so that A_raw = Lk R^T, A2_raw = Lq R^T.
+// Two variants of the kernel share everything after the gated products:
+//   * fast (fp16 gated operands): when every Lk, Lq, R, v of the chunk fits
+//     comfortably in fp16, the other operands are exact column / row
+//     rescalings of these tiles and need no tiles of their own:
+//       exp(G) k = Lk diag(exp(P))      ->  w = ((I+A)^-1 diag(beta) Lk) diag(exp(P))
+//       kg       = R  diag(exp(G_last - P)) -> Nm = -diag(exp(G_last-P)) R^T w
+//       qg       = Lq diag(exp(P))      ->  Qe = Lq diag(exp(P)) - A2 w
+//     with beta folded into the columns of the inverse.
+//   * wide (bf16 gated operands): chunks whose factors would overflow fp16
+//     (strong decay inside the chunk) are queued by the fast kernel and
+//     redone by this variant, which builds exp(G) k, kg, qg and beta v as
+//     separate fp16 tiles.
+//
+// GB300 mapping.  Persistent kernels: one 512-thread CTA per SM walks the
+// work items.  The 128-wide contractions run on tcgen05 tensor cores with
+// fp32 accumulators in TMEM; the prefix sum, the gated operands and the
+// 16x16 / 32x32 / 64x64 levels of the inverse run on CUDA cores in fp32; the
+// 64 -> 128 level of the inverse runs on the tensor cores.  While one chunk
+// computes, its successor's input rows are prefetched into L2.
 #include "kda_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -34,32 +48,52 @@ constexpr float LOG2E = 1.4426950408889634f;
 // exp2 argument cap: 2^115 ~ e^80, the page's decay cap; keeps every factor
 // finite so that a zero operand never meets an infinite one.
 constexpr float EXP2_CAP = 115.0f;
+// The fast variant keeps a chunk only if every gated operand is below this
+// (fp16 max is 65504; the margin keeps products and sums finite).
+constexpr float FP16_SAFE = 16384.0f;
 
-// Shared-memory map (bytes from the 1024-aligned base).
-constexpr uint32_t RX = 0;        // 64 KB: Lk | Lq  ->  qg | kg
-constexpr uint32_t RY = 65536;    // 32 KB: R -> A10 / P / Q / T merge tiles -> Ainv
-constexpr uint32_t RZ = 98304;    // 64 KB: RHS [t][k|v] -> w|u
-constexpr uint32_t RW = 163840;   // 48 KB: fp32 diagonal 64-blocks + merge temps -> A2 fp16
-constexpr uint32_t RM = 212992;   // misc
+// Shared-memory regions (bytes from the 1024-aligned base).
+//                      fast variant                      wide variant
+//   0      .. 64K :    Lk | v16   -> w | u               Lk | Lq -> qg | kg
+//   64K    .. 96K :    Lq                                R -> merge tiles -> Ainv
+//   96K    .. 128K:    R                                 RHS (k part) -> w
+//   128K   .. 160K:    merge tiles -> Ainv               RHS (v part) -> u
+//   160K   .. 208K:    scan sums -> fp32 diag blocks     qg stash -> fp32 diag
+//                      -> A2                             blocks -> A2
+constexpr uint32_t RM = 212992;            // misc
 constexpr uint32_t M_G64 = RM;             // f32[128]  G at the pivot row (log2 units)
 constexpr uint32_t M_GL = RM + 512;        // f32[128]  G at the last row (log2 units)
 constexpr uint32_t M_BETA = RM + 1024;     // f32[128]
 constexpr uint32_t M_INVQ = RM + 1536;     // f32[128]  scale / ||q|| (or scale)
 constexpr uint32_t M_INVK = RM + 2048;     // f32[128]  1 / ||k|| (or 1)
-constexpr uint32_t M_TOT = RM + 2560;      // f32[8][128] row-block sums of the scan
-constexpr uint32_t M_BAR = RM + 6656;      // mbarrier
-constexpr uint32_t M_TMEM = RM + 6720;     // TMEM base address
-constexpr uint32_t M_FLAG = RM + 6724;     // failure flag
-constexpr uint32_t SMEM_USED = RM + 6784;
+constexpr uint32_t M_EP = RM + 2560;       // f32[128]  exp(P)          (fast)
+constexpr uint32_t M_CL = RM + 3072;       // f32[128]  exp(G_last - P) (fast)
+constexpr uint32_t M_TOT = RM + 3584;      // f32[8][128] row-block sums (wide)
+constexpr uint32_t M_BAR = RM + 7680;      // mbarrier
+constexpr uint32_t M_TMEM = RM + 7744;     // TMEM base address
+constexpr uint32_t M_FLAG = RM + 7748;     // failure flag
+constexpr uint32_t SMEM_USED = RM + 7808;
 constexpr uint32_t PREP_SMEM = SMEM_USED + 1024;  // + alignment slack
 
+constexpr uint32_t RW = 163840;
 // fp32 diagonal 64-blocks of (the strictly lower part of) A, then of its
 // inverse, row stride 68 floats (conflict-free column walks).
 constexpr int DS = 68;
 constexpr uint32_t W_DIAG = RW;                          // 2 x 64 x 68 floats = 34816 B
 constexpr uint32_t W_TMP = RW + 2 * 64 * DS * 4;         // merge temps, up to 8 KB
-// level-3 tiles in region Y (fp16, 64 x 64, 8 KB each)
-constexpr uint32_t YA = RY, YP = RY + 8192, YQ = RY + 16384, YT = RY + 24576;
+
+template <bool FAST>
+struct Map {
+    static constexpr uint32_t LK = 0;
+    static constexpr uint32_t LQ = FAST ? 65536 : 32768;
+    static constexpr uint32_t RR = FAST ? 98304 : 65536;      // R
+    static constexpr uint32_t Y = FAST ? 131072 : 65536;      // merge tiles, then Ainv
+    static constexpr uint32_t B2 = FAST ? 0 : 98304;          // B operand of the WY product (N = 256)
+    static constexpr uint32_t WU = FAST ? 0 : 98304;          // w | u (N = 256)
+    static constexpr uint32_t KGT = FAST ? 98304 : 32768;     // A operand (MN-major) of the Nm | Bc product
+    static constexpr uint32_t QS = FAST ? 65536 : 0;          // Lq (fast) or qg (wide) for the Qe epilogue
+    static constexpr uint32_t YA = Y, YP = Y + 8192, YQ = Y + 16384, YT = Y + 24576;
+};
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -99,6 +133,11 @@ __device__ __forceinline__ uint32_t ldg_u32(const uint16_t* p) {
     return __ldg(reinterpret_cast<const unsigned int*>(p));
 }
 __device__ __forceinline__ float2 ldg_f2(const float* p) { return __ldg(reinterpret_cast<const float2*>(p)); }
+
+__device__ __forceinline__ void unpack8_bf16(const uint4 u, float (&x)[8]) {
+    float2 a = unpack_bf16(u.x), b = unpack_bf16(u.y), c = unpack_bf16(u.z), d = unpack_bf16(u.w);
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y; x[4] = c.x; x[5] = c.y; x[6] = d.x; x[7] = d.y;
+}
 
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -146,23 +185,41 @@ __device__ __forceinline__ void prefetch_chunk(const FwdParams& p, const ChunkRe
     }
 }
 
-// Next non-empty work item at or after `item` (stride gridDim.x).
-__device__ __forceinline__ bool next_item(const FwdParams& p, long long& item, long long nitems, ChunkRef& c,
-                                          int& h) {
-    while (item < nitems) {
-        if (slot_chunk(p, (int)(item / p.H), c)) {
-            h = (int)(item % p.H);
-            return true;
+// Work iteration.  Fast: every (slot, head) item, grid-stride, skipping
+// empty slots.  Wide: the entries of the queue the fast kernel filled.
+template <bool FAST>
+__device__ __forceinline__ bool fetch_item(const FwdParams& p, long long& idx, long long& item, ChunkRef& c,
+                                           int& h) {
+    if (FAST) {
+        const long long nitems = (long long)p.nslots * p.H;
+        while (idx < nitems) {
+            if (slot_chunk(p, (int)(idx / p.H), c)) {
+                item = idx;
+                h = (int)(idx % p.H);
+                return true;
+            }
+            idx += gridDim.x;
         }
-        item += gridDim.x;
+        return false;
+    } else {
+        const long long n = (long long)*reinterpret_cast<volatile uint32_t*>(p.wide_count);
+        while (idx < n) {
+            item = p.wide_list[idx];
+            if (slot_chunk(p, (int)(item / p.H), c)) {
+                h = (int)(item % p.H);
+                return true;
+            }
+            idx += gridDim.x;
+        }
+        return false;
     }
-    return false;
 }
 
 }  // namespace
 
-template <bool L2NORM>
+template <bool L2NORM, bool FAST>
 __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdParams p) {
+    using MP = Map<FAST>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -180,18 +237,18 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     float* sBeta = reinterpret_cast<float*>(sm + M_BETA);
     float* sInvQ = reinterpret_cast<float*>(sm + M_INVQ);
     float* sInvK = reinterpret_cast<float*>(sm + M_INVK);
-    float* sTot = reinterpret_cast<float*>(sm + M_TOT);
+    float* sEP = reinterpret_cast<float*>(sm + M_EP);
+    float* sCL = reinterpret_cast<float*>(sm + M_CL);
     float* Wd = reinterpret_cast<float*>(sm + W_DIAG);
     float* Wt = reinterpret_cast<float*>(sm + W_TMP);
     const uint32_t bar = sbase + M_BAR;
     volatile uint32_t* sFlag = reinterpret_cast<volatile uint32_t*>(sm + M_FLAG);
     uint32_t phase = 0;
 
-    const long long nitems = (long long)p.nslots * H;
-    long long item = blockIdx.x;
+    long long idx = blockIdx.x, item = 0;
     ChunkRef c;
     int h = 0;
-    bool have = next_item(p, item, nitems, c, h);
+    bool have = fetch_item<FAST>(p, idx, item, c, h);
     if (!have) return;                    // uniform: nothing for this CTA
 
     if (warp == 0) {
@@ -209,11 +266,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + M_TMEM);
 
-    // elementwise mapping: d-pair x 16-row block
-    const int d0 = (tid & 63) * 2;
-    const int rb = tid >> 6;
-    const int t0 = rb * 16;
-
     auto wait_mma = [&]() {
         if (!mbar_wait(bar, phase, WAIT_LIMIT)) *sFlag = 1;
         phase ^= 1;
@@ -221,10 +273,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     };
 
     while (have && *sFlag == 0) {
-        long long nxt = item + gridDim.x;
+        long long nidx = idx + gridDim.x, nitem = 0;
         ChunkRef cn;
         int hn = 0;
-        const bool have_n = next_item(p, nxt, nitems, cn, hn);
+        const bool have_n = fetch_item<FAST>(p, nidx, nitem, cn, hn);
         const int len = c.len;
         const size_t row0 = (size_t)c.tok0 * H + h;
 
@@ -265,426 +317,596 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
         }
 
         // ------------------------------------------------------------------
-        // Phase 1: gate prefix sum (log2 units) over the chunk; pivot row 64.
+        // Phase 1: gate prefix sum (log2 units), pivot row 64, gated operands.
         // ------------------------------------------------------------------
-        float G0[16], G1[16];
+        bool unsafe = false;
+        uint32_t kgr[16];   // wide variant: kg held until region 0 is free
+        (void)kgr;
+        if constexpr (FAST) {
+            // thread = 8 consecutive dimensions x 4 consecutive rows
+            const int d8 = (tid & 15) * 8;
+            const int grp = tid >> 4;
+            const int tg0 = grp * 4;
+            float G[4][8];
+            // k, q, v rows are loaded one row ahead of their use (row 0 with
+            // the gate), so each row's loads are in flight before the
+            // previous row's shared-memory stores.
+            uint4 kn = make_uint4(0u, 0u, 0u, 0u), qn = kn, vn = kn;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int t = t0 + r;
-            float2 gv = make_float2(0.f, 0.f);
-            if (t < len) gv = ldg_f2(p.g + (row0 + (size_t)t * H) * KD + d0);
-            G0[r] = gv.x;
-            G1[r] = gv.y;
-        }
-        {
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                a0 += G0[r] * LOG2E;
-                a1 += G1[r] * LOG2E;
-                G0[r] = a0;
-                G1[r] = a1;
-            }
-            sTot[rb * 128 + d0] = a0;
-            sTot[rb * 128 + d0 + 1] = a1;
-        }
-        __syncthreads();
-        {
-            float o0 = 0.f, o1 = 0.f;
-            for (int b2 = 0; b2 < rb; ++b2) {
-                o0 += sTot[b2 * 128 + d0];
-                o1 += sTot[b2 * 128 + d0 + 1];
-            }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                G0[r] += o0;
-                G1[r] += o1;
-            }
-            if (rb == 4) {
-                sG64[d0] = G0[0];
-                sG64[d0 + 1] = G1[0];
-            }
-            if (rb == 7) {
-                sGL[d0] = G0[15];
-                sGL[d0 + 1] = G1[15];
-            }
-        }
-        __syncthreads();
-        const float P0 = sG64[d0], P1 = sG64[d0 + 1];
-        const float eP0 = ex2(P0), eP1 = ex2(P1);
-        const float cL0 = ex2(fminf(sGL[d0] - P0, EXP2_CAP)), cL1 = ex2(fminf(sGL[d0 + 1] - P1, EXP2_CAP));
-
-        // Operands (E = 2^(G-P) <= 2^cap, F = 2^(P-G)):
-        //   Lk = k E, Lq = qs E, R = k F        bf16 K-major [t][d]
-        //   RHS = [beta k exp(G) | beta v]      fp16 MN-major [t][n]
-        //   qg = qs exp(G) stashed in region W (free until phase 2) and
-        //   kg = k exp(G_last-G) kept in registers, until the gated products
-        //   release region X.
-        uint32_t kgr[16];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            asm volatile("" ::: "memory");
-            uint32_t kr[8], qr[8], vr[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int t = t0 + half * 8 + r;
-                kr[r] = qr[r] = vr[r] = 0u;
+            for (int r = 0; r < 4; ++r) {
+                const int t = tg0 + r;
+                float4 ga = make_float4(0.f, 0.f, 0.f, 0.f), gb = ga;
                 if (t < len) {
-                    const size_t off = (row0 + (size_t)t * H) * KD + d0;
-                    kr[r] = ldg_u32(p.k + off);
-                    qr[r] = ldg_u32(p.q + off);
-                    vr[r] = ldg_u32(p.v + off);
+                    const size_t off = (row0 + (size_t)t * H) * KD + d8;
+                    ga = __ldg(reinterpret_cast<const float4*>(p.g + off));
+                    gb = __ldg(reinterpret_cast<const float4*>(p.g + off + 4));
+                    if (r == 0) {
+                        kn = __ldg(reinterpret_cast<const uint4*>(p.k + off));
+                        qn = __ldg(reinterpret_cast<const uint4*>(p.q + off));
+                        vn = __ldg(reinterpret_cast<const uint4*>(p.v + off));
+                    }
+                }
+                G[r][0] = ga.x; G[r][1] = ga.y; G[r][2] = ga.z; G[r][3] = ga.w;
+                G[r][4] = gb.x; G[r][5] = gb.y; G[r][6] = gb.z; G[r][7] = gb.w;
+            }
+            float* tot = reinterpret_cast<float*>(sm + RW);     // [32 groups][128]
+            {
+                float acc[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        acc[j] = fmaf(G[r][j], LOG2E, acc[j]);
+                        G[r][j] = acc[j];
+                    }
+                *reinterpret_cast<float4*>(tot + grp * 128 + d8) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                *reinterpret_cast<float4*>(tot + grp * 128 + d8 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            }
+            __syncthreads();
+            if (tid < 128) {            // exclusive prefix over the 32 row groups
+                float run = 0.f;
+                for (int g2 = 0; g2 < 32; ++g2) {
+                    const float x = tot[g2 * 128 + tid];
+                    tot[g2 * 128 + tid] = run;
+                    run += x;
                 }
             }
+            __syncthreads();
+            {
+                const float4 o0 = *reinterpret_cast<const float4*>(tot + grp * 128 + d8);
+                const float4 o1 = *reinterpret_cast<const float4*>(tot + grp * 128 + d8 + 4);
+                const float off8[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int rr = half * 8 + r;
-                const int t = t0 + rr;
-                float2 kf = unpack_bf16(kr[r]), qf = unpack_bf16(qr[r]), vf = unpack_bf16(vr[r]);
-                const float ik = sInvK[t], iq = sInvQ[t], b = sBeta[t];
-                kf.x *= ik; kf.y *= ik;
-                qf.x *= iq; qf.y *= iq;
-                const float E0 = ex2(fminf(G0[rr] - P0, EXP2_CAP)), E1 = ex2(fminf(G1[rr] - P1, EXP2_CAP));
-                const float F0 = ex2(fminf(P0 - G0[rr], EXP2_CAP)), F1 = ex2(fminf(P1 - G1[rr], EXP2_CAP));
-                const uint32_t off = sw128_off(t, d0, 128);
-                sts_u32(sm, RX + off, pack_bf16(kf.x * E0, kf.y * E1));            // Lk
-                sts_u32(sm, RX + 32768 + off, pack_bf16(qf.x * E0, qf.y * E1));    // Lq
-                sts_u32(sm, RY + off, pack_bf16(kf.x * F0, kf.y * F1));            // R
-                const float eg0 = E0 * eP0, eg1 = E1 * eP1;                      // exp(G_t) <= 1
-                sts_u32(sm, RZ + off, pack_f16(b * kf.x * eg0, b * kf.y * eg1));                 // RHS k
-                sts_u32(sm, RZ + sw128_off(t, 128 + d0, 128), pack_f16(b * vf.x, b * vf.y));     // RHS v
-                sts_u32(sm, RW + off, pack_f16(qf.x * eg0, qf.y * eg1));                         // qg (stash)
-                kgr[rr] = pack_f16(kf.x * F0 * cL0, kf.y * F1 * cL1);
-            }
-        }
-        sync_for_mma();
-        if (tid == 0) {
-            const uint32_t id = idesc_f16(T_BF16, 128, 128, false, false);
-            const Operand Lk{sbase + RX, false, 128}, Lq{sbase + RX + 32768, false, 128}, R{sbase + RY, false, 128};
-            mma_128(tmem + 0, Lk, R, id, 8);     // A_raw  -> cols [0,128)
-            mma_128(tmem + 128, Lq, R, id, 8);   // A2_raw -> cols [128,256)
-            mma_commit(bar);
-        }
-        // the next chunk's rows stream into L2 while this one computes
-        if (have_n) prefetch_chunk(p, cn, hn, tid);
-        wait_mma();
-
-        // ------------------------------------------------------------------
-        // Phase 2: qg, kg to region X; A (strictly lower, times beta_row)
-        // from TMEM: diagonal 64-blocks to fp32 (W), A10 to fp16 (YA).
-        // ------------------------------------------------------------------
+                for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sts_u32(sm, RX + 32768 + sw128_off(t0 + r, d0, 128), kgr[r]);
+                    for (int j = 0; j < 8; ++j) G[r][j] += off8[j];
+                if (grp == 16) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {   // qg: 32 KB from the stash in W to X
-            const uint32_t off = (uint32_t)(tid + i * PREP_THREADS) * 16u;
-            *reinterpret_cast<uint4*>(sm + RX + off) = *reinterpret_cast<const uint4*>(sm + RW + off);
-        }
-        __syncthreads();
-        {
-            const int col0 = cg * 32;
-            // warps whose block lies above the diagonal (row < 64, col >= 64) skip
-            if (!(trow < 64 && col0 >= 64)) {
-                float x[32];
-                tmem_ld32(tmem + lane_off + (uint32_t)col0, x);
-                tmem_ld_wait();
-                const float b = sBeta[trow];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = (col0 + j < trow) ? b * x[j] : 0.f;
-                if (trow >= 64 && col0 < 64) {
-#pragma unroll
-                    for (int j = 0; j < 32; j += 8)
-                        sts_v4(sm, YA + sw128_off(trow - 64, col0 + j, 64), pack_f16(x[j], x[j + 1]),
-                               pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]), pack_f16(x[j + 6], x[j + 7]));
-                } else {
-                    float* dst = Wd + (trow >> 6) * 64 * DS + (trow & 63) * DS + (col0 & 63);
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4*>(dst + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                    for (int j = 0; j < 8; ++j) sG64[d8 + j] = G[0][j];
                 }
-            }
-        }
-        tc_fence_before();
-        __syncthreads();
-
-        // ------------------------------------------------------------------
-        // Phase 3: (I + A)^-1.
-        // Level 0: the eight 16x16 diagonal blocks, one column per thread,
-        // forward substitution (unit diagonal implied; stored parts are
-        // strictly lower, zeros elsewhere).
-        // ------------------------------------------------------------------
-        {
-            float x[16];
-            const int blk = (tid >> 4) & 7, j = tid & 15;
-            float* A0 = Wd + (blk >> 2) * 64 * DS + (blk & 3) * 16 * (DS + 1);
-            if (tid < 128) {
+                if (grp == 31) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float s = 0.f;
-#pragma unroll
-                    for (int m = 0; m < i; ++m) s = fmaf(A0[i * DS + m], x[m], s);
-                    x[i] = (i == j) ? 1.f : (i < j ? 0.f : -s);
+                    for (int j = 0; j < 8; ++j) sGL[d8 + j] = G[3][j];
                 }
             }
             __syncthreads();
             if (tid < 128) {
+                const float P = sG64[tid];
+                sEP[tid] = ex2(P);
+                sCL[tid] = ex2(fminf(sGL[tid] - P, EXP2_CAP));
+            }
+            float P[8];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    if (i > j) A0[i * DS + j] = x[i];
+            for (int j = 0; j < 8; ++j) P[j] = sG64[d8 + j];
+            float m = 0.f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = tg0 + r;
+                const uint4 kc = kn, qc = qn, vc = vn;
+                if (r < 3) {
+                    kn = qn = vn = make_uint4(0u, 0u, 0u, 0u);
+                    if (t + 1 < len) {
+                        const size_t off = (row0 + (size_t)(t + 1) * H) * KD + d8;
+                        kn = __ldg(reinterpret_cast<const uint4*>(p.k + off));
+                        qn = __ldg(reinterpret_cast<const uint4*>(p.q + off));
+                        vn = __ldg(reinterpret_cast<const uint4*>(p.v + off));
+                    }
+                }
+                float kf[8], qf[8], vf[8];
+                unpack8_bf16(kc, kf);
+                unpack8_bf16(qc, qf);
+                unpack8_bf16(vc, vf);
+                const float ik = sInvK[t], iq = sInvQ[t];
+                uint32_t lk[4], lqv[4], rk[4], v16[4];
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {
+                    const float E0 = ex2(fminf(G[r][j] - P[j], EXP2_CAP));
+                    const float E1 = ex2(fminf(G[r][j + 1] - P[j + 1], EXP2_CAP));
+                    const float F0 = ex2(fminf(P[j] - G[r][j], EXP2_CAP));
+                    const float F1 = ex2(fminf(P[j + 1] - G[r][j + 1], EXP2_CAP));
+                    const float k0 = kf[j] * ik, k1 = kf[j + 1] * ik;
+                    const float q0 = qf[j] * iq, q1 = qf[j + 1] * iq;
+                    const float a0 = k0 * E0, a1 = k1 * E1, b0 = q0 * E0, b1 = q1 * E1, c0 = k0 * F0, c1 = k1 * F1;
+                    m = fmaxf(m, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))));
+                    m = fmaxf(m, fmaxf(fmaxf(fabsf(c0), fabsf(c1)), fmaxf(fabsf(vf[j]), fabsf(vf[j + 1]))));
+                    lk[j / 2] = pack_f16(a0, a1);
+                    lqv[j / 2] = pack_f16(b0, b1);
+                    rk[j / 2] = pack_f16(c0, c1);
+                    v16[j / 2] = pack_f16(vf[j], vf[j + 1]);
+                }
+                const uint32_t off = sw128_off(t, d8, 128);
+                sts_v4(sm, MP::LK + off, lk[0], lk[1], lk[2], lk[3]);
+                sts_v4(sm, MP::LK + 32768 + off, v16[0], v16[1], v16[2], v16[3]);
+                sts_v4(sm, MP::LQ + off, lqv[0], lqv[1], lqv[2], lqv[3]);
+                sts_v4(sm, MP::RR + off, rk[0], rk[1], rk[2], rk[3]);
+            }
+            unsafe = !(m <= FP16_SAFE);
+        } else {
+            // thread = dimension pair x 16 consecutive rows
+            const int d0 = (tid & 63) * 2;
+            const int rb = tid >> 6;
+            const int t0 = rb * 16;
+            float* sTot = reinterpret_cast<float*>(sm + M_TOT);
+            float G0[16], G1[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const int t = t0 + r;
+                float2 gv = make_float2(0.f, 0.f);
+                if (t < len) gv = ldg_f2(p.g + (row0 + (size_t)t * H) * KD + d0);
+                G0[r] = gv.x;
+                G1[r] = gv.y;
+            }
+            {
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    a0 += G0[r] * LOG2E;
+                    a1 += G1[r] * LOG2E;
+                    G0[r] = a0;
+                    G1[r] = a1;
+                }
+                sTot[rb * 128 + d0] = a0;
+                sTot[rb * 128 + d0 + 1] = a1;
             }
             __syncthreads();
-        }
-        // Levels 1 and 2 inside each diagonal 64-block:
-        //   inv([[X, 0], [Y, Z]]) = [[Xi, 0], [-Zi Y Xi, Zi]]
-        // T = Y Xi = Y + Y Xs (Xs: stored strictly-lower part of Xi) into a
-        // temp, then -Zi T = -(T + Zs T) in place of Y.
-        {
-            // level 1: 4 merges of 16-blocks (2 per diagonal block), 2 outputs per thread
-            const int m = tid >> 7;
-            const int db = m >> 1;
-            const int C0 = (m & 1) * 32, R0 = C0 + 16;
-            const int li = tid & 127;
-            const int rr = li >> 3, cc = (li & 7) * 2;
-            float* Db = Wd + db * 64 * DS;
-            float* T1 = Wt + m * 256;
-            float t0v = Db[(R0 + rr) * DS + C0 + cc], t1v = Db[(R0 + rr) * DS + C0 + cc + 1];
+            {
+                float o0 = 0.f, o1 = 0.f;
+                for (int b2 = 0; b2 < rb; ++b2) {
+                    o0 += sTot[b2 * 128 + d0];
+                    o1 += sTot[b2 * 128 + d0 + 1];
+                }
 #pragma unroll
-            for (int mm = 0; mm < 16; ++mm) {
-                const float y = Db[(R0 + rr) * DS + C0 + mm];
-                const float2 xs = *reinterpret_cast<const float2*>(Db + (C0 + mm) * DS + C0 + cc);
-                t0v = fmaf(y, xs.x, t0v);
-                t1v = fmaf(y, xs.y, t1v);
+                for (int r = 0; r < 16; ++r) {
+                    G0[r] += o0;
+                    G1[r] += o1;
+                }
+                if (rb == 4) {
+                    sG64[d0] = G0[0];
+                    sG64[d0 + 1] = G1[0];
+                }
+                if (rb == 7) {
+                    sGL[d0] = G0[15];
+                    sGL[d0 + 1] = G1[15];
+                }
             }
-            T1[rr * 16 + cc] = t0v;
-            T1[rr * 16 + cc + 1] = t1v;
             __syncthreads();
-            float l0 = t0v, l1 = t1v;
+            const float P0 = sG64[d0], P1 = sG64[d0 + 1];
+            const float eP0 = ex2(P0), eP1 = ex2(P1);
+            const float cL0 = ex2(fminf(sGL[d0] - P0, EXP2_CAP)), cL1 = ex2(fminf(sGL[d0 + 1] - P1, EXP2_CAP));
+            // Lk, Lq, R bf16; RHS = [beta exp(G) k | beta v] fp16; qg fp16
+            // stashed in region W; kg fp16 in registers.
 #pragma unroll
-            for (int mm = 0; mm < 16; ++mm) {
-                const float z = Db[(R0 + rr) * DS + R0 + mm];    // zero for mm >= rr
-                l0 = fmaf(z, T1[mm * 16 + cc], l0);
-                l1 = fmaf(z, T1[mm * 16 + cc + 1], l1);
+            for (int half = 0; half < 2; ++half) {
+                asm volatile("" ::: "memory");
+                uint32_t kr[8], qr[8], vr[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int t = t0 + half * 8 + r;
+                    kr[r] = qr[r] = vr[r] = 0u;
+                    if (t < len) {
+                        const size_t off = (row0 + (size_t)t * H) * KD + d0;
+                        kr[r] = ldg_u32(p.k + off);
+                        qr[r] = ldg_u32(p.q + off);
+                        vr[r] = ldg_u32(p.v + off);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int rr = half * 8 + r;
+                    const int t = t0 + rr;
+                    float2 kf = unpack_bf16(kr[r]), qf = unpack_bf16(qr[r]), vf = unpack_bf16(vr[r]);
+                    const float ik = sInvK[t], iq = sInvQ[t], b = sBeta[t];
+                    kf.x *= ik; kf.y *= ik;
+                    qf.x *= iq; qf.y *= iq;
+                    const float E0 = ex2(fminf(G0[rr] - P0, EXP2_CAP)), E1 = ex2(fminf(G1[rr] - P1, EXP2_CAP));
+                    const float F0 = ex2(fminf(P0 - G0[rr], EXP2_CAP)), F1 = ex2(fminf(P1 - G1[rr], EXP2_CAP));
+                    const uint32_t off = sw128_off(t, d0, 128);
+                    sts_u32(sm, MP::LK + off, pack_bf16(kf.x * E0, kf.y * E1));
+                    sts_u32(sm, MP::LQ + off, pack_bf16(qf.x * E0, qf.y * E1));
+                    sts_u32(sm, MP::RR + off, pack_bf16(kf.x * F0, kf.y * F1));
+                    const float eg0 = E0 * eP0, eg1 = E1 * eP1;                      // exp(G_t) <= 1
+                    sts_u32(sm, MP::B2 + off, pack_f16(b * kf.x * eg0, b * kf.y * eg1));
+                    sts_u32(sm, MP::B2 + sw128_off(t, 128 + d0, 128), pack_f16(b * vf.x, b * vf.y));
+                    sts_u32(sm, RW + off, pack_f16(qf.x * eg0, qf.y * eg1));        // qg stash
+                    kgr[rr] = pack_f16(kf.x * F0 * cL0, kf.y * F1 * cL1);
+                }
             }
-            Db[(R0 + rr) * DS + C0 + cc] = -l0;
-            Db[(R0 + rr) * DS + C0 + cc + 1] = -l1;
         }
-        __syncthreads();
-        {
-            // level 2: 2 merges of 32-blocks (one per diagonal block), 4 outputs per thread
-            const int db = tid >> 8;
-            const int li = tid & 255;
-            const int rr = li >> 3, cc = (li & 7) * 4;
-            float* Db = Wd + db * 64 * DS;
-            float* T2 = Wt + db * 1024;
-            float4 t = *reinterpret_cast<const float4*>(Db + (32 + rr) * DS + cc);
-#pragma unroll
-            for (int mm = 0; mm < 32; ++mm) {
-                const float y = Db[(32 + rr) * DS + mm];
-                const float4 xs = *reinterpret_cast<const float4*>(Db + mm * DS + cc);
-                t.x = fmaf(y, xs.x, t.x);
-                t.y = fmaf(y, xs.y, t.y);
-                t.z = fmaf(y, xs.z, t.z);
-                t.w = fmaf(y, xs.w, t.w);
+        // The fast variant hands chunks it cannot hold in fp16 to the wide one.
+        if (FAST && __syncthreads_or(unsafe)) {
+            if (tid == 0) {
+                const uint32_t slot_i = atomicAdd(p.wide_count, 1u);
+                p.wide_list[slot_i] = (int32_t)item;
             }
-            *reinterpret_cast<float4*>(T2 + rr * 32 + cc) = t;
+            if (have_n) prefetch_chunk(p, cn, hn, tid);
             __syncthreads();
-            float4 l = t;
-#pragma unroll
-            for (int mm = 0; mm < 32; ++mm) {
-                const float z = Db[(32 + rr) * DS + 32 + mm];    // zero for mm >= rr
-                const float4 tv = *reinterpret_cast<const float4*>(T2 + mm * 32 + cc);
-                l.x = fmaf(z, tv.x, l.x);
-                l.y = fmaf(z, tv.y, l.y);
-                l.z = fmaf(z, tv.z, l.z);
-                l.w = fmaf(z, tv.w, l.w);
+        } else {
+            sync_for_mma();
+            if (tid == 0) {
+                const uint32_t id = idesc_f16(FAST ? T_F16 : T_BF16, 128, 128, false, false);
+                const Operand Lk{sbase + MP::LK, false, 128}, Lq{sbase + MP::LQ, false, 128},
+                    R{sbase + MP::RR, false, 128};
+                mma_128(tmem + 0, Lk, R, id, 8);     // A_raw  -> cols [0,128)
+                mma_128(tmem + 128, Lq, R, id, 8);   // A2_raw -> cols [128,256)
+                mma_commit(bar);
             }
-            *reinterpret_cast<float4*>(Db + (32 + rr) * DS + cc) = make_float4(-l.x, -l.y, -l.z, -l.w);
-        }
-        __syncthreads();
-        // Level 3 on tensor cores: L = -Q (A10 P), P / Q the inverses of the
-        // two diagonal 64-blocks.  fp16 tiles in region Y: A10 [r][m] K-major
-        // (written in phase 2; rows 64..127 of the M=128 MMA read the next
-        // tile and land in TMEM lanes never read), P [m][c] MN-major,
-        // Q [r'][r] K-major, T [r][c] MN-major.
-        for (int idx = tid; idx < 64 * 32; idx += PREP_THREADS) {
-            const int r = idx >> 5, c2 = (idx & 31) * 2;
-            const float* P = Wd + r * DS + c2;
-            const float* Q = Wd + 64 * DS + r * DS + c2;
-            sts_u32(sm, YP + sw128_off(r, c2, 64),
-                    pack_f16(P[0] + (r == c2 ? 1.f : 0.f), P[1] + (r == c2 + 1 ? 1.f : 0.f)));
-            sts_u32(sm, YQ + sw128_off(r, c2, 64),
-                    pack_f16(Q[0] + (r == c2 ? 1.f : 0.f), Q[1] + (r == c2 + 1 ? 1.f : 0.f)));
-        }
-        sync_for_mma();
-        if (tid == 0) {
-            const Operand A10{sbase + YA, false, 64}, Ph{sbase + YP, true, 64};
-            mma_128(tmem + 0, A10, Ph, idesc_f16(T_F16, 128, 64, false, true), 4);   // T -> cols [0,64)
-            mma_commit(bar);
-        }
-        wait_mma();
-        if (lq < 2) {
-            float x[16];
-            tmem_ld16(tmem + lane_off + (uint32_t)(cg * 16), x);
-            tmem_ld_wait();
+            // the next chunk's rows stream into L2 while this one computes
+            if (have_n) prefetch_chunk(p, cn, hn, tid);
+            wait_mma();
+
+            // --------------------------------------------------------------
+            // Phase 2: A (strictly lower, times beta_row) from TMEM: diagonal
+            // 64-blocks to fp32 (W), A10 to fp16 (YA).  The wide variant
+            // first moves kg and qg into region 0.
+            // --------------------------------------------------------------
+            if constexpr (!FAST) {
+                const int d0 = (tid & 63) * 2;
+                const int t0 = (tid >> 6) * 16;
 #pragma unroll
-            for (int j = 0; j < 16; j += 8)
-                sts_v4(sm, YT + sw128_off(trow, cg * 16 + j, 64), pack_f16(x[j], x[j + 1]),
-                       pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]), pack_f16(x[j + 6], x[j + 7]));
-        }
-        sync_for_mma();
-        if (tid == 0) {
-            const Operand Qh{sbase + YQ, false, 64}, Th{sbase + YT, true, 64};
-            mma_128(tmem + 64, Qh, Th, idesc_f16(T_F16, 128, 64, false, true, /*neg_a=*/true), 4);  // L -> [64,128)
-            mma_commit(bar);
-        }
-        wait_mma();
-        // Assemble (I + A)^-1 as fp16, K-major [c][i], in region Y:
-        //   rows 0..63:  [P | 0],   rows 64..127: [L | Q]   (unit diagonal)
-        if (lq < 2) {
-            float x[16];
-            tmem_ld16(tmem + lane_off + 64u + (uint32_t)(cg * 16), x);
-            tmem_ld_wait();
+                for (int r = 0; r < 16; ++r) sts_u32(sm, 32768 + sw128_off(t0 + r, d0, 128), kgr[r]);
 #pragma unroll
-            for (int j = 0; j < 16; j += 8)
-                sts_v4(sm, RY + sw128_off(64 + trow, cg * 16 + j, 128), pack_f16(x[j], x[j + 1]),
-                       pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]), pack_f16(x[j + 6], x[j + 7]));
-        }
-        for (int ch = tid; ch < 1536; ch += PREP_THREADS) {
-            int r, c0;
-            if (ch < 1024) {            // rows 0..63: P (cols 0..63), zeros (cols 64..127)
-                r = ch >> 4;
-                c0 = (ch & 15) * 8;
-            } else {                    // rows 64..127: Q (cols 64..127)
-                r = 64 + ((ch - 1024) >> 3);
-                c0 = 64 + ((ch - 1024) & 7) * 8;
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t off = (uint32_t)(tid + i * PREP_THREADS) * 16u;
+                    *reinterpret_cast<uint4*>(sm + off) = *reinterpret_cast<const uint4*>(sm + RW + off);
+                }
+                __syncthreads();
             }
-            float x[8];
-            if (r < 64 && c0 >= 64) {
+            {
+                const int col0 = cg * 32;
+                // warps whose block lies above the diagonal (row < 64, col >= 64) skip
+                if (!(trow < 64 && col0 >= 64)) {
+                    float x[32];
+                    tmem_ld32(tmem + lane_off + (uint32_t)col0, x);
+                    tmem_ld_wait();
+                    const float b = sBeta[trow];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = 0.f;
-            } else {
-                const float* src = Wd + (r >> 6) * 64 * DS + (r & 63) * DS + (c0 & 63);
-                const float4 a = *reinterpret_cast<const float4*>(src), b = *reinterpret_cast<const float4*>(src + 4);
-                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] += (c0 + e == r) ? 1.f : 0.f;
-            }
-            sts_v4(sm, RY + sw128_off(r, c0, 128), pack_f16(x[0], x[1]), pack_f16(x[2], x[3]), pack_f16(x[4], x[5]),
-                   pack_f16(x[6], x[7]));
-        }
-        sync_for_mma();
-
-        // ------------------------------------------------------------------
-        // Phase 4: [w | u] = Ainv [beta exp(G) k | beta v]  (M=128, N=256)
-        // ------------------------------------------------------------------
-        if (tid == 0) {
-            const Operand Ai{sbase + RY, false, 128}, Rh{sbase + RZ, true, 128};
-            mma_128(tmem + 256, Ai, Rh, idesc_f16(T_F16, 128, 256, false, true), 8);
-            mma_commit(bar);
-        }
-        // Meanwhile: A2 (inclusive lower) from TMEM [128,256) to fp16 K-major
-        // [t][i] in region W (the fp32 blocks are no longer needed).
-        {
-            float x[32];
-            const int col0 = cg * 32;
-            tmem_ld32(tmem + lane_off + 128u + (uint32_t)col0, x);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = (col0 + j <= trow) ? x[j] : 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; j += 8)
-                sts_v4(sm, RW + sw128_off(trow, col0 + j, 128), pack_f16(x[j], x[j + 1]), pack_f16(x[j + 2], x[j + 3]),
-                       pack_f16(x[j + 4], x[j + 5]), pack_f16(x[j + 6], x[j + 7]));
-        }
-        wait_mma();
-        // Phase 5: w | u from TMEM [256,512) to fp16 MN-major [t][n] in Z.
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            float x[32];
-            const int col0 = cg * 64 + part * 32;
-            tmem_ld32(tmem + lane_off + 256u + (uint32_t)col0, x);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; j += 8)
-                sts_v4(sm, RZ + sw128_off(trow, col0 + j, 128), pack_f16(x[j], x[j + 1]), pack_f16(x[j + 2], x[j + 3]),
-                       pack_f16(x[j + 4], x[j + 5]), pack_f16(x[j + 6], x[j + 7]));
-        }
-        sync_for_mma();
-
-        // ------------------------------------------------------------------
-        // Phase 6: [kg^T w | kg^T u] -> [0,256);  [A2 w | A2 u] -> [256,512)
-        // ------------------------------------------------------------------
-        if (tid == 0) {
-            const Operand KgT{sbase + RX + 32768, true, 128}, A2h{sbase + RW, false, 128}, WU{sbase + RZ, true, 128};
-            mma_128(tmem + 0, KgT, WU, idesc_f16(T_F16, 128, 256, true, true), 8);
-            mma_128(tmem + 256, A2h, WU, idesc_f16(T_F16, 128, 256, false, true), 8);
-            mma_commit(bar);
-        }
-        wait_mma();
-
-        // ------------------------------------------------------------------
-        // Phase 7: epilogue, straight from TMEM to the workspace tile.
-        //   warps 0-7:  lanes = d;  Nm = -(kg^T w), Bc = kg^T u
-        //   warps 8-15: lanes = t;  Qe = qg - A2 w, Oi = A2 u
-        // ------------------------------------------------------------------
-        {
-            uint8_t* dst = tile_ptr(p, c.slot, h);
-            const bool second = warp >= 8;
-            const int half = (warp >> 2) & 1;     // which 128 columns of the 256
-#pragma unroll 1
-            for (int part = 0; part < 4; ++part) {
-                float x[32];
-                const int col0 = half * 128 + part * 32;
-                tmem_ld32(tmem + lane_off + (second ? 256u : 0u) + (uint32_t)col0, x);
-                tmem_ld_wait();
-                if (!second) {
-                    if (half == 0) {
+                    for (int j = 0; j < 32; ++j) x[j] = (col0 + j < trow) ? b * x[j] : 0.f;
+                    if (trow >= 64 && col0 < 64) {
 #pragma unroll
                         for (int j = 0; j < 32; j += 8)
-                            stg_v4(dst, TILE_NM + sw128_off(trow, col0 + j, 128), pack_f16(-x[j], -x[j + 1]),
-                                   pack_f16(-x[j + 2], -x[j + 3]), pack_f16(-x[j + 4], -x[j + 5]),
-                                   pack_f16(-x[j + 6], -x[j + 7]));
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 8)
-                            stg_v4(dst, TILE_BC + part * BC_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
+                            sts_v4(sm, MP::YA + sw128_off(trow - 64, col0 + j, 64), pack_f16(x[j], x[j + 1]),
                                    pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]),
                                    pack_f16(x[j + 6], x[j + 7]));
-                    }
-                } else {
-                    if (half == 0) {
+                    } else {
+                        float* dst = Wd + (trow >> 6) * 64 * DS + (trow & 63) * DS + (col0 & 63);
 #pragma unroll
-                        for (int j = 0; j < 32; j += 8) {
-                            const uint4 qv = *reinterpret_cast<const uint4*>(sm + RX + sw128_off(trow, col0 + j, 128));
-                            const float2 g0 = unpack_f16(qv.x), g1 = unpack_f16(qv.y), g2 = unpack_f16(qv.z),
-                                         g3 = unpack_f16(qv.w);
-                            stg_v4(dst, TILE_QE + sw128_off(trow, col0 + j, 128), pack_f16(g0.x - x[j], g0.y - x[j + 1]),
-                                   pack_f16(g1.x - x[j + 2], g1.y - x[j + 3]), pack_f16(g2.x - x[j + 4], g2.y - x[j + 5]),
-                                   pack_f16(g3.x - x[j + 6], g3.y - x[j + 7]));
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4*>(dst + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncthreads();
+
+            // --------------------------------------------------------------
+            // Phase 3: (I + A)^-1.
+            // Level 0: the eight 16x16 diagonal blocks, one column per
+            // thread, forward substitution (unit diagonal implied; stored
+            // parts are strictly lower, zeros elsewhere).
+            // --------------------------------------------------------------
+            {
+                float x[16];
+                const int blk = (tid >> 4) & 7, j = tid & 15;
+                float* A0 = Wd + (blk >> 2) * 64 * DS + (blk & 3) * 16 * (DS + 1);
+                if (tid < 128) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float s = 0.f;
+#pragma unroll
+                        for (int mm = 0; mm < i; ++mm) s = fmaf(A0[i * DS + mm], x[mm], s);
+                        x[i] = (i == j) ? 1.f : (i < j ? 0.f : -s);
+                    }
+                }
+                __syncthreads();
+                if (tid < 128) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (i > j) A0[i * DS + j] = x[i];
+                }
+                __syncthreads();
+            }
+            // Levels 1 and 2 inside each diagonal 64-block:
+            //   inv([[X, 0], [Y, Z]]) = [[Xi, 0], [-Zi Y Xi, Zi]]
+            // T = Y Xi = Y + Y Xs (Xs: stored strictly-lower part of Xi) into
+            // a temp, then -Zi T = -(T + Zs T) in place of Y.
+            {
+                // level 1: 4 merges of 16-blocks (2 per diagonal block), 2 outputs per thread
+                const int mg = tid >> 7;
+                const int db = mg >> 1;
+                const int C0 = (mg & 1) * 32, R0 = C0 + 16;
+                const int li = tid & 127;
+                const int rr = li >> 3, cc = (li & 7) * 2;
+                float* Db = Wd + db * 64 * DS;
+                float* T1 = Wt + mg * 256;
+                float t0v = Db[(R0 + rr) * DS + C0 + cc], t1v = Db[(R0 + rr) * DS + C0 + cc + 1];
+#pragma unroll
+                for (int mm = 0; mm < 16; ++mm) {
+                    const float y = Db[(R0 + rr) * DS + C0 + mm];
+                    const float2 xs = *reinterpret_cast<const float2*>(Db + (C0 + mm) * DS + C0 + cc);
+                    t0v = fmaf(y, xs.x, t0v);
+                    t1v = fmaf(y, xs.y, t1v);
+                }
+                T1[rr * 16 + cc] = t0v;
+                T1[rr * 16 + cc + 1] = t1v;
+                __syncthreads();
+                float l0 = t0v, l1 = t1v;
+#pragma unroll
+                for (int mm = 0; mm < 16; ++mm) {
+                    const float z = Db[(R0 + rr) * DS + R0 + mm];    // zero for mm >= rr
+                    l0 = fmaf(z, T1[mm * 16 + cc], l0);
+                    l1 = fmaf(z, T1[mm * 16 + cc + 1], l1);
+                }
+                Db[(R0 + rr) * DS + C0 + cc] = -l0;
+                Db[(R0 + rr) * DS + C0 + cc + 1] = -l1;
+            }
+            __syncthreads();
+            {
+                // level 2: 2 merges of 32-blocks (one per diagonal block), 4 outputs per thread
+                const int db = tid >> 8;
+                const int li = tid & 255;
+                const int rr = li >> 3, cc = (li & 7) * 4;
+                float* Db = Wd + db * 64 * DS;
+                float* T2 = Wt + db * 1024;
+                float4 t = *reinterpret_cast<const float4*>(Db + (32 + rr) * DS + cc);
+#pragma unroll
+                for (int mm = 0; mm < 32; ++mm) {
+                    const float y = Db[(32 + rr) * DS + mm];
+                    const float4 xs = *reinterpret_cast<const float4*>(Db + mm * DS + cc);
+                    t.x = fmaf(y, xs.x, t.x);
+                    t.y = fmaf(y, xs.y, t.y);
+                    t.z = fmaf(y, xs.z, t.z);
+                    t.w = fmaf(y, xs.w, t.w);
+                }
+                *reinterpret_cast<float4*>(T2 + rr * 32 + cc) = t;
+                __syncthreads();
+                float4 l = t;
+#pragma unroll
+                for (int mm = 0; mm < 32; ++mm) {
+                    const float z = Db[(32 + rr) * DS + 32 + mm];    // zero for mm >= rr
+                    const float4 tv = *reinterpret_cast<const float4*>(T2 + mm * 32 + cc);
+                    l.x = fmaf(z, tv.x, l.x);
+                    l.y = fmaf(z, tv.y, l.y);
+                    l.z = fmaf(z, tv.z, l.z);
+                    l.w = fmaf(z, tv.w, l.w);
+                }
+                *reinterpret_cast<float4*>(Db + (32 + rr) * DS + cc) = make_float4(-l.x, -l.y, -l.z, -l.w);
+            }
+            __syncthreads();
+            // Level 3 on tensor cores: L = -Q (A10 P), P / Q the inverses of
+            // the two diagonal 64-blocks.  fp16 tiles: A10 [r][m] K-major
+            // (written in phase 2; rows 64..127 of the M=128 MMA read the
+            // next tile and land in TMEM lanes never read), P [m][c]
+            // MN-major, Q [r'][r] K-major, T [r][c] MN-major.
+            for (int e = tid; e < 64 * 32; e += PREP_THREADS) {
+                const int r = e >> 5, c2 = (e & 31) * 2;
+                const float* Pp = Wd + r * DS + c2;
+                const float* Qp = Wd + 64 * DS + r * DS + c2;
+                sts_u32(sm, MP::YP + sw128_off(r, c2, 64),
+                        pack_f16(Pp[0] + (r == c2 ? 1.f : 0.f), Pp[1] + (r == c2 + 1 ? 1.f : 0.f)));
+                sts_u32(sm, MP::YQ + sw128_off(r, c2, 64),
+                        pack_f16(Qp[0] + (r == c2 ? 1.f : 0.f), Qp[1] + (r == c2 + 1 ? 1.f : 0.f)));
+            }
+            sync_for_mma();
+            if (tid == 0) {
+                const Operand A10{sbase + MP::YA, false, 64}, Ph{sbase + MP::YP, true, 64};
+                mma_128(tmem + 0, A10, Ph, idesc_f16(T_F16, 128, 64, false, true), 4);   // T -> cols [0,64)
+                mma_commit(bar);
+            }
+            wait_mma();
+            if (lq < 2) {
+                float x[16];
+                tmem_ld16(tmem + lane_off + (uint32_t)(cg * 16), x);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; j += 8)
+                    sts_v4(sm, MP::YT + sw128_off(trow, cg * 16 + j, 64), pack_f16(x[j], x[j + 1]),
+                           pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]), pack_f16(x[j + 6], x[j + 7]));
+            }
+            sync_for_mma();
+            if (tid == 0) {
+                const Operand Qh{sbase + MP::YQ, false, 64}, Th{sbase + MP::YT, true, 64};
+                mma_128(tmem + 64, Qh, Th, idesc_f16(T_F16, 128, 64, false, true, /*neg_a=*/true), 4);  // L
+                mma_commit(bar);
+            }
+            wait_mma();
+            // Assemble (I + A)^-1 as fp16, K-major [c][i], in region Y:
+            //   rows 0..63:  [P | 0],   rows 64..127: [L | Q]   (unit diagonal)
+            // The fast variant folds diag(beta) into its columns.
+            if (lq < 2) {
+                float x[16];
+                tmem_ld16(tmem + lane_off + 64u + (uint32_t)(cg * 16), x);
+                tmem_ld_wait();
+                if (FAST) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) x[j] *= sBeta[cg * 16 + j];
+                }
+#pragma unroll
+                for (int j = 0; j < 16; j += 8)
+                    sts_v4(sm, MP::Y + sw128_off(64 + trow, cg * 16 + j, 128), pack_f16(x[j], x[j + 1]),
+                           pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]), pack_f16(x[j + 6], x[j + 7]));
+            }
+            for (int ch = tid; ch < 1536; ch += PREP_THREADS) {
+                int r, c0;
+                if (ch < 1024) {            // rows 0..63: P (cols 0..63), zeros (cols 64..127)
+                    r = ch >> 4;
+                    c0 = (ch & 15) * 8;
+                } else {                    // rows 64..127: Q (cols 64..127)
+                    r = 64 + ((ch - 1024) >> 3);
+                    c0 = 64 + ((ch - 1024) & 7) * 8;
+                }
+                float x[8];
+                if (r < 64 && c0 >= 64) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = 0.f;
+                } else {
+                    const float* src = Wd + (r >> 6) * 64 * DS + (r & 63) * DS + (c0 & 63);
+                    const float4 a = *reinterpret_cast<const float4*>(src), b = *reinterpret_cast<const float4*>(src + 4);
+                    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        x[e] += (c0 + e == r) ? 1.f : 0.f;
+                        if (FAST) x[e] *= sBeta[c0 + e];
+                    }
+                }
+                sts_v4(sm, MP::Y + sw128_off(r, c0, 128), pack_f16(x[0], x[1]), pack_f16(x[2], x[3]),
+                       pack_f16(x[4], x[5]), pack_f16(x[6], x[7]));
+            }
+            sync_for_mma();
+
+            // --------------------------------------------------------------
+            // Phase 4: WY product (M=128, N=256, K=128) into TMEM [256,512):
+            //   fast: Ainv diag(beta) [Lk | v]     (w still lacks diag(exp(P)))
+            //   wide: Ainv [beta exp(G) k | beta v]
+            // --------------------------------------------------------------
+            if (tid == 0) {
+                const Operand Ai{sbase + MP::Y, false, 128}, Rh{sbase + MP::B2, true, 128};
+                mma_128(tmem + 256, Ai, Rh, idesc_f16(T_F16, 128, 256, false, true), 8);
+                mma_commit(bar);
+            }
+            // Meanwhile: A2 (inclusive lower) from TMEM [128,256) to fp16
+            // K-major [t][i] in region W (the fp32 blocks are no longer needed).
+            {
+                float x[32];
+                const int col0 = cg * 32;
+                tmem_ld32(tmem + lane_off + 128u + (uint32_t)col0, x);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = (col0 + j <= trow) ? x[j] : 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; j += 8)
+                    sts_v4(sm, RW + sw128_off(trow, col0 + j, 128), pack_f16(x[j], x[j + 1]), pack_f16(x[j + 2], x[j + 3]),
+                           pack_f16(x[j + 4], x[j + 5]), pack_f16(x[j + 6], x[j + 7]));
+            }
+            wait_mma();
+            // Phase 5: w | u from TMEM [256,512) to fp16 MN-major [t][n]
+            // (fast: w columns scaled by exp(P)).
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                float x[32];
+                const int col0 = cg * 64 + part * 32;
+                tmem_ld32(tmem + lane_off + 256u + (uint32_t)col0, x);
+                tmem_ld_wait();
+                if (FAST && col0 < 128) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) x[j] *= sEP[col0 + j];
+                }
+#pragma unroll
+                for (int j = 0; j < 32; j += 8)
+                    sts_v4(sm, MP::WU + sw128_off(trow, col0 + j, 128), pack_f16(x[j], x[j + 1]),
+                           pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]), pack_f16(x[j + 6], x[j + 7]));
+            }
+            sync_for_mma();
+
+            // --------------------------------------------------------------
+            // Phase 6: [X^T w | X^T u] -> [0,256) with X = R (fast) or kg
+            // (wide);  [A2 w | A2 u] -> [256,512)
+            // --------------------------------------------------------------
+            if (tid == 0) {
+                const Operand KgT{sbase + MP::KGT, true, 128}, A2h{sbase + RW, false, 128},
+                    WU{sbase + MP::WU, true, 128};
+                mma_128(tmem + 0, KgT, WU, idesc_f16(T_F16, 128, 256, true, true), 8);
+                mma_128(tmem + 256, A2h, WU, idesc_f16(T_F16, 128, 256, false, true), 8);
+                mma_commit(bar);
+            }
+            wait_mma();
+
+            // --------------------------------------------------------------
+            // Phase 7: epilogue, straight from TMEM to the workspace tile.
+            //   warps 0-7:  lanes = d;  Nm = -cL (X^T w), Bc = cL X^T u
+            //               (cL = exp(G_last - P) for the fast variant, else 1)
+            //   warps 8-15: lanes = t;  Qe = qg - A2 w, Oi = A2 u
+            //               (fast: qg = Lq diag(exp(P)))
+            // --------------------------------------------------------------
+            {
+                uint8_t* dst = tile_ptr(p, c.slot, h);
+                const bool second = warp >= 8;
+                const int half = (warp >> 2) & 1;     // which 128 columns of the 256
+                const float rs = (FAST && !second) ? sCL[trow] : 1.f;
+#pragma unroll 1
+                for (int part = 0; part < 4; ++part) {
+                    float x[32];
+                    const int col0 = half * 128 + part * 32;
+                    tmem_ld32(tmem + lane_off + (second ? 256u : 0u) + (uint32_t)col0, x);
+                    tmem_ld_wait();
+                    if (!second) {
+                        if (half == 0) {
+                            const float ns = -rs;
+#pragma unroll
+                            for (int j = 0; j < 32; j += 8)
+                                stg_v4(dst, TILE_NM + sw128_off(trow, col0 + j, 128), pack_f16(ns * x[j], ns * x[j + 1]),
+                                       pack_f16(ns * x[j + 2], ns * x[j + 3]), pack_f16(ns * x[j + 4], ns * x[j + 5]),
+                                       pack_f16(ns * x[j + 6], ns * x[j + 7]));
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 8)
+                                stg_v4(dst, TILE_BC + part * BC_PIECE + sw64_off(trow, j), pack_f16(rs * x[j], rs * x[j + 1]),
+                                       pack_f16(rs * x[j + 2], rs * x[j + 3]), pack_f16(rs * x[j + 4], rs * x[j + 5]),
+                                       pack_f16(rs * x[j + 6], rs * x[j + 7]));
                         }
                     } else {
+                        if (half == 0) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 8)
-                            stg_v4(dst, TILE_OI + part * OI_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
-                                   pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]),
-                                   pack_f16(x[j + 6], x[j + 7]));
+                            for (int j = 0; j < 32; j += 8) {
+                                const uint4 qv = *reinterpret_cast<const uint4*>(sm + MP::QS + sw128_off(trow, col0 + j, 128));
+                                float2 g0 = unpack_f16(qv.x), g1 = unpack_f16(qv.y), g2 = unpack_f16(qv.z),
+                                       g3 = unpack_f16(qv.w);
+                                if (FAST) {
+                                    const float4 e0 = *reinterpret_cast<const float4*>(sEP + col0 + j);
+                                    const float4 e1 = *reinterpret_cast<const float4*>(sEP + col0 + j + 4);
+                                    g0.x *= e0.x; g0.y *= e0.y; g1.x *= e0.z; g1.y *= e0.w;
+                                    g2.x *= e1.x; g2.y *= e1.y; g3.x *= e1.z; g3.y *= e1.w;
+                                }
+                                stg_v4(dst, TILE_QE + sw128_off(trow, col0 + j, 128), pack_f16(g0.x - x[j], g0.y - x[j + 1]),
+                                       pack_f16(g1.x - x[j + 2], g1.y - x[j + 3]), pack_f16(g2.x - x[j + 4], g2.y - x[j + 5]),
+                                       pack_f16(g3.x - x[j + 6], g3.y - x[j + 7]));
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; j += 8)
+                                stg_v4(dst, TILE_OI + part * OI_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
+                                       pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]),
+                                       pack_f16(x[j + 6], x[j + 7]));
+                        }
                     }
                 }
+                if (tid < 32) {
+                    float4 dg;
+                    dg.x = ex2(sGL[tid * 4 + 0]);
+                    dg.y = ex2(sGL[tid * 4 + 1]);
+                    dg.z = ex2(sGL[tid * 4 + 2]);
+                    dg.w = ex2(sGL[tid * 4 + 3]);
+                    *reinterpret_cast<float4*>(dst + TILE_DG + tid * 16) = dg;
+                }
             }
-            if (tid < 32) {
-                float4 dg;
-                dg.x = ex2(sGL[tid * 4 + 0]);
-                dg.y = ex2(sGL[tid * 4 + 1]);
-                dg.z = ex2(sGL[tid * 4 + 2]);
-                dg.w = ex2(sGL[tid * 4 + 3]);
-                *reinterpret_cast<float4*>(dst + TILE_DG + tid * 16) = dg;
-            }
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
         }
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
 
-        item = nxt;
+        idx = nidx;
+        item = nitem;
         c = cn;
         h = hn;
         have = have_n;
@@ -695,7 +917,18 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// Host-side launcher: one persistent CTA per SM (fewer if there is less work).
+template <bool L2NORM, bool FAST>
+static cudaError_t launch_one(const FwdParams& p, unsigned grid, cudaStream_t stream) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kda_prep_kernel<L2NORM, FAST>, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
+    if (e != cudaSuccess) return e;
+    kda_prep_kernel<L2NORM, FAST><<<grid, PREP_THREADS, PREP_SMEM, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// Host-side launcher: the fast variant over every work item, then the wide
+// variant over whatever the fast one queued (usually nothing; its CTAs then
+// exit at once).  One persistent CTA per SM, fewer if there is less work.
 cudaError_t launch_prep(const FwdParams& p, bool l2norm, cudaStream_t stream) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -705,16 +938,9 @@ cudaError_t launch_prep(const FwdParams& p, bool l2norm, cudaStream_t stream) {
     const long long items = (long long)p.nslots * p.H;
     const unsigned grid = (unsigned)(items < sms ? items : sms);
     if (grid == 0) return cudaSuccess;
-    if (l2norm) {
-        e = cudaFuncSetAttribute(kda_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
-        if (e != cudaSuccess) return e;
-        kda_prep_kernel<true><<<grid, PREP_THREADS, PREP_SMEM, stream>>>(p);
-    } else {
-        e = cudaFuncSetAttribute(kda_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
-        if (e != cudaSuccess) return e;
-        kda_prep_kernel<false><<<grid, PREP_THREADS, PREP_SMEM, stream>>>(p);
-    }
-    return cudaGetLastError();
+    e = l2norm ? launch_one<true, true>(p, grid, stream) : launch_one<false, true>(p, grid, stream);
+    if (e != cudaSuccess) return e;
+    return l2norm ? launch_one<true, false>(p, grid, stream) : launch_one<false, false>(p, grid, stream);
 }
 
 }  // namespace kda

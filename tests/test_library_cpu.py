@@ -32,9 +32,9 @@ def test_workspace_bytes():
     lib = binding.load_library()
     tile = 131584
     # fixed length: B * T/128 slots; varlen bound: T/128 + N + 1
-    assert lib.kda_fwd_workspace_bytes(1, 65536, 32, 128, 128, 1) == 256 + 514 * 32 * tile
-    assert lib.kda_fwd_workspace_bytes(4, 8192, 16, 128, 128, 4) == 256 + 256 * 16 * tile
-    assert lib.kda_fwd_workspace_bytes(1, 9192, 32, 128, 128, 6) == 256 + 78 * 32 * tile
+    assert lib.kda_fwd_workspace_bytes(1, 65536, 32, 128, 128, 1) == 256 + ((514 * 32 * 4 + 255) // 256) * 256 + 514 * 32 * tile
+    assert lib.kda_fwd_workspace_bytes(4, 8192, 16, 128, 128, 4) == 256 + ((256 * 16 * 4 + 255) // 256) * 256 + 256 * 16 * tile
+    assert lib.kda_fwd_workspace_bytes(1, 9192, 32, 128, 128, 6) == 256 + ((78 * 32 * 4 + 255) // 256) * 256 + 78 * 32 * tile
     assert lib.kda_fwd_workspace_bytes(1, 256, 1, 64, 128, 1) == 0
 
 
