@@ -93,6 +93,11 @@ struct Map {
     static constexpr uint32_t KGT = FAST ? 98304 : 32768;     // A operand (MN-major) of the Nm | Bc product
     static constexpr uint32_t QS = FAST ? 65536 : 0;          // Lq (fast) or qg (wide) for the Qe epilogue
     static constexpr uint32_t YA = Y, YP = Y + 8192, YQ = Y + 16384, YT = Y + 24576;
+    // staging of the output tile for the bulk store (regions free by then)
+    static constexpr uint32_t ST_NM = FAST ? 0 : 65536;
+    static constexpr uint32_t ST_BC = 32768;
+    static constexpr uint32_t ST_QE = FAST ? 131072 : 98304;
+    static constexpr uint32_t ST_OI = FAST ? 98304 : 131072;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -139,6 +144,69 @@ __device__ __forceinline__ void unpack8_bf16(const uint4 u, float (&x)[8]) {
     x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y; x[4] = c.x; x[5] = c.y; x[6] = d.x; x[7] = d.y;
 }
 
+// Warp-level tf32 tensor-core product D += A B (m16n8k8, fp32 accumulate),
+// used for the small 16x16 / 32x32 merges of the inverse.  Fragments:
+// g = lane / 4, t = lane % 4;  A: (g, t) (g+8, t) (g, t+4) (g+8, t+4);
+// B: (k = t, n = g) (k = t+4, n = g);  D: (g, 2t) (g, 2t+1) (g+8, 2t) (g+8, 2t+1).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One 16 x 16 output tile of  C + A B  with A = rows [ar, ar+16) x cols
+// [ac, ac+K) and B = rows [br, br+K) x cols [bc, bc+16) of fp32 matrices in
+// shared memory (row strides sa, sb); C arrives and leaves in D-fragment
+// layout, two 8-column halves.
+template <int K>
+__device__ __forceinline__ void mma_tile16(float (&c)[2][4], const float* A, int sa, const float* B, int sb,
+                                           int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < K / 8; ++ks) {
+        uint32_t a[4];
+        a[0] = to_tf32(A[g * sa + ks * 8 + t]);
+        a[1] = to_tf32(A[(g + 8) * sa + ks * 8 + t]);
+        a[2] = to_tf32(A[g * sa + ks * 8 + t + 4]);
+        a[3] = to_tf32(A[(g + 8) * sa + ks * 8 + t + 4]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t b0 = to_tf32(B[(ks * 8 + t) * sb + nt * 8 + g]);
+            const uint32_t b1 = to_tf32(B[(ks * 8 + t + 4) * sb + nt * 8 + g]);
+            mma_tf32(c[nt], a, b0, b1);
+        }
+    }
+}
+
+// Load / store a 16 x 16 fp32 tile (row stride s) in D-fragment layout.
+__device__ __forceinline__ void tile16_load(float (&c)[2][4], const float* M, int s, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        c[nt][0] = M[g * s + nt * 8 + 2 * t];
+        c[nt][1] = M[g * s + nt * 8 + 2 * t + 1];
+        c[nt][2] = M[(g + 8) * s + nt * 8 + 2 * t];
+        c[nt][3] = M[(g + 8) * s + nt * 8 + 2 * t + 1];
+    }
+}
+__device__ __forceinline__ void tile16_store(const float (&c)[2][4], float* M, int s, int lane, float sign) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        M[g * s + nt * 8 + 2 * t] = sign * c[nt][0];
+        M[g * s + nt * 8 + 2 * t + 1] = sign * c[nt][1];
+        M[(g + 8) * s + nt * 8 + 2 * t] = sign * c[nt][2];
+        M[(g + 8) * s + nt * 8 + 2 * t + 1] = sign * c[nt][3];
+    }
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
@@ -163,6 +231,10 @@ __device__ __forceinline__ void mma_128(uint32_t d_tmem, const Operand& a, const
     for (int ks = 0; ks < ksteps; ++ks) mma_f16(d_tmem, op_desc(a, ks), op_desc(b, ks), idesc, ks > 0);
 }
 
+__device__ __forceinline__ void bar_sync_named(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Barrier between a phase's shared-memory / TMEM writes and the tensor core
 // reading them (or a new MMA overwriting TMEM that was read).
 __device__ __forceinline__ void sync_for_mma() {
@@ -177,6 +249,7 @@ __device__ __forceinline__ void prefetch_chunk(const FwdParams& p, const ChunkRe
     const int t = tid & 127;
     if (t >= c.len) return;
     const size_t row = (size_t)(c.tok0 + t) * p.H + h;
+    if (tid < 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.beta + row) : "memory");
     switch (tid >> 7) {
         case 0: prefetch_l2(p.q + row * KD, KD * 2); break;
         case 1: prefetch_l2(p.k + row * KD, KD * 2); break;
@@ -349,7 +422,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 G[r][0] = ga.x; G[r][1] = ga.y; G[r][2] = ga.z; G[r][3] = ga.w;
                 G[r][4] = gb.x; G[r][5] = gb.y; G[r][6] = gb.z; G[r][7] = gb.w;
             }
-            float* tot = reinterpret_cast<float*>(sm + RW);     // [32 groups][128]
+            // [32 groups][129]: the odd row stride keeps the column-wise
+            // prefix scan free of shared-memory bank conflicts
+            constexpr int TS = 129;
+            float* tot = reinterpret_cast<float*>(sm + RW);
             {
                 float acc[8];
 #pragma unroll
@@ -361,27 +437,33 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                         acc[j] = fmaf(G[r][j], LOG2E, acc[j]);
                         G[r][j] = acc[j];
                     }
-                *reinterpret_cast<float4*>(tot + grp * 128 + d8) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                *reinterpret_cast<float4*>(tot + grp * 128 + d8 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) tot[grp * TS + d8 + j] = acc[j];
             }
             __syncthreads();
-            if (tid < 128) {            // exclusive prefix over the 32 row groups
-                float run = 0.f;
-                for (int g2 = 0; g2 < 32; ++g2) {
-                    const float x = tot[g2 * 128 + tid];
-                    tot[g2 * 128 + tid] = run;
-                    run += x;
+            {                           // exclusive prefix over the 32 row groups:
+                // warp w scans dimensions 8w .. 8w+7, lane = row group
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int d = warp * 8 + j;
+                    const float x = tot[lane * TS + d];
+                    float incl = x;
+#pragma unroll
+                    for (int s2 = 1; s2 < 32; s2 <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, incl, s2);
+                        if (lane >= s2) incl += y;
+                    }
+                    tot[lane * TS + d] = incl - x;
                 }
             }
             __syncthreads();
             {
-                const float4 o0 = *reinterpret_cast<const float4*>(tot + grp * 128 + d8);
-                const float4 o1 = *reinterpret_cast<const float4*>(tot + grp * 128 + d8 + 4);
-                const float off8[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
+                for (int j = 0; j < 8; ++j) {
+                    const float o = tot[grp * TS + d8 + j];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) G[r][j] += off8[j];
+                    for (int r = 0; r < 4; ++r) G[r][j] += o;
+                }
                 if (grp == 16) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) sG64[d8 + j] = G[0][j];
@@ -391,6 +473,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                     for (int j = 0; j < 8; ++j) sGL[d8 + j] = G[3][j];
                 }
             }
+            if (tid == 0) bulk_wait_read0();   // previous tile's bulk store has read its staging
             __syncthreads();
             if (tid < 128) {
                 const float P = sG64[tid];
@@ -491,6 +574,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                     sGL[d0 + 1] = G1[15];
                 }
             }
+            if (tid == 0) bulk_wait_read0();   // previous tile's bulk store has read its staging
             __syncthreads();
             const float P0 = sG64[d0], P1 = sG64[d0 + 1];
             const float eP0 = ex2(P0), eP1 = ex2(P1);
@@ -630,68 +714,37 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             // Levels 1 and 2 inside each diagonal 64-block:
             //   inv([[X, 0], [Y, Z]]) = [[Xi, 0], [-Zi Y Xi, Zi]]
             // T = Y Xi = Y + Y Xs (Xs: stored strictly-lower part of Xi) into
-            // a temp, then -Zi T = -(T + Zs T) in place of Y.
-            {
-                // level 1: 4 merges of 16-blocks (2 per diagonal block), 2 outputs per thread
-                const int mg = tid >> 7;
-                const int db = mg >> 1;
-                const int C0 = (mg & 1) * 32, R0 = C0 + 16;
-                const int li = tid & 127;
-                const int rr = li >> 3, cc = (li & 7) * 2;
+            // a temp, then -Zi T = -(T + Zs T) in place of Y.  Products on
+            // the tensor cores (warp-level tf32, fp32 accumulate).
+            if (warp < 4) {
+                // level 1: 4 merges of 16-blocks (2 per diagonal block), one warp each
+                const int db = warp >> 1;
+                const int C0 = (warp & 1) * 32, R0 = C0 + 16;
                 float* Db = Wd + db * 64 * DS;
-                float* T1 = Wt + mg * 256;
-                float t0v = Db[(R0 + rr) * DS + C0 + cc], t1v = Db[(R0 + rr) * DS + C0 + cc + 1];
-#pragma unroll
-                for (int mm = 0; mm < 16; ++mm) {
-                    const float y = Db[(R0 + rr) * DS + C0 + mm];
-                    const float2 xs = *reinterpret_cast<const float2*>(Db + (C0 + mm) * DS + C0 + cc);
-                    t0v = fmaf(y, xs.x, t0v);
-                    t1v = fmaf(y, xs.y, t1v);
-                }
-                T1[rr * 16 + cc] = t0v;
-                T1[rr * 16 + cc + 1] = t1v;
-                __syncthreads();
-                float l0 = t0v, l1 = t1v;
-#pragma unroll
-                for (int mm = 0; mm < 16; ++mm) {
-                    const float z = Db[(R0 + rr) * DS + R0 + mm];    // zero for mm >= rr
-                    l0 = fmaf(z, T1[mm * 16 + cc], l0);
-                    l1 = fmaf(z, T1[mm * 16 + cc + 1], l1);
-                }
-                Db[(R0 + rr) * DS + C0 + cc] = -l0;
-                Db[(R0 + rr) * DS + C0 + cc + 1] = -l1;
+                float* T1 = Wt + warp * 256;
+                float acc[2][4];
+                tile16_load(acc, Db + R0 * DS + C0, DS, lane);                           // Y
+                mma_tile16<16>(acc, Db + R0 * DS + C0, DS, Db + C0 * DS + C0, DS, lane);  // + Y Xs
+                tile16_store(acc, T1, 16, lane, 1.f);
+                __syncwarp();
+                mma_tile16<16>(acc, Db + R0 * DS + R0, DS, T1, 16, lane);               // T + Zs T
+                tile16_store(acc, Db + R0 * DS + C0, DS, lane, -1.f);
             }
             __syncthreads();
-            {
-                // level 2: 2 merges of 32-blocks (one per diagonal block), 4 outputs per thread
-                const int db = tid >> 8;
-                const int li = tid & 255;
-                const int rr = li >> 3, cc = (li & 7) * 4;
+            if (warp < 8) {
+                // level 2: 2 merges of 32-blocks (one per diagonal block), one
+                // 16x16 quadrant of the 32x32 result per warp
+                const int db = warp >> 2;
+                const int mr = ((warp >> 1) & 1) * 16, nc = (warp & 1) * 16;
                 float* Db = Wd + db * 64 * DS;
-                float* T2 = Wt + db * 1024;
-                float4 t = *reinterpret_cast<const float4*>(Db + (32 + rr) * DS + cc);
-#pragma unroll
-                for (int mm = 0; mm < 32; ++mm) {
-                    const float y = Db[(32 + rr) * DS + mm];
-                    const float4 xs = *reinterpret_cast<const float4*>(Db + mm * DS + cc);
-                    t.x = fmaf(y, xs.x, t.x);
-                    t.y = fmaf(y, xs.y, t.y);
-                    t.z = fmaf(y, xs.z, t.z);
-                    t.w = fmaf(y, xs.w, t.w);
-                }
-                *reinterpret_cast<float4*>(T2 + rr * 32 + cc) = t;
-                __syncthreads();
-                float4 l = t;
-#pragma unroll
-                for (int mm = 0; mm < 32; ++mm) {
-                    const float z = Db[(32 + rr) * DS + 32 + mm];    // zero for mm >= rr
-                    const float4 tv = *reinterpret_cast<const float4*>(T2 + mm * 32 + cc);
-                    l.x = fmaf(z, tv.x, l.x);
-                    l.y = fmaf(z, tv.y, l.y);
-                    l.z = fmaf(z, tv.z, l.z);
-                    l.w = fmaf(z, tv.w, l.w);
-                }
-                *reinterpret_cast<float4*>(Db + (32 + rr) * DS + cc) = make_float4(-l.x, -l.y, -l.z, -l.w);
+                float* T2 = Wt + db * 1024;     // 32 x 32
+                float acc[2][4];
+                tile16_load(acc, Db + (32 + mr) * DS + nc, DS, lane);                        // Y
+                mma_tile16<32>(acc, Db + (32 + mr) * DS, DS, Db + nc, DS, lane);             // + Y Xs
+                tile16_store(acc, T2 + mr * 32 + nc, 32, lane, 1.f);
+                bar_sync_named(1, 256);
+                mma_tile16<32>(acc, Db + (32 + mr) * DS + 32, DS, T2 + nc, 32, lane);        // T + Zs T
+                tile16_store(acc, Db + (32 + mr) * DS + nc, DS, lane, -1.f);
             }
             __syncthreads();
             // Level 3 on tensor cores: L = -Q (A10 P), P / Q the inverses of
@@ -855,13 +908,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                             const float ns = -rs;
 #pragma unroll
                             for (int j = 0; j < 32; j += 8)
-                                stg_v4(dst, TILE_NM + sw128_off(trow, col0 + j, 128), pack_f16(ns * x[j], ns * x[j + 1]),
+                                sts_v4(sm, MP::ST_NM + sw128_off(trow, col0 + j, 128), pack_f16(ns * x[j], ns * x[j + 1]),
                                        pack_f16(ns * x[j + 2], ns * x[j + 3]), pack_f16(ns * x[j + 4], ns * x[j + 5]),
                                        pack_f16(ns * x[j + 6], ns * x[j + 7]));
                         } else {
 #pragma unroll
                             for (int j = 0; j < 32; j += 8)
-                                stg_v4(dst, TILE_BC + part * BC_PIECE + sw64_off(trow, j), pack_f16(rs * x[j], rs * x[j + 1]),
+                                sts_v4(sm, MP::ST_BC + part * BC_PIECE + sw64_off(trow, j), pack_f16(rs * x[j], rs * x[j + 1]),
                                        pack_f16(rs * x[j + 2], rs * x[j + 3]), pack_f16(rs * x[j + 4], rs * x[j + 5]),
                                        pack_f16(rs * x[j + 6], rs * x[j + 7]));
                         }
@@ -878,14 +931,14 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                                     g0.x *= e0.x; g0.y *= e0.y; g1.x *= e0.z; g1.y *= e0.w;
                                     g2.x *= e1.x; g2.y *= e1.y; g3.x *= e1.z; g3.y *= e1.w;
                                 }
-                                stg_v4(dst, TILE_QE + sw128_off(trow, col0 + j, 128), pack_f16(g0.x - x[j], g0.y - x[j + 1]),
+                                sts_v4(sm, MP::ST_QE + sw128_off(trow, col0 + j, 128), pack_f16(g0.x - x[j], g0.y - x[j + 1]),
                                        pack_f16(g1.x - x[j + 2], g1.y - x[j + 3]), pack_f16(g2.x - x[j + 4], g2.y - x[j + 5]),
                                        pack_f16(g3.x - x[j + 6], g3.y - x[j + 7]));
                             }
                         } else {
 #pragma unroll
                             for (int j = 0; j < 32; j += 8)
-                                stg_v4(dst, TILE_OI + part * OI_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
+                                sts_v4(sm, MP::ST_OI + part * OI_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
                                        pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]),
                                        pack_f16(x[j + 6], x[j + 7]));
                         }
@@ -899,10 +952,18 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                     dg.w = ex2(sGL[tid * 4 + 3]);
                     *reinterpret_cast<float4*>(dst + TILE_DG + tid * 16) = dg;
                 }
+                fence_async_smem();
+                tc_fence_before();
+                __syncthreads();
+                tc_fence_after();
+                if (tid == 0) {      // asynchronous: drains while the next chunk loads
+                    bulk_s2g(dst + TILE_NM, sbase + MP::ST_NM, KD * KD * 2);
+                    bulk_s2g(dst + TILE_QE, sbase + MP::ST_QE, BT * KD * 2);
+                    bulk_s2g(dst + TILE_BC, sbase + MP::ST_BC, NVT * BC_PIECE);
+                    bulk_s2g(dst + TILE_OI, sbase + MP::ST_OI, NVT * OI_PIECE);
+                    bulk_commit();
+                }
             }
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
         }
 
         idx = nidx;
@@ -911,7 +972,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
         h = hn;
         have = have_n;
     }
-    if (tid == 0 && *sFlag != 0) atomicOr(p.status, STATUS_TIMEOUT);
+    if (tid == 0) {
+        bulk_wait0();
+        if (*sFlag != 0) atomicOr(p.status, STATUS_TIMEOUT);
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
