@@ -226,9 +226,19 @@ __device__ __forceinline__ uint64_t op_desc(const Operand& o, int ks) {
                      SW_128B);
 }
 
+// Descriptor advance per k-step, in the 16-byte units of the start-address
+// field (adding it to a base descriptor never carries out of the field:
+// shared addresses stay below 256 KB).
+__device__ __forceinline__ uint64_t op_step(const Operand& o, int ks) {
+    if (o.mn_major) return (uint64_t)ks * 128u;
+    return (uint64_t)((ks >> 2) * (int)o.rows * 8 + (ks & 3) * 2);
+}
+
 __device__ __forceinline__ void mma_128(uint32_t d_tmem, const Operand& a, const Operand& b, uint32_t idesc,
                                         int ksteps) {
-    for (int ks = 0; ks < ksteps; ++ks) mma_f16(d_tmem, op_desc(a, ks), op_desc(b, ks), idesc, ks > 0);
+    const uint64_t da = op_desc(a, 0), db = op_desc(b, 0);
+#pragma unroll
+    for (int ks = 0; ks < ksteps; ++ks) mma_f16(d_tmem, da + op_step(a, ks), db + op_step(b, ks), idesc, ks > 0);
 }
 
 __device__ __forceinline__ void bar_sync_named(int id, int nthreads) {
