@@ -8,12 +8,19 @@
 // states use the page's [N, H, V, K] layout (section "算子签名与 I/O 规格"),
 // i.e. the transpose of the K x V state; the transpose happens here.
 //
-// GB300 mapping.  128 threads; thread i owns state row d = i and output row
-// t = i (TMEM lane i).  Per chunk, two M=128 N=32 K=128 fp16 MMAs (Nm S and
-// Qe S) read the fp16 copy of S from shared memory and accumulate in TMEM;
-// the fp32 state update, Bc / Oi additions and the bf16 output conversion
-// run on CUDA cores.  The chunk tiles are double-buffered with 1-D bulk
-// copies so that chunk j+1's tiles land while chunk j computes.
+// GB300 mapping.  320 threads in four roles, handing work to each other
+// through mbarriers so that no role waits on another's latency:
+//   warps 0-3  state:  thread i owns row d = i of S (fp32, registers); per
+//              chunk it reads Nm S from TMEM, applies S' = Dg S + Nm S + Bc
+//              and writes the fp16 copy of S' the next chunk's MMAs read;
+//   warps 4-7  output: thread i owns row t = i; reads Qe S from one of two
+//              TMEM buffers, adds Oi, rounds to bf16 and stores o;
+//   warp 8     MMA issue: per chunk the Nm S product (the critical chain),
+//              then the Qe S product, which executes while the state warps
+//              update S;
+//   warp 9     loads: bulk copies of the chunk tiles, two chunks ahead.
+// Chunk tiles (Nm, Qe, Bc, Dg) are double-buffered, Oi goes through a ring
+// of four, the fp16 state copy is double-buffered.
 #include "kda_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -21,19 +28,23 @@ namespace kda {
 
 namespace {
 
-constexpr int SCAN_THREADS = 128;
+constexpr int SCAN_THREADS = 320;
+// stage: Nm | Qe | Bc piece | Dg
 constexpr uint32_t ST_NM = 0;
 constexpr uint32_t ST_QE = 32768;
 constexpr uint32_t ST_BC = 65536;
-constexpr uint32_t ST_OI = 73728;
-constexpr uint32_t ST_DG = 81920;
-constexpr uint32_t ST_BYTES = 82432;          // bytes loaded per stage
-constexpr uint32_t ST_STRIDE = 82944;         // 1024-aligned stage stride
-constexpr uint32_t S_S16 = 2 * ST_STRIDE;     // fp16 state copy, [K][32] 64B-swizzled
-constexpr uint32_t S_BAR = S_S16 + 8192;      // full[2], mma
-constexpr uint32_t S_TMEM = S_BAR + 64;
+constexpr uint32_t ST_DG = 73728;
+constexpr uint32_t ST_BYTES = 74240;          // bytes loaded per stage
+constexpr uint32_t ST_STRIDE = 74752;         // 1024-aligned stage stride
+constexpr uint32_t S_OI = 2 * ST_STRIDE;      // Oi ring: 4 x 8 KB
+constexpr uint32_t S_S16 = S_OI + 4 * OI_PIECE;   // fp16 state copies: 2 x [K][32] 64B-swizzled
+constexpr uint32_t S_BAR = S_S16 + 2 * 8192;
+// barrier offsets (8 bytes each)
+constexpr uint32_t B_FULL = 0, B_OIFULL = 16, B_OIFREE = 48, B_MMAS = 80, B_MMAO = 88, B_OFREE = 104,
+                   B_S16 = 120, B_SFREE = 128;
+constexpr uint32_t S_TMEM = S_BAR + 192;
 constexpr uint32_t S_FLAG = S_TMEM + 4;
-constexpr uint32_t SCAN_SMEM = S_BAR + 128 + 1024;
+constexpr uint32_t SCAN_SMEM = S_BAR + 256 + 1024;
 
 __device__ __forceinline__ void load_stage(const FwdParams& p, int slot, int h, int vt, uint32_t dst,
                                            uint32_t bar) {
@@ -42,8 +53,12 @@ __device__ __forceinline__ void load_stage(const FwdParams& p, int slot, int h, 
     bulk_g2s(dst + ST_NM, src + TILE_NM, KD * KD * 2, bar);
     bulk_g2s(dst + ST_QE, src + TILE_QE, BT * KD * 2, bar);
     bulk_g2s(dst + ST_BC, src + TILE_BC + vt * BC_PIECE, BC_PIECE, bar);
-    bulk_g2s(dst + ST_OI, src + TILE_OI + vt * OI_PIECE, OI_PIECE, bar);
     bulk_g2s(dst + ST_DG, src + TILE_DG, KD * 4, bar);
+}
+
+__device__ __forceinline__ void load_oi(const FwdParams& p, int slot, int h, int vt, uint32_t dst, uint32_t bar) {
+    mbar_arrive_expect_tx(bar, OI_PIECE);
+    bulk_g2s(dst, tile_ptr(p, slot, h) + TILE_OI + vt * OI_PIECE, OI_PIECE, bar);
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
@@ -58,6 +73,9 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
     __half2 h = *reinterpret_cast<__half2*>(&u);
     return __half22float2(h);
 }
+__device__ __forceinline__ void bar_sync_named(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 }  // namespace
 
@@ -71,88 +89,91 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
     const int H = p.H;
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int row = tid & 127;                      // state row d, or output row t
 
     long long bos;
     int len;
     if (!seq_bounds(p, n, bos, len)) return;        // uniform
     const int nch = (len + BT - 1) / BT;
 
-    const uint32_t full0 = sbase + S_BAR, full1 = sbase + S_BAR + 8, mbar = sbase + S_BAR + 16;
+    const uint32_t bars = sbase + S_BAR;
+    auto full = [&](int s) { return bars + B_FULL + 8u * (uint32_t)s; };
+    auto oifull = [&](int r) { return bars + B_OIFULL + 8u * (uint32_t)r; };
+    auto oifree = [&](int r) { return bars + B_OIFREE + 8u * (uint32_t)r; };
+    auto mmao = [&](int b) { return bars + B_MMAO + 8u * (uint32_t)b; };
+    auto ofree = [&](int b) { return bars + B_OFREE + 8u * (uint32_t)b; };
+    auto sfree = [&](int s) { return bars + B_SFREE + 8u * (uint32_t)s; };
+    const uint32_t mmas = bars + B_MMAS, s16rdy = bars + B_S16;
     volatile uint32_t* sFlag = reinterpret_cast<volatile uint32_t*>(sm + S_FLAG);
     if (warp == 0) {
-        tmem_alloc(sbase + S_TMEM, 64);
+        tmem_alloc(sbase + S_TMEM, 128);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(full0, 1);
-        mbar_init(full1, 1);
-        mbar_init(mbar, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(full(i), 1);
+            mbar_init(mmao(i), 1);
+            mbar_init(ofree(i), 1);
+            mbar_init(sfree(i), 1);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(oifull(i), 1);
+            mbar_init(oifree(i), 1);
+        }
+        mbar_init(mmas, 1);
+        mbar_init(s16rdy, 1);
         fence_mbar_init();
         *sFlag = 0;
     }
 
-    // State rows: thread d holds S[d][vt*32 .. vt*32+31] (fp32).
-    const int d = tid;
+    // State rows: state thread d holds S[d][vt*32 .. vt*32+31] (fp32).
     float S[BV];
     const size_t sbase_state = ((size_t)n * H + h) * VD * KD;   // [N,H,V,K] slab
-    if (p.h0 != nullptr) {
+    if (warp < 4) {
+        if (p.h0 != nullptr) {
 #pragma unroll
-        for (int j = 0; j < BV; ++j) S[j] = __ldg(p.h0 + sbase_state + (size_t)(vt * BV + j) * KD + d);
-    } else {
+            for (int j = 0; j < BV; ++j) S[j] = __ldg(p.h0 + sbase_state + (size_t)(vt * BV + j) * KD + row);
+        } else {
 #pragma unroll
-        for (int j = 0; j < BV; ++j) S[j] = 0.f;
+            for (int j = 0; j < BV; ++j) S[j] = 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < BV; j += 8)
+            *reinterpret_cast<uint4*>(sm + S_S16 + sw64_off(row, j)) =
+                make_uint4(pack_f16x2(S[j], S[j + 1]), pack_f16x2(S[j + 2], S[j + 3]),
+                           pack_f16x2(S[j + 4], S[j + 5]), pack_f16x2(S[j + 6], S[j + 7]));
     }
-#pragma unroll
-    for (int j = 0; j < BV; j += 8)
-        *reinterpret_cast<uint4*>(sm + S_S16 + sw64_off(d, j)) =
-            make_uint4(pack_f16x2(S[j], S[j + 1]), pack_f16x2(S[j + 2], S[j + 3]), pack_f16x2(S[j + 4], S[j + 5]),
-                       pack_f16x2(S[j + 6], S[j + 7]));
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + S_TMEM);
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
 
-    if (tid == 0) {
-        if (nch > 0) load_stage(p, chunk_slot(p, n, 0), h, vt, sbase + 0 * ST_STRIDE, full0);
-        if (nch > 1) load_stage(p, chunk_slot(p, n, 1), h, vt, sbase + 1 * ST_STRIDE, full1);
-    }
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (!mbar_wait(bar, parity, WAIT_LIMIT)) *sFlag = 1;
+    };
 
-    const uint32_t id = idesc_f16(T_F16, 128, BV, false, true);
-    for (int j = 0; j < nch; ++j) {
-        const int s = j & 1;
-        const uint32_t stage = sbase + (uint32_t)s * ST_STRIDE;
-        const uint8_t* st = sm + (size_t)s * ST_STRIDE;
-        if (!mbar_wait(s ? full1 : full0, (uint32_t)(j >> 1) & 1u, WAIT_LIMIT)) *sFlag = 1;
-        if (tid == 0) {
+    if (warp < 4) {
+        // ------------------------------------------------------------------
+        // State: S' = Dg S + Nm S + Bc, row d = tid.
+        // ------------------------------------------------------------------
+        for (int j = 0; j < nch; ++j) {
+            const int s = j & 1, b = j & 1;
+            wait(full(s), (uint32_t)(j >> 1) & 1u);   // Bc / Dg of this chunk have landed
+            wait(mmas, (uint32_t)j & 1u);
             tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t bdesc = smem_desc(sbase + S_S16 + (uint32_t)ks * 1024u, 512u, 512u, SW_64B);
-                const uint64_t a_nm = smem_desc(stage + ST_NM + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u,
-                                                16u, 1024u, SW_128B);
-                const uint64_t a_qe = smem_desc(stage + ST_QE + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u,
-                                                16u, 1024u, SW_128B);
-                mma_f16(tmem + 0, a_nm, bdesc, id, ks > 0);
-                mma_f16(tmem + BV, a_qe, bdesc, id, ks > 0);
-            }
-            mma_commit(mbar);
-        }
-        if (!mbar_wait(mbar, (uint32_t)j & 1u, WAIT_LIMIT)) *sFlag = 1;
-        tc_fence_after();
-
-        // State update, row d = tid.
-        {
+            const uint8_t* st = sm + (size_t)s * ST_STRIDE;
             float x[BV];
-            tmem_ld32(tmem + lane_off + 0u, x);
+            tmem_ld32(tmem + lane_off, x);
             tmem_ld_wait();
-            const float Dd = *reinterpret_cast<const float*>(st + ST_DG + d * 4);
+            const float Dd = *reinterpret_cast<const float*>(st + ST_DG + row * 4);
 #pragma unroll
             for (int c8 = 0; c8 < BV; c8 += 8) {
-                const uint4 b = *reinterpret_cast<const uint4*>(st + ST_BC + sw64_off(d, c8));
-                const float2 b0 = unpack_f16x2(b.x), b1 = unpack_f16x2(b.y), b2 = unpack_f16x2(b.z),
-                             b3 = unpack_f16x2(b.w);
+                const uint4 bc = *reinterpret_cast<const uint4*>(st + ST_BC + sw64_off(row, c8));
+                const float2 b0 = unpack_f16x2(bc.x), b1 = unpack_f16x2(bc.y), b2 = unpack_f16x2(bc.z),
+                             b3 = unpack_f16x2(bc.w);
                 S[c8 + 0] = fmaf(Dd, S[c8 + 0], x[c8 + 0] + b0.x);
                 S[c8 + 1] = fmaf(Dd, S[c8 + 1], x[c8 + 1] + b0.y);
                 S[c8 + 2] = fmaf(Dd, S[c8 + 2], x[c8 + 2] + b1.x);
@@ -162,24 +183,48 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
                 S[c8 + 6] = fmaf(Dd, S[c8 + 6], x[c8 + 6] + b3.x);
                 S[c8 + 7] = fmaf(Dd, S[c8 + 7], x[c8 + 7] + b3.y);
             }
+            // next chunk's fp16 state copy goes to the other buffer: the MMAs
+            // that read it one chunk ago precede mma_s in issue order
+            uint8_t* s16 = sm + S_S16 + (uint32_t)(b ^ 1) * 8192u;
 #pragma unroll
             for (int c8 = 0; c8 < BV; c8 += 8)
-                *reinterpret_cast<uint4*>(sm + S_S16 + sw64_off(d, c8)) =
+                *reinterpret_cast<uint4*>(s16 + sw64_off(row, c8)) =
                     make_uint4(pack_f16x2(S[c8], S[c8 + 1]), pack_f16x2(S[c8 + 2], S[c8 + 3]),
                                pack_f16x2(S[c8 + 4], S[c8 + 5]), pack_f16x2(S[c8 + 6], S[c8 + 7]));
+            fence_async_smem();
+            tc_fence_before();
+            bar_sync_named(1, 128);
+            if (tid == 0) {
+                mbar_arrive(s16rdy);      // next chunk's MMAs may start
+                mbar_arrive(sfree(s));    // Bc / Dg of stage s are read
+            }
         }
-        // Output row t = tid.
-        {
+        if (p.ht != nullptr) {
+#pragma unroll
+            for (int j = 0; j < BV; ++j) p.ht[sbase_state + (size_t)(vt * BV + j) * KD + row] = S[j];
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------------------------
+        // Output: o rows of chunk j from TMEM buffer j & 1 plus Oi.
+        // ------------------------------------------------------------------
+        for (int j = 0; j < nch; ++j) {
+            const int b = j & 1, r = j & 3;
+            wait(mmao(b), (uint32_t)(j >> 1) & 1u);
+            tc_fence_after();
             float y[BV];
-            tmem_ld32(tmem + lane_off + (uint32_t)BV, y);
+            tmem_ld32(tmem + lane_off + 32u + 32u * (uint32_t)b, y);
             tmem_ld_wait();
-            const int t = tid;
+            tc_fence_before();
+            bar_sync_named(2, 128);
+            if (tid == 128) mbar_arrive(ofree(b));
+            wait(oifull(r), (uint32_t)(j >> 2) & 1u);
             const int rows = len - j * BT < BT ? len - j * BT : BT;
-            if (t < rows) {
+            if (row < rows) {
+                const uint8_t* oi_s = sm + S_OI + (uint32_t)r * OI_PIECE;
                 uint32_t w[BV / 2];
 #pragma unroll
                 for (int c8 = 0; c8 < BV; c8 += 8) {
-                    const uint4 oi = *reinterpret_cast<const uint4*>(st + ST_OI + sw64_off(t, c8));
+                    const uint4 oi = *reinterpret_cast<const uint4*>(oi_s + sw64_off(row, c8));
                     const float2 a0 = unpack_f16x2(oi.x), a1 = unpack_f16x2(oi.y), a2 = unpack_f16x2(oi.z),
                                  a3 = unpack_f16x2(oi.w);
                     w[c8 / 2 + 0] = pack_bf16x2(y[c8 + 0] + a0.x, y[c8 + 1] + a0.y);
@@ -187,28 +232,73 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
                     w[c8 / 2 + 2] = pack_bf16x2(y[c8 + 4] + a2.x, y[c8 + 5] + a2.y);
                     w[c8 / 2 + 3] = pack_bf16x2(y[c8 + 6] + a3.x, y[c8 + 7] + a3.y);
                 }
-                uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)(bos + (long long)j * BT + t) * H + h) * VD +
+                uint4* dst = reinterpret_cast<uint4*>(p.o + ((size_t)(bos + (long long)j * BT + row) * H + h) * VD +
                                                       vt * BV);
 #pragma unroll
                 for (int q4 = 0; q4 < BV / 8; ++q4)
                     dst[q4] = make_uint4(w[q4 * 4 + 0], w[q4 * 4 + 1], w[q4 * 4 + 2], w[q4 * 4 + 3]);
             }
+            bar_sync_named(2, 128);
+            if (tid == 128) mbar_arrive(oifree(r));
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (*sFlag != 0) break;   // uniform after the barrier
-        if (tid == 0 && j + 2 < nch) load_stage(p, chunk_slot(p, n, j + 2), h, vt, stage, s ? full1 : full0);
+    } else if (warp == 8) {
+        // ------------------------------------------------------------------
+        // MMA issue (one thread).
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            const uint32_t id = idesc_f16(T_F16, 128, BV, false, true);
+            // per k-step only the start-address field of these advances
+            const uint64_t a_nm0 = smem_desc(sbase + ST_NM, 16u, 1024u, SW_128B);
+            const uint64_t a_nm1 = smem_desc(sbase + ST_STRIDE + ST_NM, 16u, 1024u, SW_128B);
+            const uint64_t a_qe0 = smem_desc(sbase + ST_QE, 16u, 1024u, SW_128B);
+            const uint64_t a_qe1 = smem_desc(sbase + ST_STRIDE + ST_QE, 16u, 1024u, SW_128B);
+            const uint64_t b_s0 = smem_desc(sbase + S_S16, 512u, 512u, SW_64B);
+            const uint64_t b_s1 = smem_desc(sbase + S_S16 + 8192u, 512u, 512u, SW_64B);
+            for (int j = 0; j < nch; ++j) {
+                const int s = j & 1, b = j & 1;
+                wait(full(s), (uint32_t)(j >> 1) & 1u);
+                if (j >= 1) wait(s16rdy, (uint32_t)(j - 1) & 1u);
+                tc_fence_after();
+                const uint64_t a_nm = s ? a_nm1 : a_nm0, a_qe = s ? a_qe1 : a_qe0, b_s = b ? b_s1 : b_s0;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)   // critical chain first: Nm S -> cols [0,32)
+                    mma_f16(tmem, a_nm + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), b_s + (uint64_t)(ks * 64), id,
+                            ks > 0);
+                mma_commit(mmas);
+                if (j >= 2) wait(ofree(b), (uint32_t)((j - 2) >> 1) & 1u);
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)   // output product Qe S -> buffer b
+                    mma_f16(tmem + 32u + 32u * (uint32_t)b, a_qe + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
+                            b_s + (uint64_t)(ks * 64), id, ks > 0);
+                mma_commit(mmao(b));
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------
+        // Loads (one thread): chunk tiles two chunks ahead.
+        // ------------------------------------------------------------------
+        if (lane == 0) {
+            for (int c = 0; c < nch; ++c) {
+                const int s = c & 1, r = c & 3;
+                if (c >= 2) {
+                    // stage s held chunk c-2: its MMAs (Qe S last) and the
+                    // state warps' Bc / Dg reads are done
+                    wait(mmao(s), (uint32_t)((c - 2) >> 1) & 1u);
+                    wait(sfree(s), (uint32_t)((c - 2) >> 1) & 1u);
+                }
+                load_stage(p, chunk_slot(p, n, c), h, vt, sbase + (uint32_t)s * ST_STRIDE, full(s));
+                if (c >= 4) wait(oifree(r), (uint32_t)((c - 4) >> 2) & 1u);
+                load_oi(p, chunk_slot(p, n, c), h, vt, sbase + S_OI + (uint32_t)r * OI_PIECE, oifull(r));
+            }
+        }
     }
 
+    __syncwarp();
     if (*sFlag != 0 && tid == 0) atomicOr(p.status, STATUS_TIMEOUT);
-    if (p.ht != nullptr) {
-#pragma unroll
-        for (int j = 0; j < BV; ++j) p.ht[sbase_state + (size_t)(vt * BV + j) * KD + d] = S[j];
-    }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 64);
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 cudaError_t launch_scan(const FwdParams& p, cudaStream_t stream) {
