@@ -26,6 +26,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from chunked_gated_delta_kda_gb300.inputs import WORKLOADS, custom, make_inputs  # noqa: E402
@@ -210,6 +211,135 @@ def run_reference(args, w, rank, world):
 
 
 # ---------------------------------------------------------------------------
+# Decode (token-by-token entry point)
+# ---------------------------------------------------------------------------
+
+DECODE_METRIC = "KDA decode (token-by-token, in-place state pool) token*heads/s"
+DECODE_N, DECODE_H, DECODE_POOL = 256, 32, 512
+# Per (sequence, head) and token: the fp32 state read and written once
+# (2 x 64 KiB) plus q, k, v, o bf16 (4 x 256 B), g fp32 512 B, beta 4 B.
+DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + 4 * 256 + 512 + 4
+
+
+def decode_oracle_rate(x, target_s):
+    import oracle
+    n = 1
+    while True:
+        sl = {k: x[k][:n].float().cpu().numpy() for k in ("q", "k", "v", "g", "beta")}
+        # the slots the sample touches, renumbered 0..n-1 (the oracle copies its pool)
+        sub = x["pool"][x["indices"][:n, 0].long()].cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.fused_recurrent(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], sub, np.arange(n))
+        dt = time.perf_counter() - t0
+        if dt > target_s / 4 or n >= DECODE_N:
+            break
+        n = min(DECODE_N, n * 4)
+    return {"value": n * DECODE_H / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"fp64 numpy decode oracle, {n} sequences x {DECODE_H} heads x 1 token ({dt:.1f} s)"}
+
+
+def run_decode(args, rank, world, local):
+    from chunked_gated_delta_kda_gb300 import binding
+    from chunked_gated_delta_kda_gb300.inputs import make_decode_inputs
+    name = f"decode_n{DECODE_N}_h{DECODE_H}_pool{DECODE_POOL}"
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        x = make_decode_inputs(DECODE_N, DECODE_H, 1, pool_slots=DECODE_POOL, seed=5)
+        cb = decode_oracle_rate(x, target_s=max(1.0, 60.0 / max(1, args.steps + args.warmup)))
+        line = {"impl": "reference", "metric": DECODE_METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": 0,
+                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": name},
+                "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load_library()
+    x = make_decode_inputs(DECODE_N, DECODE_H, 1, pool_slots=DECODE_POOL, seed=5 + rank, device=str(dev))
+    q, k, v, g, beta, pool = (x[n] for n in ("q", "k", "v", "g", "beta", "pool"))
+    # two disjoint slot sets, alternated between steps: the 1 GiB touched per
+    # pair of steps is far larger than L2, so no step reads a cached state
+    perm = torch.randperm(DECODE_POOL, generator=torch.Generator().manual_seed(11)).to(torch.int32)
+    idx = [perm[:DECODE_N].reshape(-1, 1).to(dev), perm[DECODE_N:].reshape(-1, 1).to(dev)]
+    o = torch.empty((DECODE_N, 1, DECODE_H, 128), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(256, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        binding.kda_fused_recurrent(q, k, v, g, beta, None, pool, idx[i & 1], None, None, o, DECODE_N, 0, ws)
+
+    for i in range(args.warmup):
+        step(i)
+    assert binding.get_status(ws) == 0
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_end = time.time()
+    clocks.stop()
+    assert binding.get_status(ws) == 0
+    t = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item()) / args.steps
+    units = DECODE_N * DECODE_H
+    peaks = load_peaks()
+    achieved = units * DECODE_BYTES_PER_UNIT / (ms * 1e-3) / 1e9
+    tr = load_traffic().get("kda_recurrent_kernel")
+    line = {"metric": DECODE_METRIC, "value": world * units / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": name, "sequences": DECODE_N, "H": DECODE_H, "tokens_per_sequence": 1,
+                       "pool_slots": DECODE_POOL,
+                       "l2_between_steps": "alternating disjoint slot sets, 1 GiB of state per step pair; no flush"},
+            "roofline": {"kernel": "kda_recurrent_kernel", "bound": "hbm", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": (tr * units if tr is not None else None),
+                         "alg_bytes_per_launch": units * DECODE_BYTES_PER_UNIT, "ms_per_launch": ms},
+            "gpu_launches": args.steps}
+    if args.e2e_steps > 0:
+        host = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta")}
+        dbuf = {n: torch.empty_like(x[n]) for n in host}
+        o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for i in range(args.e2e_steps):
+            for n, tt in host.items():
+                dbuf[n].copy_(tt, non_blocking=True)
+            binding.kda_fused_recurrent(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], None, pool,
+                                        idx[i & 1], None, None, o, DECODE_N, 0, ws)
+            o_host.copy_(o, non_blocking=True)
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        te = f0.elapsed_time(f1) / args.e2e_steps
+        line["e2e"] = {"value": world * units / (te * 1e-3), "unit": UNIT,
+                       "h2d_bytes_per_step": sum(tt.numel() * tt.element_size() for tt in host.values()),
+                       "d2h_bytes_per_step": o_host.numel() * o_host.element_size(), "ms_per_step": te}
+    line["clocks"] = clocks.summary(t_start, t_end)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = decode_oracle_rate({kk: (vv.cpu() if isinstance(vv, torch.Tensor) else vv)
+                                                   for kk, vv in x.items()}, target_s=min(args.cpu_seconds, 10.0))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+# ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
 
@@ -223,6 +353,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--op", choices=["fwd", "decode"], default="fwd",
+                    help="fwd: the chunked forward (default); decode: the token-by-token entry point")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
@@ -231,6 +363,8 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     w = WORKLOADS[args.workload]
 
+    if args.op == "decode":
+        return run_decode(args, rank, world, local)
     if args.impl == "reference":
         return run_reference(args, w, rank, world)
 
@@ -331,7 +465,7 @@ def main():
                           "frac": t_roof / (ms_per_step * 1e-3)},
         "stages_ms": {"kda_prep_kernel": prep_ms, "kda_scan_kernel": scan_ms},
         "roofline": roofline,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 3 * args.steps,   # fast prep, wide prep (exits at once when no chunk needs it), scan
     }
 
     # End to end through the public API: pinned host inputs -> device, forward,
@@ -369,7 +503,7 @@ def main():
             dist.all_reduce(te, op=dist.ReduceOp.MAX)
         line["e2e"] = {"value": world * th / (float(te.item()) * 1e-3), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": float(te.item())}
-        line["gpu_launches_e2e"] = 2 * args.e2e_steps
+        line["gpu_launches_e2e"] = 3 * args.e2e_steps
 
     line["clocks"] = clocks.summary(t_start, t_end)
 

@@ -27,7 +27,10 @@ KDA_FLAG_QK_L2NORM = 1
 _STATUS = {
     0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
     4: "invalid cu_seqlens", 5: "device wait timed out", 6: "too large for the no-alloc scratch",
+    7: "state slot index or accepted-token count out of range",
 }
+
+RECURRENT_WORKSPACE_BYTES = 256
 
 _lib = None
 
@@ -57,6 +60,9 @@ def load_library(path: Optional[str] = None):
     lib.kda_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i]
     lib.kda_get_status.restype = ctypes.c_int
     lib.kda_get_status.argtypes = [vp, vp]
+    lib.kda_fused_recurrent.restype = ctypes.c_int
+    lib.kda_fused_recurrent.argtypes = [vp, vp, vp, vp, vp, f, vp, i, vp, i, vp, vp, vp,
+                                        i, i, i, i, i, i, u, vp, vp]
     lib.kda_status_str.restype = ctypes.c_char_p
     lib.kda_status_str.argtypes = [i]
     _lib = lib
@@ -181,3 +187,70 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
     with torch.cuda.device(dev):
         kda_fwd(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, N, flags, workspace)
     return o, ht
+
+
+def kda_fused_recurrent(q, k, v, g, beta, scale, state_pool, ssm_state_indices, num_accepted_tokens,
+                        cu_seqlens, o, N: int, flags: int, workspace: torch.Tensor) -> None:
+    """Direct call of the token-by-token entry point on caller-provided
+    tensors.  ``state_pool`` fp32 [P,H,V,K] is updated in place;
+    ``ssm_state_indices`` is int32 [N, stride].  Raises KdaError on a
+    non-zero status."""
+    lib = load_library()
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    stride = ssm_state_indices.shape[1] if ssm_state_indices.dim() == 2 else 1
+    rc = lib.kda_fused_recurrent(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                 float(scale if scale is not None else -1.0), _ptr(state_pool),
+                                 int(state_pool.shape[0]), _ptr(ssm_state_indices), stride,
+                                 _ptr(num_accepted_tokens), _ptr(cu_seqlens), _ptr(o), B, T, H, K, V, N,
+                                 flags, _ptr(workspace), _stream_handle(q.device))
+    if rc != 0:
+        raise KdaError(rc, "kda_fused_recurrent")
+
+
+def fused_recurrent(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                    state_pool: torch.Tensor, ssm_state_indices: torch.Tensor, scale: Optional[float] = None,
+                    num_accepted_tokens: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None,
+                    use_qk_l2norm_in_kernel: bool = False, workspace: Optional[torch.Tensor] = None
+                    ) -> torch.Tensor:
+    """Token-by-token KDA with an in-place state pool (the decode sibling of
+    ``fwd``).  q, k: bf16 [B,T,H,K]; v: bf16 [B,T,H,V]; g fp32 [B,T,H,K];
+    beta fp32 [B,T,H]; state_pool fp32 [P,H,V,K] (updated in place);
+    ssm_state_indices int32 [N] or [N, S]; num_accepted_tokens int32 [N] or
+    None; cu_seqlens int32 [N+1] (B == 1) or None.  Returns o bf16
+    [B,T,H,V]."""
+    _check("q", q, torch.bfloat16, 4)
+    _check("k", k, torch.bfloat16, 4)
+    _check("v", v, torch.bfloat16, 4)
+    _check("g", g, torch.float32, 4)
+    _check("beta", beta, torch.float32, 3)
+    _check("state_pool", state_pool, torch.float32, 4)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if k.shape != q.shape or g.shape != q.shape or v.shape[:3] != q.shape[:3] or beta.shape != q.shape[:3]:
+        raise ValueError("shape mismatch among q, k, v, g, beta")
+    if tuple(state_pool.shape[1:]) != (H, V, K) or not state_pool.is_contiguous():
+        raise ValueError(f"state_pool must be a contiguous [P, {H}, {V}, {K}] tensor")
+    idx = ssm_state_indices
+    if idx.dtype != torch.int32 or not idx.is_cuda or idx.dim() not in (1, 2):
+        raise ValueError("ssm_state_indices must be a CUDA int32 tensor [N] or [N, S]")
+    idx = idx.reshape(idx.shape[0], -1).contiguous()
+    N = idx.shape[0]
+    if cu_seqlens is not None:
+        _check("cu_seqlens", cu_seqlens, torch.int32, 1)
+        if cu_seqlens.numel() != N + 1:
+            raise ValueError("cu_seqlens must have N + 1 entries")
+    if num_accepted_tokens is not None:
+        _check("num_accepted_tokens", num_accepted_tokens, torch.int32, 1)
+        if num_accepted_tokens.numel() != N:
+            raise ValueError("num_accepted_tokens must have N entries")
+    dev = q.device
+    q, k, v, g, beta = (t.contiguous() for t in (q, k, v, g, beta))
+    o = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=dev)
+    if workspace is None or workspace.numel() * workspace.element_size() < RECURRENT_WORKSPACE_BYTES:
+        workspace = torch.empty(RECURRENT_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
+    flags = KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0
+    with torch.cuda.device(dev):
+        kda_fused_recurrent(q, k, v, g, beta, scale, state_pool, idx, num_accepted_tokens, cu_seqlens, o, N,
+                            flags, workspace)
+    return o

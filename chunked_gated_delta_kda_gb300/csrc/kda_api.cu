@@ -119,6 +119,7 @@ kda_status kda_get_status(const void* workspace, cudaStream_t stream) {
     if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return KDA_ERR_CUDA;
     if (word & kda::STATUS_BAD_CU) return KDA_ERR_BAD_CU_SEQLENS;
     if (word & kda::STATUS_TIMEOUT) return KDA_ERR_TIMEOUT;
+    if (word & kda::STATUS_BAD_INDEX) return KDA_ERR_BAD_STATE_INDEX;
     return KDA_OK;
 }
 
@@ -131,6 +132,7 @@ const char* kda_status_str(kda_status status) {
         case KDA_ERR_BAD_CU_SEQLENS: return "device found cu_seqlens invalid";
         case KDA_ERR_TIMEOUT: return "a bounded device wait ran out";
         case KDA_ERR_TOO_LARGE: return "problem too large for the static no-alloc scratch";
+        case KDA_ERR_BAD_STATE_INDEX: return "device found a state slot index or accepted-token count out of range";
     }
     return "unknown status";
 }

@@ -53,6 +53,7 @@ constexpr uint32_t TILE_BYTES = TILE_DG + KD * 4;            // 131584
 // first 16 bytes are cleared at the start of every call.
 constexpr uint32_t STATUS_BAD_CU = 1u;
 constexpr uint32_t STATUS_TIMEOUT = 2u;
+constexpr uint32_t STATUS_BAD_INDEX = 4u;   // token-by-token kernel: a state slot out of range
 constexpr uint32_t WS_HEADER = 256;
 constexpr uint32_t WS_CLEAR = 16;
 

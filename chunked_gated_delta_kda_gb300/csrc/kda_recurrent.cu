@@ -1,0 +1,297 @@
+// Token-by-token KDA ("fused recurrent"): the decode-phase sibling of the
+// chunked forward.  Page "PyPTO-Gym chunk_kda operator: an NPU forward of
+// chunked gated delta-rule linear attention", section "与其他 KDA 算子的关系"
+// (relation to the other KDA operators): fused_recurrent_kda keeps an fp32
+// [H, V, K] state per sequence and steps it one token at a time, with the
+// state updated in place at a slot named by ssm_state_indices, speculative
+// decoding through num_accepted_tokens, and the optional in-kernel q/k L2
+// normalisation.  Per token (section "算子定位与算法背景"):
+//   S <- diag(exp(g)) S;   S <- S + beta k (v - S^T k)^T;   o = S^T (scale q)
+//
+// In the page's [V, K] state layout every value row v is independent:
+//   s_v <- s_v * exp(g);   s_v <- s_v + beta (v_v - k.s_v) k;   o_v = q.s_v
+// so a warp owns 8 value rows, each lane 4 consecutive K entries of each
+// (32 fp32 registers), and the two dot products per row are warp reductions.
+// A CTA of 4 warps covers 32 value rows of one (sequence, head); the grid is
+// (V / 32, H, N).  The state is read once and written once per call (once
+// per token in speculative mode), so the kernel is bound by HBM traffic on
+// the state, 2 x 64 KiB per (sequence, head).
+#include <cuda_bf16.h>
+
+#include "kda.h"
+#include "kda_common.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int REC_THREADS = 128;
+constexpr int REC_ROWS = 8;                       // value rows per warp
+constexpr int REC_ROWS_CTA = REC_ROWS * (REC_THREADS / 32);
+
+struct RecParams {
+    const uint16_t* q;          // bf16 [B*T, H, K]
+    const uint16_t* k;          // bf16 [B*T, H, K]
+    const uint16_t* v;          // bf16 [B*T, H, V]
+    const float* g;             // fp32 [B*T, H, K]
+    const float* beta;          // fp32 [B*T, H]
+    float* pool;                // fp32 [pool_slots, H, V, K], updated in place
+    const int32_t* idx;         // int32 [N, stride]
+    const int32_t* nacc;        // int32 [N] or null
+    const int32_t* cu;          // int32 [N+1] or null
+    uint16_t* o;                // bf16 [B*T, H, V]
+    uint32_t* status;
+    float scale;
+    int T, H, N, pool_slots, stride, l2norm;
+};
+
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+    return x;
+}
+
+// All-reduce eight per-lane partial sums over the warp: a reduce-scatter by
+// halving (xor 16, 8, 4: each step keeps half of the rows and adds the
+// partner's half), a butterfly over the last two lane bits, then a gather of
+// the eight totals.  17 shuffles instead of 40.
+__device__ __forceinline__ void warp_sum8(float (&a)[REC_ROWS], int lane) {
+    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
+    float b[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float send = h16 ? a[j] : a[j + 4];
+        const float keep = h16 ? a[j + 4] : a[j];
+        b[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    float c[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float send = h8 ? b[j] : b[j + 2];
+        const float keep = h8 ? b[j + 2] : b[j];
+        c[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float d;
+    {
+        const float send = h4 ? c[0] : c[1];
+        const float keep = h4 ? c[1] : c[0];
+        d = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    d += __shfl_xor_sync(0xffffffffu, d, 2);
+    d += __shfl_xor_sync(0xffffffffu, d, 1);
+    // lane holds the total of row 4*h16 + 2*h8 + h4; fetch every row's total
+#pragma unroll
+    for (int r = 0; r < REC_ROWS; ++r)
+        a[r] = __shfl_sync(0xffffffffu, d, ((r >> 2) << 4) | (((r >> 1) & 1) << 3) | ((r & 1) << 2));
+}
+
+__device__ __forceinline__ void load4_bf16(const uint16_t* p, float (&x)[4]) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    x[0] = __uint_as_float(u.x << 16);
+    x[1] = __uint_as_float(u.x & 0xffff0000u);
+    x[2] = __uint_as_float(u.y << 16);
+    x[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+
+__device__ __forceinline__ void store_rows(float* dst, const float (&s)[REC_ROWS][4], int lane) {
+#pragma unroll
+    for (int r = 0; r < REC_ROWS; ++r)
+        *reinterpret_cast<float4*>(dst + (size_t)r * KD + 4 * lane) = make_float4(s[r][0], s[r][1], s[r][2], s[r][3]);
+}
+
+__device__ __forceinline__ void zero_output(const RecParams& p, long long bos, int len, int h, int v0, int lane) {
+    if (lane != 0) return;
+    for (int t = 0; t < len; ++t)
+        *reinterpret_cast<uint4*>(p.o + ((size_t)(bos + t) * p.H + h) * VD + v0) = make_uint4(0, 0, 0, 0);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(REC_THREADS) kda_recurrent_kernel(const RecParams p) {
+    const int h = (int)blockIdx.y, n = (int)blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int v0 = (int)blockIdx.x * REC_ROWS_CTA + warp * REC_ROWS;
+    const int H = p.H;
+    const bool first = blockIdx.x == 0 && threadIdx.x == 0;   // reports errors once per (n, h)
+
+    // sequence bounds (section "主机侧 wrapper 与输入校验": fixed length is N = B
+    // sequences of T tokens; varlen offsets come from cu_seqlens on the device)
+    long long bos;
+    int len;
+    if (p.cu == nullptr) {
+        bos = (long long)n * p.T;
+        len = p.T;
+    } else {
+        const int a = p.cu[n], b = p.cu[n + 1];
+        if (a < 0 || b < a || b > p.T || (n == 0 && a != 0) || (n == p.N - 1 && b != p.T)) {
+            if (first && h == 0) atomicOr(p.status, STATUS_BAD_CU);
+            return;
+        }
+        bos = a;
+        len = b - a;
+    }
+    if (len == 0) return;
+
+    // state slots: read slot, and (speculative mode) one write slot per token
+    const int32_t* row = p.idx + (size_t)n * p.stride;
+    int rslot;
+    if (p.nacc == nullptr) {
+        rslot = row[0];
+    } else {
+        const int acc = p.nacc[n];
+        bool ok = acc >= 1 && acc <= p.stride && len <= p.stride;
+        if (ok) {
+            for (int t = 0; t < len; ++t) ok = ok && row[t] < p.pool_slots;
+        }
+        if (!ok) {
+            if (first && h == 0) atomicOr(p.status, STATUS_BAD_INDEX);
+            zero_output(p, bos, len, h, v0, lane);
+            return;
+        }
+        rslot = row[acc - 1];
+    }
+    if (rslot >= p.pool_slots) {
+        if (first && h == 0) atomicOr(p.status, STATUS_BAD_INDEX);
+        zero_output(p, bos, len, h, v0, lane);
+        return;
+    }
+    if (rslot < 0) {   // padding entry: no state, no output
+        zero_output(p, bos, len, h, v0, lane);
+        return;
+    }
+
+    float s[REC_ROWS][4];
+    {
+        const float* src = p.pool + (((size_t)rslot * H + h) * VD + v0) * KD;
+#pragma unroll
+        for (int r = 0; r < REC_ROWS; ++r) {
+            const float4 x = *reinterpret_cast<const float4*>(src + (size_t)r * KD + 4 * lane);
+            s[r][0] = x.x; s[r][1] = x.y; s[r][2] = x.z; s[r][3] = x.w;
+        }
+    }
+
+    for (int t = 0; t < len; ++t) {
+        const size_t tok = (size_t)(bos + t) * H + h;
+        float qv[4], kv[4];
+        load4_bf16(p.q + tok * KD + 4 * lane, qv);
+        load4_bf16(p.k + tok * KD + 4 * lane, kv);
+        const float4 gv = *reinterpret_cast<const float4*>(p.g + tok * KD + 4 * lane);
+        const float bt = p.beta[tok];
+        const uint4 vu = *reinterpret_cast<const uint4*>(p.v + tok * VD + v0);
+        float vv[REC_ROWS];
+        vv[0] = __uint_as_float(vu.x << 16); vv[1] = __uint_as_float(vu.x & 0xffff0000u);
+        vv[2] = __uint_as_float(vu.y << 16); vv[3] = __uint_as_float(vu.y & 0xffff0000u);
+        vv[4] = __uint_as_float(vu.z << 16); vv[5] = __uint_as_float(vu.z & 0xffff0000u);
+        vv[6] = __uint_as_float(vu.w << 16); vv[7] = __uint_as_float(vu.w & 0xffff0000u);
+
+        float qs = p.scale, ks = 1.f;
+        if (p.l2norm) {   // x / sqrt(sum x^2 + 1e-6), section "测试与验证体系"
+            const float sq = warp_sum(qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3]);
+            const float sk = warp_sum(kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3]);
+            qs *= rsqrtf(sq + 1e-6f);
+            ks = rsqrtf(sk + 1e-6f);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            qv[i] *= qs;
+            kv[i] *= ks;
+        }
+        const float e[4] = {__expf(gv.x), __expf(gv.y), __expf(gv.z), __expf(gv.w)};
+
+        // decay, then k . s_v
+        float dot[REC_ROWS];
+#pragma unroll
+        for (int r = 0; r < REC_ROWS; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                s[r][i] *= e[i];
+                acc = fmaf(kv[i], s[r][i], acc);
+            }
+            dot[r] = acc;
+        }
+        warp_sum8(dot, lane);
+        // delta update, then q . s_v
+#pragma unroll
+        for (int r = 0; r < REC_ROWS; ++r) {
+            const float delta = bt * (vv[r] - dot[r]);
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                s[r][i] = fmaf(kv[i], delta, s[r][i]);
+                acc = fmaf(qv[i], s[r][i], acc);
+            }
+            dot[r] = acc;
+        }
+        warp_sum8(dot, lane);
+        if (lane == 0) {
+            __nv_bfloat162 o2[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o2[j] = __floats2bfloat162_rn(dot[2 * j], dot[2 * j + 1]);
+            *reinterpret_cast<uint4*>(p.o + tok * VD + v0) = *reinterpret_cast<const uint4*>(o2);
+        }
+        if (p.nacc != nullptr) {   // speculative mode: the state after token t goes to slot row[t]
+            const int ws = row[t];
+            if (ws >= 0) store_rows(p.pool + (((size_t)ws * H + h) * VD + v0) * KD, s, lane);
+        }
+    }
+    if (p.nacc == nullptr) store_rows(p.pool + (((size_t)rslot * H + h) * VD + v0) * KD, s, lane);
+}
+
+}  // namespace kda
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+
+extern "C" kda_status kda_fused_recurrent(const void* q, const void* k, const void* v, const float* g,
+                                          const float* beta, float scale, float* state_pool, int pool_slots,
+                                          const int32_t* ssm_state_indices, int indices_stride,
+                                          const int32_t* num_accepted_tokens, const int32_t* cu_seqlens,
+                                          void* o, int B, int T, int H, int K, int V, int N, unsigned flags,
+                                          void* workspace, cudaStream_t stream) {
+    using namespace kda;
+    if (K != KD || V != VD) return KDA_ERR_UNSUPPORTED;
+    if (B < 0 || T < 0 || H <= 0 || N < 0 || pool_slots <= 0 || indices_stride <= 0) return KDA_ERR_INVALID_ARG;
+    if ((flags & ~KDA_FLAG_QK_L2NORM) != 0u) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens == nullptr) {
+        if (N != B) return KDA_ERR_INVALID_ARG;
+    } else if (B != 1) {
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0u) return KDA_ERR_INVALID_ARG;
+    if (state_pool == nullptr || ssm_state_indices == nullptr) return KDA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(state_pool) & 15u) != 0u) return KDA_ERR_INVALID_ARG;
+    const bool any_tokens = (long long)B * T > 0;
+    if (any_tokens) {
+        const void* ptrs[] = {q, k, v, g, beta, o};
+        for (const void* ptr : ptrs)
+            if (ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0u) return KDA_ERR_INVALID_ARG;
+    }
+    if (cudaMemsetAsync(workspace, 0, WS_CLEAR, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (!any_tokens || N == 0) return KDA_OK;
+
+    RecParams p;
+    p.q = static_cast<const uint16_t*>(q);
+    p.k = static_cast<const uint16_t*>(k);
+    p.v = static_cast<const uint16_t*>(v);
+    p.g = g;
+    p.beta = beta;
+    p.pool = state_pool;
+    p.idx = ssm_state_indices;
+    p.nacc = num_accepted_tokens;
+    p.cu = cu_seqlens;
+    p.o = static_cast<uint16_t*>(o);
+    p.status = static_cast<uint32_t*>(workspace);
+    p.scale = (scale > 0.f) ? scale : 0.08838834764831845f;   // 128^-0.5
+    p.T = cu_seqlens == nullptr ? T : B * T;
+    p.H = H;
+    p.N = N;
+    p.pool_slots = pool_slots;
+    p.stride = indices_stride;
+    p.l2norm = (flags & KDA_FLAG_QK_L2NORM) ? 1 : 0;
+    const dim3 grid((unsigned)(VD / REC_ROWS_CTA), (unsigned)H, (unsigned)N);
+    kda_recurrent_kernel<<<grid, REC_THREADS, 0, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}

@@ -114,3 +114,64 @@ def custom(name: str, B: int, T: int, H: int, seqlens=None, with_h0=False, seed=
     """A workload with the same distributions and other sizes (tests use these)."""
     return Workload(name, B=B, T=T, H=H, seqlens=tuple(seqlens) if seqlens else None,
                     with_h0=with_h0, seed=seed, gate_div=gate_div)
+
+
+def make_decode_inputs(N: int, H: int, lens, pool_slots: int, stride: int = 1, spec: bool = False,
+                       pad: Sequence[int] = (), seed: int = 0, gate_div: float = 16.0, K: int = 128,
+                       V: int = 128, device: str = "cpu", draw_on_device: bool = False):
+    """Inputs of the token-by-token (decode) entry point, with the same
+    distributions as the forward recipe.
+
+    ``lens`` is an int (fixed length: B = N sequences of that many tokens) or
+    a list of N lengths (varlen: B = 1, packed, with cu_seqlens).  The state
+    pool is 0.1 * N(0,1) [pool_slots, H, V, K]; each sequence gets ``stride``
+    distinct slots drawn without replacement (so no two sequences share one);
+    sequences listed in ``pad`` get slot -1 in every column (padding
+    entries).  With ``spec`` the accepted-token counts are drawn uniformly
+    from [1, stride].  Returns a dict with q, k, v, g, beta, pool, indices
+    (int32 [N, stride]), num_accepted (int32 [N] or None), cu_seqlens (int32
+    or None), B, T, N."""
+    gdev = device if draw_on_device else "cpu"
+    gen = torch.Generator(device=gdev)
+    gen.manual_seed(int(seed))
+    if isinstance(lens, int):
+        B, T, seqlens = N, lens, None
+    else:
+        seqlens = [int(x) for x in lens]
+        assert len(seqlens) == N
+        B, T = 1, sum(seqlens)
+    assert N * stride <= pool_slots
+
+    def randn(shape):
+        return torch.randn(shape, generator=gen, dtype=torch.float32, device=gdev)
+
+    def unit_rows(shape):
+        x = randn(shape)
+        x = x / x.norm(dim=-1, keepdim=True)
+        return x.to(torch.bfloat16)
+
+    q = unit_rows((B, T, H, K))
+    k = unit_rows((B, T, H, K))
+    v = randn((B, T, H, V)).to(torch.bfloat16)
+    g = F.logsigmoid(randn((B, T, H, K))) / gate_div
+    beta = torch.sigmoid(randn((B, T, H)))
+    pool = 0.1 * randn((pool_slots, H, V, K))
+    perm = torch.randperm(pool_slots, generator=torch.Generator().manual_seed(int(seed) + 7919))
+    indices = perm[: N * stride].reshape(N, stride).to(torch.int32)
+    for n in pad:
+        indices[n] = -1
+    num_accepted = None
+    if spec:
+        num_accepted = torch.randint(1, stride + 1, (N,), generator=torch.Generator().manual_seed(int(seed) + 31),
+                                     dtype=torch.int32)
+    cu = None
+    if seqlens is not None:
+        c = [0]
+        for s in seqlens:
+            c.append(c[-1] + s)
+        cu = torch.tensor(c, dtype=torch.int32)
+    out = dict(q=q, k=k, v=v, g=g, beta=beta, pool=pool, indices=indices, num_accepted=num_accepted,
+               cu_seqlens=cu, B=B, T=T, N=N)
+    if device != "cpu":
+        out = {kk: (vv.to(device) if isinstance(vv, torch.Tensor) else vv) for kk, vv in out.items()}
+    return out

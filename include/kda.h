@@ -46,8 +46,10 @@ typedef enum {
     KDA_ERR_CUDA = 3,            /* a CUDA runtime call failed */
     KDA_ERR_BAD_CU_SEQLENS = 4,  /* device found cu_seqlens invalid (via kda_get_status) */
     KDA_ERR_TIMEOUT = 5,         /* a bounded device wait ran out (via kda_get_status) */
-    KDA_ERR_TOO_LARGE = 6        /* kda_fwd_noalloc: the problem needs more workspace than
+    KDA_ERR_TOO_LARGE = 6,       /* kda_fwd_noalloc: the problem needs more workspace than
                                     the library's static scratch holds */
+    KDA_ERR_BAD_STATE_INDEX = 7  /* kda_fused_recurrent: device found a state slot index or an
+                                    accepted-token count out of range (via kda_get_status) */
 } kda_status;
 
 /* Apply the per-token L2 normalisation x / sqrt(sum(x^2) + 1e-6) to q and k
@@ -86,8 +88,9 @@ size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int N);
  *   stream      CUDA stream for every launch
  *
  * Precision: bf16 inputs, fp32 gate prefix sums, fp32 (I+A)^-1 and fp32
- * state; tensor-core products use bf16 operands for the gated q.k / k.k
- * matrices and fp16 operands for the rest, always with fp32 accumulation.
+ * state; tensor-core products take fp16 operands with fp32 accumulation
+ * (bf16 operands for the gated q.k / k.k products of chunks whose in-chunk
+ * decay is too strong for fp16 factors).
  * The gated products are factored around the chunk's middle row; factors are
  * capped at e^80, so results are exact (up to rounding) while the gate decay
  * over any 64 tokens of a chunk stays below 80 in each dimension.
@@ -112,8 +115,9 @@ kda_status kda_fwd_timed(const void* q, const void* k, const void* v, const floa
 
 /*
  * Synchronise `stream`, then read the device status word that the last
- * kda_fwd on this workspace wrote.  Returns KDA_OK, KDA_ERR_BAD_CU_SEQLENS,
- * KDA_ERR_TIMEOUT, or KDA_ERR_CUDA if synchronising or reading failed.
+ * kda_fwd or kda_fused_recurrent on this workspace wrote.  Returns KDA_OK,
+ * KDA_ERR_BAD_CU_SEQLENS, KDA_ERR_TIMEOUT, KDA_ERR_BAD_STATE_INDEX, or
+ * KDA_ERR_CUDA if synchronising or reading failed.
  */
 kda_status kda_get_status(const void* workspace, cudaStream_t stream);
 
@@ -147,6 +151,56 @@ kda_status kda_get_status(const void* workspace, cudaStream_t stream);
 kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                            float scale, const float* h0, const int32_t* cu_seqlens, void* o, float* ht,
                            int B, int T, int H, int K, int V, int N, unsigned flags, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace kda_fused_recurrent needs: the status word only.
+ */
+#define KDA_RECURRENT_WORKSPACE_BYTES 256u
+
+/*
+ * Token-by-token KDA with an in-place state pool: the decode-phase sibling
+ * of kda_fwd (page "PyPTO-Gym chunk_kda operator", section "与其他 KDA 算子
+ * 的关系": fused_recurrent_kda keeps an fp32 [H, V, K] state per sequence,
+ * updates it in place at slots given by ssm_state_indices, supports
+ * speculative decoding through num_accepted_tokens and the in-kernel q/k L2
+ * normalisation).  Per token the same recurrence as kda_fwd (decay, delta
+ * update, read-out), evaluated directly, one token after another.
+ *
+ *   q, k, v, g, beta, scale, cu_seqlens, o, B, T, H, K, V, N, flags
+ *               as for kda_fwd, except that fixed-length T need not be a
+ *               multiple of 128 (decode is typically T = 1 per sequence)
+ *   state_pool  fp32 [pool_slots, H, V, K]: the states, read and written in
+ *               place (same transposed layout as h0 / ht of kda_fwd)
+ *   ssm_state_indices  int32 [N, indices_stride], device.  Row n names the
+ *               slots of sequence n.
+ *   num_accepted_tokens  int32 [N] device, or NULL.
+ *     NULL (plain decode): sequence n starts from slot idx[n][0] and its
+ *       final state is written back to that slot.  A negative slot marks a
+ *       padding entry: the sequence is skipped, its output rows are zero
+ *       and no state is read or written.
+ *     non-NULL (speculative decoding): sequence n (at most indices_stride
+ *       tokens) starts from slot idx[n][num_accepted_tokens[n] - 1], and the
+ *       state after its token t is written to slot idx[n][t] (skipped where
+ *       that slot is negative), so a verifier can resume from any accepted
+ *       prefix.  num_accepted_tokens[n] must lie in [1, indices_stride].
+ *     The pages name these two arguments without defining them further;
+ *     this is the reading the library implements.
+ *   workspace   device scratch of KDA_RECURRENT_WORKSPACE_BYTES, 256-byte
+ *               aligned: the device status word, read with kda_get_status().
+ *
+ * Slots of different sequences must be distinct (two sequences writing one
+ * slot race).  A slot >= pool_slots or an accepted count out of range sets
+ * KDA_ERR_BAD_STATE_INDEX in the status word; that sequence's output rows
+ * are zero and its states are left untouched.  An invalid cu_seqlens sets
+ * KDA_ERR_BAD_CU_SEQLENS and the kernel does nothing for the bad entries.
+ * Precision: fp32 state and arithmetic, bf16 output (round to nearest even).
+ */
+kda_status kda_fused_recurrent(const void* q, const void* k, const void* v, const float* g,
+                               const float* beta, float scale, float* state_pool, int pool_slots,
+                               const int32_t* ssm_state_indices, int indices_stride,
+                               const int32_t* num_accepted_tokens, const int32_t* cu_seqlens, void* o,
+                               int B, int T, int H, int K, int V, int N, unsigned flags, void* workspace,
+                               cudaStream_t stream);
 
 /* Static English description of a status code. */
 const char* kda_status_str(kda_status status);

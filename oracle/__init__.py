@@ -13,8 +13,11 @@ Two independent forms:
   * ``kda_chunked``: the chunked M1-M4 form in numpy fp64 with an explicit
     triangular solve (``chunked.py``).  It equals the recurrence up to rounding
     order and serves to pin the chunked reading of the page.
+  * ``fused_recurrent``: the token-by-token recurrence with an in-place state
+    pool, slot indices and speculative-decoding checkpoints, numpy fp64
+    (``decode.py``): the oracle of the decode entry point.
 
-Parity pins for both live in ``tests/test_oracle.py``.
+Parity pins live in ``tests/test_oracle.py`` and ``tests/test_oracle_decode.py``.
 """
 
 from __future__ import annotations
@@ -26,6 +29,7 @@ import subprocess
 import numpy as np
 
 from .chunked import kda_chunked  # noqa: F401
+from .decode import fused_recurrent  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kda_recurrent.c")

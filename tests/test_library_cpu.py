@@ -41,7 +41,7 @@ def test_workspace_bytes():
 def test_status_strings():
     from chunked_gated_delta_kda_gb300 import binding
     lib = binding.load_library()
-    for code in range(7):
+    for code in range(8):
         assert lib.kda_status_str(code)
     assert b"unknown" in lib.kda_status_str(99)
 
@@ -76,3 +76,41 @@ def test_host_validation_rejects_before_any_cuda_call():
     misaligned = ctypes.c_void_p(p.value + 8)
     assert call(o=misaligned) == 1          # 16-byte alignment
     assert call(ws=misaligned) == 1         # 256-byte workspace alignment
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-pointer validation cases run on CPU-only hosts")
+def test_fused_recurrent_host_validation():
+    """kda_fused_recurrent's host checks fail before any CUDA call."""
+    from chunked_gated_delta_kda_gb300 import binding
+    lib = binding.load_library()
+    buf = (ctypes.c_uint8 * 4096)()
+    p = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf) % 256), ctypes.c_void_p)
+
+    def call(**kw):
+        a = dict(q=p, k=p, v=p, g=p, beta=p, scale=0.0, pool=p, P=4, idx=p, stride=1, acc=None, cu=None, o=p,
+                 B=2, T=1, H=1, K=128, V=128, N=2, flags=0, ws=p)
+        a.update(kw)
+        return lib.kda_fused_recurrent(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["pool"], a["P"],
+                                       a["idx"], a["stride"], a["acc"], a["cu"], a["o"], a["B"], a["T"], a["H"],
+                                       a["K"], a["V"], a["N"], a["flags"], a["ws"], None)
+
+    assert call(K=64) == 2
+    assert call(V=64) == 2
+    assert call(pool=None) == 1
+    assert call(idx=None) == 1
+    assert call(ws=None) == 1
+    assert call(q=None) == 1
+    assert call(P=0) == 1
+    assert call(stride=0) == 1
+    assert call(N=3) == 1                   # fixed length needs N == B
+    assert call(cu=p) == 1                  # varlen needs B == 1
+    assert call(flags=2) == 1
+    misaligned = ctypes.c_void_p(p.value + 8)
+    assert call(pool=misaligned) == 1
+    assert call(ws=misaligned) == 1
+
+
+def test_decode_status_string():
+    from chunked_gated_delta_kda_gb300 import binding
+    lib = binding.load_library()
+    assert b"slot" in lib.kda_status_str(7)
