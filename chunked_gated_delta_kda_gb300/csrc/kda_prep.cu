@@ -207,10 +207,6 @@ __device__ __forceinline__ void tile16_store(const float (&c)[2][4], float* M, i
     }
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // 128B-swizzled tile operand: K-major (rows = M or N, 128 B of K per row,
 // 64-wide K slabs `rows` rows apart) or MN-major (rows = K, 64-wide MN atoms
 // one slab apart).
@@ -254,17 +250,38 @@ __device__ __forceinline__ void sync_for_mma() {
     tc_fence_after();
 }
 
-// L2 prefetch of one chunk's input rows (q, k, v, g), one row per thread.
+__device__ __forceinline__ void prefetch_line(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
+// L2 prefetch of one chunk's input rows (q, k, v, g): one row per thread,
+// one 128-byte line per instruction.  Plain line prefetches go through the
+// load path; bulk prefetches would queue behind the previous tile's bulk
+// stores and stall the issuing threads.
 __device__ __forceinline__ void prefetch_chunk(const FwdParams& p, const ChunkRef& c, int h, int tid) {
     const int t = tid & 127;
     if (t >= c.len) return;
     const size_t row = (size_t)(c.tok0 + t) * p.H + h;
-    if (tid < 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.beta + row) : "memory");
     switch (tid >> 7) {
-        case 0: prefetch_l2(p.q + row * KD, KD * 2); break;
-        case 1: prefetch_l2(p.k + row * KD, KD * 2); break;
-        case 2: prefetch_l2(p.v + row * VD, VD * 2); break;
-        default: prefetch_l2(p.g + row * KD, KD * 4); break;
+        case 0:
+            prefetch_line(p.beta + row);
+            prefetch_line(p.q + row * KD);
+            prefetch_line(p.q + row * KD + 64);
+            break;
+        case 1:
+            prefetch_line(p.k + row * KD);
+            prefetch_line(p.k + row * KD + 64);
+            break;
+        case 2:
+            prefetch_line(p.v + row * VD);
+            prefetch_line(p.v + row * VD + 64);
+            break;
+        default:
+            prefetch_line(p.g + row * KD);
+            prefetch_line(p.g + row * KD + 32);
+            prefetch_line(p.g + row * KD + 64);
+            prefetch_line(p.g + row * KD + 96);
+            break;
     }
 }
 
@@ -354,6 +371,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
         phase ^= 1;
         tc_fence_after();
     };
+
 
     while (have && *sFlag == 0) {
         long long nidx = idx + gridDim.x, nitem = 0;
@@ -511,7 +529,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 unpack8_bf16(kc, kf);
                 unpack8_bf16(qc, qf);
                 unpack8_bf16(vc, vf);
-                const float ik = sInvK[t], iq = sInvQ[t];
+                const float ik = L2NORM ? sInvK[t] : 1.f, iq = sInvQ[t];
                 uint32_t lk[4], lqv[4], rk[4], v16[4];
 #pragma unroll
                 for (int j = 0; j < 8; j += 2) {
@@ -628,8 +646,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 }
             }
         }
-        // The fast variant hands chunks it cannot hold in fp16 to the wide one.
-        if (FAST && __syncthreads_or(unsafe)) {
+        // The fast variant hands chunks it cannot hold in fp16 to the wide
+        // one.  The same barrier hands the operands to the tensor core.
+        fence_async_smem();
+        tc_fence_before();
+        const bool to_wide = __syncthreads_or(FAST && unsafe) != 0;
+        tc_fence_after();
+        if (to_wide) {
             if (tid == 0) {
                 const uint32_t slot_i = atomicAdd(p.wide_count, 1u);
                 p.wide_list[slot_i] = (int32_t)item;
@@ -637,7 +660,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             if (have_n) prefetch_chunk(p, cn, hn, tid);
             __syncthreads();
         } else {
-            sync_for_mma();
             if (tid == 0) {
                 const uint32_t id = idesc_f16(FAST ? T_F16 : T_BF16, 128, 128, false, false);
                 const Operand Lk{sbase + MP::LK, false, 128}, Lq{sbase + MP::LQ, false, 128},
@@ -905,16 +927,21 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             {
                 uint8_t* dst = tile_ptr(p, c.slot, h);
                 const bool second = warp >= 8;
-                const int half = (warp >> 2) & 1;     // which 128 columns of the 256
+                const int half = (warp >> 2) & 1;
                 const float rs = (FAST && !second) ? sCL[trow] : 1.f;
+                // 32-column blocks b = 2 part + half: blocks 0-3 are the first
+                // product (Nm, or Qe), blocks 4-7 the second (Bc, or Oi), so
+                // each warp does two of each (Qe costs more than Oi)
 #pragma unroll 1
                 for (int part = 0; part < 4; ++part) {
                     float x[32];
-                    const int col0 = half * 128 + part * 32;
+                    const int b = part * 2 + half;
+                    const int vt = b & 3;
+                    const int col0 = (b < 4 ? 0 : 128) + vt * 32;
                     tmem_ld32(tmem + lane_off + (second ? 256u : 0u) + (uint32_t)col0, x);
                     tmem_ld_wait();
                     if (!second) {
-                        if (half == 0) {
+                        if (b < 4) {
                             const float ns = -rs;
 #pragma unroll
                             for (int j = 0; j < 32; j += 8)
@@ -924,12 +951,12 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                         } else {
 #pragma unroll
                             for (int j = 0; j < 32; j += 8)
-                                sts_v4(sm, MP::ST_BC + part * BC_PIECE + sw64_off(trow, j), pack_f16(rs * x[j], rs * x[j + 1]),
+                                sts_v4(sm, MP::ST_BC + vt * BC_PIECE + sw64_off(trow, j), pack_f16(rs * x[j], rs * x[j + 1]),
                                        pack_f16(rs * x[j + 2], rs * x[j + 3]), pack_f16(rs * x[j + 4], rs * x[j + 5]),
                                        pack_f16(rs * x[j + 6], rs * x[j + 7]));
                         }
                     } else {
-                        if (half == 0) {
+                        if (b < 4) {
 #pragma unroll
                             for (int j = 0; j < 32; j += 8) {
                                 const uint4 qv = *reinterpret_cast<const uint4*>(sm + MP::QS + sw128_off(trow, col0 + j, 128));
@@ -948,7 +975,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                         } else {
 #pragma unroll
                             for (int j = 0; j < 32; j += 8)
-                                sts_v4(sm, MP::ST_OI + part * OI_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
+                                sts_v4(sm, MP::ST_OI + vt * OI_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
                                        pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]),
                                        pack_f16(x[j + 6], x[j + 7]));
                         }
