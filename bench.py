@@ -149,6 +149,35 @@ def algorithmic(w, N):
 
 
 # ---------------------------------------------------------------------------
+# Ranks: one process per GPU; the (sequence, head) units of a step are
+# independent, so every rank runs its own full copy of the workload (weak
+# scaling) and the only collectives are the barrier around the timed region
+# and the max of the elapsed times.
+# ---------------------------------------------------------------------------
+
+def rank_env():
+    """(world, rank, local_rank) from the torchrun environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, device, world: int) -> float:
+    """Max of a per-rank number over all ranks (all_reduce MAX; the identity
+    at world 1)."""
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: int, world: int, slowest_ms_per_step: float) -> float:
+    """Whole-job throughput: the units every rank processed, over the slowest
+    rank's time."""
+    return world * units_per_rank / (slowest_ms_per_step * 1e-3)
+
+
+# ---------------------------------------------------------------------------
 # CPU baseline / reference arm: the fp64 oracle on a bounded sample
 # ---------------------------------------------------------------------------
 
@@ -291,15 +320,12 @@ def run_decode(args, rank, world, local):
     t_end = time.time()
     clocks.stop()
     assert binding.get_status(ws) == 0
-    t = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms = float(t.item()) / args.steps
+    ms = max_over_ranks(e0.elapsed_time(e1), dev, world) / args.steps
     units = DECODE_N * DECODE_H
     peaks = load_peaks()
     achieved = units * DECODE_BYTES_PER_UNIT / (ms * 1e-3) / 1e9
     tr = load_traffic().get("kda_recurrent_kernel")
-    line = {"metric": DECODE_METRIC, "value": world * units / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+    line = {"metric": DECODE_METRIC, "value": job_rate(units, world, ms), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": name, "sequences": DECODE_N, "H": DECODE_H, "tokens_per_sequence": 1,
@@ -324,8 +350,8 @@ def run_decode(args, rank, world, local):
             o_host.copy_(o, non_blocking=True)
         f1.record(stream)
         torch.cuda.synchronize(dev)
-        te = f0.elapsed_time(f1) / args.e2e_steps
-        line["e2e"] = {"value": world * units / (te * 1e-3), "unit": UNIT,
+        te = max_over_ranks(f0.elapsed_time(f1) / args.e2e_steps, dev, world)
+        line["e2e"] = {"value": job_rate(units, world, te), "unit": UNIT,
                        "h2d_bytes_per_step": sum(tt.numel() * tt.element_size() for tt in host.values()),
                        "d2h_bytes_per_step": o_host.numel() * o_host.element_size(), "ms_per_step": te}
     line["clocks"] = clocks.summary(t_start, t_end)
@@ -358,9 +384,7 @@ def main():
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     w = WORKLOADS[args.workload]
 
     if args.op == "decode":
@@ -421,13 +445,10 @@ def main():
     st = binding.get_status(ws)
     assert st == 0, f"device status {st}"
 
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_per_step = float(t.item()) / args.steps
+    ms_per_step = max_over_ranks(total_ms, dev, world) / args.steps
 
     th, alg_bytes, alg_flop, dense_flop = algorithmic(w, N)
-    value = world * th / (ms_per_step * 1e-3)
+    value = job_rate(th, world, ms_per_step)
     peaks = load_peaks()
     t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
     t_tc = alg_flop / (peaks["bf16_tflops_sustained"] * 1e12)
@@ -498,11 +519,9 @@ def main():
             e2e_step()
         f1.record(stream)
         torch.cuda.synchronize(dev)
-        te = torch.tensor([f0.elapsed_time(f1) / args.e2e_steps], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        line["e2e"] = {"value": world * th / (float(te.item()) * 1e-3), "unit": UNIT,
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": float(te.item())}
+        te = max_over_ranks(f0.elapsed_time(f1) / args.e2e_steps, dev, world)
+        line["e2e"] = {"value": job_rate(th, world, te), "unit": UNIT,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": te}
         line["gpu_launches_e2e"] = 3 * args.e2e_steps
 
     line["clocks"] = clocks.summary(t_start, t_end)
