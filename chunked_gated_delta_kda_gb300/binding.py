@@ -63,6 +63,10 @@ def load_library(path: Optional[str] = None):
     lib.kda_fused_recurrent.restype = ctypes.c_int
     lib.kda_fused_recurrent.argtypes = [vp, vp, vp, vp, vp, f, vp, i, vp, i, vp, vp, vp,
                                         i, i, i, i, i, i, u, vp, vp]
+    lib.kda_kcp_workspace_bytes.restype = sz
+    lib.kda_kcp_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    lib.kda_kcp_fwd.restype = ctypes.c_int
+    lib.kda_kcp_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, u, vp, sz, vp]
     lib.kda_status_str.restype = ctypes.c_char_p
     lib.kda_status_str.argtypes = [i]
     _lib = lib
@@ -254,3 +258,45 @@ def fused_recurrent(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.
         kda_fused_recurrent(q, k, v, g, beta, scale, state_pool, idx, num_accepted_tokens, cu_seqlens, o, N,
                             flags, workspace)
     return o
+
+
+def kcp_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+            cu_seqlens, world_size: int, scale: Optional[float] = None,
+            initial_state: Optional[torch.Tensor] = None, output_final_state: bool = False,
+            use_qk_l2norm_in_kernel: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """KCP forward with ``world_size`` ranks simulated on q's device.
+    Packed inputs (B == 1) as for ``fwd``; ``cu_seqlens`` is a host sequence
+    of N + 1 offsets (list, numpy array or CPU tensor).  Returns (o, final
+    state or None)."""
+    _check("q", q, torch.bfloat16, 4)
+    _check("k", k, torch.bfloat16, 4)
+    _check("v", v, torch.bfloat16, 4)
+    _check("g", g, torch.float32, 4)
+    _check("beta", beta, torch.float32, 3)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if B != 1:
+        raise ValueError("kcp_fwd takes packed inputs (B == 1)")
+    cu = torch.as_tensor(cu_seqlens, dtype=torch.int32).cpu().contiguous()
+    N = cu.numel() - 1
+    dev = q.device
+    q, k, v, g, beta = (t.contiguous() for t in (q, k, v, g, beta))
+    h0 = initial_state.contiguous() if initial_state is not None else None
+    if h0 is not None and (h0.dtype != torch.float32 or tuple(h0.shape) != (N, H, V, K)):
+        raise ValueError(f"initial_state must be fp32 {(N, H, V, K)}")
+    o = torch.empty((1, T, H, V), dtype=torch.bfloat16, device=dev)
+    ht = torch.empty((N, H, V, K), dtype=torch.float32, device=dev) if output_final_state else None
+    lib = load_library()
+    nbytes = int(lib.kda_kcp_workspace_bytes(T, H, K, V, N, world_size))
+    if nbytes == 0:
+        raise KdaError(1, "kda_kcp_workspace_bytes")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    flags = KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0
+    with torch.cuda.device(dev):
+        rc = lib.kda_kcp_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                             float(scale if scale is not None else -1.0), _ptr(h0),
+                             ctypes.c_void_p(cu.data_ptr()), _ptr(o), _ptr(ht), T, H, K, V, N, world_size, flags,
+                             _ptr(ws), nbytes, _stream_handle(dev))
+    if rc != 0:
+        raise KdaError(rc, "kda_kcp_fwd")
+    return o, ht

@@ -50,7 +50,8 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const fl
     } else {
         if (B != 1) return KDA_ERR_INVALID_ARG;
     }
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) || !aligned16(o) ||
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || (reinterpret_cast<uintptr_t>(beta) & 3u) ||
+        !aligned16(o) ||
         (h0 && !aligned16(h0)) || (ht && !aligned16(ht)) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return KDA_ERR_INVALID_ARG;
     if (workspace_bytes < kda_fwd_workspace_bytes(B, T, H, K, V, N)) return KDA_ERR_INVALID_ARG;

@@ -265,9 +265,10 @@ extern "C" kda_status kda_fused_recurrent(const void* q, const void* k, const vo
     if ((reinterpret_cast<uintptr_t>(state_pool) & 15u) != 0u) return KDA_ERR_INVALID_ARG;
     const bool any_tokens = (long long)B * T > 0;
     if (any_tokens) {
-        const void* ptrs[] = {q, k, v, g, beta, o};
+        const void* ptrs[] = {q, k, v, g, o};
         for (const void* ptr : ptrs)
             if (ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0u) return KDA_ERR_INVALID_ARG;
+        if (beta == nullptr || (reinterpret_cast<uintptr_t>(beta) & 3u) != 0u) return KDA_ERR_INVALID_ARG;
     }
     if (cudaMemsetAsync(workspace, 0, WS_CLEAR, stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (!any_tokens || N == 0) return KDA_OK;

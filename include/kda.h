@@ -25,8 +25,8 @@
  *     the process is never terminated.  Faults the device detects (an invalid
  *     cu_seqlens, a wait that ran out) are recorded in the workspace status
  *     word and read with kda_get_status().
- *   - Tensor pointers must be 16-byte aligned; the tensors are contiguous in
- *     the stated layout.
+ *   - Tensor pointers must be 16-byte aligned (beta: 4-byte); the tensors are
+ *     contiguous in the stated layout.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -201,6 +201,44 @@ kda_status kda_fused_recurrent(const void* q, const void* k, const void* v, cons
                                const int32_t* num_accepted_tokens, const int32_t* cu_seqlens, void* o,
                                int B, int T, int H, int K, int V, int N, unsigned flags, void* workspace,
                                cudaStream_t stream);
+
+/*
+ * Bytes of device workspace kda_kcp_fwd needs (0 on invalid sizes).
+ */
+size_t kda_kcp_workspace_bytes(int T, int H, int K, int V, int N, int world_size);
+
+/*
+ * Kimi Context Parallel (KCP) forward, with world_size ranks simulated on
+ * this one device (page "flash-linear-attention KCP precision-debugging
+ * guide": the single-device KCP simulator that loops over ranks and calls
+ * the kernels directly).  The packed tokens [0, T) are cut into world_size
+ * contiguous rank slices, rank r owning [T r / W, T (r+1) / W), which may
+ * cut sequences anywhere.  Per rank: a pre-process computes, for its last
+ * local piece, the transition M_r and the zero-start state S_ext,r (two
+ * chunked forwards over that piece: v = 0 from the identity, and v from
+ * zero); a merge in rank order gives the state entering each rank
+ * (M_r S_start + S_ext,r); the local chunked forward then runs with that
+ * state as the initial state of the rank's first piece.  The result equals
+ * kda_fwd on the whole packed input up to rounding (chunk boundaries differ
+ * where the rank cuts are not multiples of 128 inside a sequence, so
+ * compare per token).
+ *
+ *   q, k, v, g, beta, scale, h0, o, ht, T, H, K, V, N, flags
+ *               as for kda_fwd in varlen packing (B = 1)
+ *   cu_seqlens_host  int32 [N+1] offsets in HOST memory: the rank split
+ *               needs them on the host (validated there: BAD_CU_SEQLENS)
+ *   world_size  number of simulated ranks, 1 .. 4096
+ *   workspace   device scratch of kda_kcp_workspace_bytes(...) bytes,
+ *               256-byte aligned
+ *
+ * The call synchronises `stream` once (after uploading the ranks' local
+ * offsets) and is otherwise asynchronous.  kda_get_status(workspace)
+ * reports the device status of the last internal forward.
+ */
+kda_status kda_kcp_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
+                       const float* h0, const int32_t* cu_seqlens_host, void* o, float* ht, int T, int H, int K,
+                       int V, int N, int world_size, unsigned flags, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
 
 /* Static English description of a status code. */
 const char* kda_status_str(kda_status status);

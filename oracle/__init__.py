@@ -30,6 +30,7 @@ import numpy as np
 
 from .chunked import kda_chunked  # noqa: F401
 from .decode import fused_recurrent  # noqa: F401
+from .kcp import kcp_forward  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kda_recurrent.c")

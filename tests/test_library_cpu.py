@@ -114,3 +114,21 @@ def test_decode_status_string():
     from chunked_gated_delta_kda_gb300 import binding
     lib = binding.load_library()
     assert b"slot" in lib.kda_status_str(7)
+
+
+def test_kcp_workspace_and_host_checks():
+    """kda_kcp_fwd's size function and its host-side checks (which run before
+    any CUDA call: unsupported sizes and invalid host offsets)."""
+    from chunked_gated_delta_kda_gb300 import binding
+    lib = binding.load_library()
+    assert lib.kda_kcp_workspace_bytes(1024, 4, 128, 128, 2, 2) > 0
+    assert lib.kda_kcp_workspace_bytes(1024, 4, 64, 128, 2, 2) == 0
+    assert lib.kda_kcp_workspace_bytes(1024, 4, 128, 128, 2, 0) == 0
+    buf = (ctypes.c_uint8 * 4096)()
+    p = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf) % 256), ctypes.c_void_p)
+    cu_bad = (ctypes.c_int32 * 3)(0, 200, 100)
+    big = 1 << 40
+    args = [p, p, p, p, p, 0.0, None, cu_bad, p, None, 100, 1, 128, 128, 2, 2, 0, p, big, None]
+    assert lib.kda_kcp_fwd(*args) == 4          # offsets not non-decreasing
+    args[12] = 64
+    assert lib.kda_kcp_fwd(*args) == 2          # K != 128
