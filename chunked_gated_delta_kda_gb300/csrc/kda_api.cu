@@ -121,6 +121,7 @@ kda_status kda_get_status(const void* workspace, cudaStream_t stream) {
     if (word & kda::STATUS_BAD_CU) return KDA_ERR_BAD_CU_SEQLENS;
     if (word & kda::STATUS_TIMEOUT) return KDA_ERR_TIMEOUT;
     if (word & kda::STATUS_BAD_INDEX) return KDA_ERR_BAD_STATE_INDEX;
+    if (word & kda::STATUS_DECAY_RANGE) return KDA_ERR_DECAY_RANGE;
     return KDA_OK;
 }
 
@@ -134,6 +135,8 @@ const char* kda_status_str(kda_status status) {
         case KDA_ERR_TIMEOUT: return "a bounded device wait ran out";
         case KDA_ERR_TOO_LARGE: return "problem too large for the static no-alloc scratch";
         case KDA_ERR_BAD_STATE_INDEX: return "device found a state slot index or accepted-token count out of range";
+        case KDA_ERR_DECAY_RANGE:
+            return "a chunk's gate decay exceeded the range of exact factored products; results are approximate";
     }
     return "unknown status";
 }

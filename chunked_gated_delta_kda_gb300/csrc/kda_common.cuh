@@ -54,6 +54,7 @@ constexpr uint32_t TILE_BYTES = TILE_DG + KD * 4;            // 131584
 constexpr uint32_t STATUS_BAD_CU = 1u;
 constexpr uint32_t STATUS_TIMEOUT = 2u;
 constexpr uint32_t STATUS_BAD_INDEX = 4u;   // token-by-token kernel: a state slot out of range
+constexpr uint32_t STATUS_DECAY_RANGE = 8u; // a chunk's in-chunk decay exceeded the exact range
 constexpr uint32_t WS_HEADER = 256;
 constexpr uint32_t WS_CLEAR = 16;
 

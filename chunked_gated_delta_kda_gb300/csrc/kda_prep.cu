@@ -605,6 +605,14 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             if (tid == 0) bulk_wait_read0();   // previous tile's bulk store has read its staging
             __syncthreads();
             const float P0 = sG64[d0], P1 = sG64[d0 + 1];
+            {   // beyond |G - P| = EXP2_CAP the capped factors no longer
+                // multiply back to exp(G_c - G_i): flag the result approximate
+                bool far = false;
+#pragma unroll
+                for (int r = 0; r < 16; ++r)
+                    far = far || fabsf(G0[r] - P0) > EXP2_CAP || fabsf(G1[r] - P1) > EXP2_CAP;
+                if (__any_sync(0xffffffffu, far) && lane == 0) atomicOr(p.status, STATUS_DECAY_RANGE);
+            }
             const float eP0 = ex2(P0), eP1 = ex2(P1);
             const float cL0 = ex2(fminf(sGL[d0] - P0, EXP2_CAP)), cL1 = ex2(fminf(sGL[d0 + 1] - P1, EXP2_CAP));
             // Lk, Lq, R bf16; RHS = [beta exp(G) k | beta v] fp16; qg fp16

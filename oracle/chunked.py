@@ -43,11 +43,13 @@ def _l2norm(x: np.ndarray) -> np.ndarray:
     return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + 1e-6)
 
 
-def chunk_step(S, qs, k, v, g, beta, BT):
+def chunk_step(S, qs, k, v, g, beta, BT, return_terms=False):
     """One chunk of M1-M4 for one (sequence, head).
 
     S: (K, V) state entering the chunk.  qs, k: (L, K); v: (L, V); g: (L, K);
-    beta: (L,), with L <= BT valid rows.  Returns (o (L, V), S_next (K, V)).
+    beta: (L,), with L <= BT valid rows.  Returns (o (L, V), S_next (K, V)),
+    and with ``return_terms`` also the two operands of M4's subtraction
+    v_new = u - w S as a third element (u, w S).
     """
     L = qs.shape[0]
     K = k.shape[1]
@@ -87,7 +89,21 @@ def chunk_step(S, qs, k, v, g, beta, BT):
     o = (qs_ * np.exp(G)) @ S + A2 @ v_new
     g_last = G[BT - 1]
     S_next = np.exp(g_last)[:, None] * S + (np.exp(g_last[None, :] - G) * k_).T @ v_new
+    if return_terms:
+        return o[:L], S_next, (u[:L], (w @ S)[:L])
     return o[:L], S_next
+
+
+def cancellation_ratio(S, k, v, g, beta, BT=128):
+    """How much of M4's subtraction v_new = u - w S cancels on one chunk:
+    ||u - w S|| / max(||u||, ||w S||) (Frobenius norms; near 0 = severe
+    cancellation).  Used to search for adversarial inputs (section "测试与验证
+    体系": the input generator's cancellation_stress mode searches random
+    scalings for this cancellation)."""
+    K = k.shape[1]
+    _, _, (u, wS) = chunk_step(S, np.zeros_like(k), k, v, g, beta, BT, return_terms=True)
+    den = max(np.linalg.norm(u), np.linalg.norm(wS), 1e-300)
+    return float(np.linalg.norm(u - wS) / den)
 
 
 def kda_chunked(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None,

@@ -41,7 +41,7 @@ def test_workspace_bytes():
 def test_status_strings():
     from chunked_gated_delta_kda_gb300 import binding
     lib = binding.load_library()
-    for code in range(8):
+    for code in range(9):
         assert lib.kda_status_str(code)
     assert b"unknown" in lib.kda_status_str(99)
 
