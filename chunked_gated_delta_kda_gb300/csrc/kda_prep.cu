@@ -92,7 +92,10 @@ struct Map {
     static constexpr uint32_t WU = FAST ? 0 : 98304;          // w | u (N = 256)
     static constexpr uint32_t KGT = FAST ? 98304 : 32768;     // A operand (MN-major) of the Nm | Bc product
     static constexpr uint32_t QS = FAST ? 65536 : 0;          // Lq (fast) or qg (wide) for the Qe epilogue
-    static constexpr uint32_t YA = Y, YP = Y + 8192, YQ = Y + 16384, YT = Y + 24576;
+    // level-3 merge tiles inside the Ainv region (A10, P, Q), T in the merge
+    // temps (free by then), so that Ainv's P and Q parts can be written
+    // while the last merge product runs
+    static constexpr uint32_t YA = Y, YP = Y + 8192, YQ = Y + 16384;
     // staging of the output tile for the bulk store (regions free by then)
     static constexpr uint32_t ST_NM = FAST ? 0 : 65536;
     static constexpr uint32_t ST_BC = 32768;
@@ -331,6 +334,9 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     const int cg = warp >> 2;             // column group (0..3) for TMEM read-backs
     const uint32_t lane_off = (uint32_t)(lq * 32) << 16;
     const int trow = lq * 32 + lane;      // TMEM lane = matrix row of this thread
+    // one thread in each 128-thread group issues (and later waits for) one of
+    // the four bulk tile stores
+    const bool bulk_thread = (tid & 127) == 0;
 
     float* sG64 = reinterpret_cast<float*>(sm + M_G64);
     float* sGL = reinterpret_cast<float*>(sm + M_GL);
@@ -501,7 +507,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                     for (int j = 0; j < 8; ++j) sGL[d8 + j] = G[3][j];
                 }
             }
-            if (tid == 0) bulk_wait_read0();   // previous tile's bulk store has read its staging
+            if (bulk_thread) bulk_wait_read0();   // previous tile's bulk stores have read their staging
             __syncthreads();
             if (tid < 128) {
                 const float P = sG64[tid];
@@ -602,7 +608,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                     sGL[d0 + 1] = G1[15];
                 }
             }
-            if (tid == 0) bulk_wait_read0();   // previous tile's bulk store has read its staging
+            if (bulk_thread) bulk_wait_read0();   // previous tile's bulk stores have read their staging
             __syncthreads();
             const float P0 = sG64[d0], P1 = sG64[d0 + 1];
             {   // beyond |G - P| = EXP2_CAP the capped factors no longer
@@ -814,19 +820,39 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 16; j += 8)
-                    sts_v4(sm, MP::YT + sw128_off(trow, cg * 16 + j, 64), pack_f16(x[j], x[j + 1]),
+                    sts_v4(sm, W_TMP + sw128_off(trow, cg * 16 + j, 64), pack_f16(x[j], x[j + 1]),
                            pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]), pack_f16(x[j + 6], x[j + 7]));
             }
             sync_for_mma();
             if (tid == 0) {
-                const Operand Qh{sbase + MP::YQ, false, 64}, Th{sbase + MP::YT, true, 64};
+                const Operand Qh{sbase + MP::YQ, false, 64}, Th{sbase + W_TMP, true, 64};
                 mma_128(tmem + 64, Qh, Th, idesc_f16(T_F16, 128, 64, false, true, /*neg_a=*/true), 4);  // L
                 mma_commit(bar);
             }
-            wait_mma();
             // Assemble (I + A)^-1 as fp16, K-major [c][i], in region Y:
             //   rows 0..63:  [P | 0],   rows 64..127: [L | Q]   (unit diagonal)
-            // The fast variant folds diag(beta) into its columns.
+            // The fast variant folds diag(beta) into its columns.  P (over A10,
+            // read by the finished first merge product) and Q (over nothing)
+            // are written while the second product runs; the zeros (over its
+            // Q operand) and L (its result) after it.
+            auto ainv_part = [&](int r, int c0) {
+                float x[8];
+                const float* src = Wd + (r >> 6) * 64 * DS + (r & 63) * DS + (c0 & 63);
+                const float4 a = *reinterpret_cast<const float4*>(src), b = *reinterpret_cast<const float4*>(src + 4);
+                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    x[e] += (c0 + e == r) ? 1.f : 0.f;
+                    if (FAST) x[e] *= sBeta[c0 + e];
+                }
+                sts_v4(sm, MP::Y + sw128_off(r, c0, 128), pack_f16(x[0], x[1]), pack_f16(x[2], x[3]),
+                       pack_f16(x[4], x[5]), pack_f16(x[6], x[7]));
+            };
+            for (int ch = tid; ch < 1024; ch += PREP_THREADS) {
+                if (ch < 512) ainv_part(ch >> 3, (ch & 7) * 8);                          // P: rows 0..63, cols 0..63
+                else ainv_part(64 + ((ch - 512) >> 3), 64 + ((ch - 512) & 7) * 8);       // Q: rows 64..127, cols 64..127
+            }
+            wait_mma();
             if (lq < 2) {
                 float x[16];
                 tmem_ld16(tmem + lane_off + 64u + (uint32_t)(cg * 16), x);
@@ -840,31 +866,9 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                     sts_v4(sm, MP::Y + sw128_off(64 + trow, cg * 16 + j, 128), pack_f16(x[j], x[j + 1]),
                            pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]), pack_f16(x[j + 6], x[j + 7]));
             }
-            for (int ch = tid; ch < 1536; ch += PREP_THREADS) {
-                int r, c0;
-                if (ch < 1024) {            // rows 0..63: P (cols 0..63), zeros (cols 64..127)
-                    r = ch >> 4;
-                    c0 = (ch & 15) * 8;
-                } else {                    // rows 64..127: Q (cols 64..127)
-                    r = 64 + ((ch - 1024) >> 3);
-                    c0 = 64 + ((ch - 1024) & 7) * 8;
-                }
-                float x[8];
-                if (r < 64 && c0 >= 64) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = 0.f;
-                } else {
-                    const float* src = Wd + (r >> 6) * 64 * DS + (r & 63) * DS + (c0 & 63);
-                    const float4 a = *reinterpret_cast<const float4*>(src), b = *reinterpret_cast<const float4*>(src + 4);
-                    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        x[e] += (c0 + e == r) ? 1.f : 0.f;
-                        if (FAST) x[e] *= sBeta[c0 + e];
-                    }
-                }
-                sts_v4(sm, MP::Y + sw128_off(r, c0, 128), pack_f16(x[0], x[1]), pack_f16(x[2], x[3]),
-                       pack_f16(x[4], x[5]), pack_f16(x[6], x[7]));
+            if (tid < 512) {                 // zeros: rows 0..63, cols 64..127
+                const int r = tid >> 3, c0 = 64 + (tid & 7) * 8;
+                sts_v4(sm, MP::Y + sw128_off(r, c0, 128), 0u, 0u, 0u, 0u);
             }
             sync_for_mma();
 
@@ -934,22 +938,28 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             // --------------------------------------------------------------
             {
                 uint8_t* dst = tile_ptr(p, c.slot, h);
-                const bool second = warp >= 8;
-                const int half = (warp >> 2) & 1;
-                const float rs = (FAST && !second) ? sCL[trow] : 1.f;
-                // 32-column blocks b = 2 part + half: blocks 0-3 are the first
-                // product (Nm, or Qe), blocks 4-7 the second (Bc, or Oi), so
-                // each warp does two of each (Qe costs more than Oi)
+                // 32-column blocks of the four products (kind 0 Nm, 1 Bc, 2 Qe,
+                // 3 Oi; TMEM columns kind * 128 + vt * 32).  The four warps of a
+                // lane quarter each take one Qe block, one Oi block and two Nm
+                // or two Bc blocks: Qe costs about twice the others.
+                const int role = warp >> 2;
+                const float rs = FAST ? sCL[trow] : 1.f;   // rows d of Nm / Bc
 #pragma unroll 1
                 for (int part = 0; part < 4; ++part) {
                     float x[32];
-                    const int b = part * 2 + half;
-                    const int vt = b & 3;
-                    const int col0 = (b < 4 ? 0 : 128) + vt * 32;
-                    tmem_ld32(tmem + lane_off + (second ? 256u : 0u) + (uint32_t)col0, x);
+                    int kind, vt;
+                    if (part < 2) {
+                        kind = 2 + part;
+                        vt = role;
+                    } else {
+                        kind = role & 1;
+                        vt = (role & 2) + (part - 2);
+                    }
+                    const int col0 = vt * 32;
+                    tmem_ld32(tmem + lane_off + (uint32_t)(kind * 128 + col0), x);
                     tmem_ld_wait();
-                    if (!second) {
-                        if (b < 4) {
+                    if (kind < 2) {
+                        if (kind == 0) {
                             const float ns = -rs;
 #pragma unroll
                             for (int j = 0; j < 32; j += 8)
@@ -964,7 +974,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                                        pack_f16(rs * x[j + 6], rs * x[j + 7]));
                         }
                     } else {
-                        if (b < 4) {
+                        if (kind == 2) {
 #pragma unroll
                             for (int j = 0; j < 32; j += 8) {
                                 const uint4 qv = *reinterpret_cast<const uint4*>(sm + MP::QS + sw128_off(trow, col0 + j, 128));
@@ -1001,11 +1011,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 tc_fence_before();
                 __syncthreads();
                 tc_fence_after();
-                if (tid == 0) {      // asynchronous: drains while the next chunk loads
-                    bulk_s2g(dst + TILE_NM, sbase + MP::ST_NM, KD * KD * 2);
-                    bulk_s2g(dst + TILE_QE, sbase + MP::ST_QE, BT * KD * 2);
-                    bulk_s2g(dst + TILE_BC, sbase + MP::ST_BC, NVT * BC_PIECE);
-                    bulk_s2g(dst + TILE_OI, sbase + MP::ST_OI, NVT * OI_PIECE);
+                if (bulk_thread) {   // asynchronous: drains while the next chunk loads
+                    switch (tid >> 7) {
+                        case 0: bulk_s2g(dst + TILE_NM, sbase + MP::ST_NM, KD * KD * 2); break;
+                        case 1: bulk_s2g(dst + TILE_QE, sbase + MP::ST_QE, BT * KD * 2); break;
+                        case 2: bulk_s2g(dst + TILE_BC, sbase + MP::ST_BC, NVT * BC_PIECE); break;
+                        default: bulk_s2g(dst + TILE_OI, sbase + MP::ST_OI, NVT * OI_PIECE); break;
+                    }
                     bulk_commit();
                 }
             }
@@ -1017,10 +1029,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
         h = hn;
         have = have_n;
     }
-    if (tid == 0) {
-        bulk_wait0();
-        if (*sFlag != 0) atomicOr(p.status, STATUS_TIMEOUT);
-    }
+    if (bulk_thread) bulk_wait0();
+    if (tid == 0 && *sFlag != 0) atomicOr(p.status, STATUS_TIMEOUT);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
