@@ -8,19 +8,22 @@
 // states use the page's [N, H, V, K] layout (section "算子签名与 I/O 规格"),
 // i.e. the transpose of the K x V state; the transpose happens here.
 //
-// GB300 mapping.  320 threads in four roles, handing work to each other
+// GB300 mapping.  352 threads in five roles, handing work to each other
 // through mbarriers so that no role waits on another's latency:
 //   warps 0-3  state:  thread i owns row d = i of S (fp32, registers); per
 //              chunk it reads Nm S from TMEM, applies S' = Dg S + Nm S + Bc
 //              and writes the fp16 copy of S' the next chunk's MMAs read;
 //   warps 4-7  output: thread i owns row t = i; reads Qe S from one of two
 //              TMEM buffers, adds Oi, rounds to bf16 and stores o;
-//   warp 8     MMA issue: per chunk the Nm S product (the critical chain),
-//              then the Qe S product, which executes while the state warps
-//              update S;
-//   warp 9     loads: bulk copies of the chunk tiles, two chunks ahead.
-// Chunk tiles (Nm, Qe, Bc, Dg) are double-buffered, Oi goes through a ring
-// of four, the fp16 state copy is double-buffered.
+//   warp 8     MMA issue: the Nm S product of chunk j (the critical chain),
+//              then the Qe S product of chunk j - 1, which runs while the
+//              state warps update chunk j;
+//   warp 9     loads of the critical-path stages, two chunks ahead;
+//   warp 10    loads of the output tiles (Qe, Oi).
+// The critical-path tiles (Nm, Bc piece, Dg) are double-buffered in stages
+// that free as soon as the state update is done; Qe has its own two-slot
+// ring (its product lags one chunk), Oi a four-slot ring, and the fp16 state
+// copy three buffers (chunk j's copy is read by Qe S one chunk later).
 #include "kda_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -28,20 +31,20 @@ namespace kda {
 
 namespace {
 
-constexpr int SCAN_THREADS = 320;
-// stage: Nm | Qe | Bc piece | Dg
+constexpr int SCAN_THREADS = 352;
+// stage: Nm | Bc piece | Dg
 constexpr uint32_t ST_NM = 0;
-constexpr uint32_t ST_QE = 32768;
-constexpr uint32_t ST_BC = 65536;
-constexpr uint32_t ST_DG = 73728;
-constexpr uint32_t ST_BYTES = 74240;          // bytes loaded per stage
-constexpr uint32_t ST_STRIDE = 74752;         // 1024-aligned stage stride
-constexpr uint32_t S_OI = 2 * ST_STRIDE;      // Oi ring: 4 x 8 KB
-constexpr uint32_t S_S16 = S_OI + 4 * OI_PIECE;   // fp16 state copies: 2 x [K][32] 64B-swizzled
-constexpr uint32_t S_BAR = S_S16 + 2 * 8192;
+constexpr uint32_t ST_BC = 32768;
+constexpr uint32_t ST_DG = 40960;
+constexpr uint32_t ST_BYTES = 41472;          // bytes loaded per stage
+constexpr uint32_t ST_STRIDE = 41984;         // 1024-aligned stage stride
+constexpr uint32_t S_QE = 2 * ST_STRIDE;      // Qe ring: 2 x 32 KB
+constexpr uint32_t S_OI = S_QE + 2 * 32768;   // Oi ring: 4 x 8 KB
+constexpr uint32_t S_S16 = S_OI + 4 * OI_PIECE;   // fp16 state copies: 3 x [K][32] 64B-swizzled
+constexpr uint32_t S_BAR = S_S16 + 3 * 8192;
 // barrier offsets (8 bytes each)
-constexpr uint32_t B_FULL = 0, B_OIFULL = 16, B_OIFREE = 48, B_MMAS = 80, B_MMAO = 88, B_OFREE = 104,
-                   B_S16 = 120, B_SFREE = 128;
+constexpr uint32_t B_FULL = 0, B_QFULL = 16, B_OIFULL = 32, B_OIFREE = 64, B_MMAS = 96, B_MMAO = 104,
+                   B_OFREE = 120, B_S16 = 136, B_SFREE = 144;
 constexpr uint32_t S_TMEM = S_BAR + 192;
 constexpr uint32_t S_FLAG = S_TMEM + 4;
 constexpr uint32_t SCAN_SMEM = S_BAR + 256 + 1024;
@@ -51,14 +54,13 @@ __device__ __forceinline__ void load_stage(const FwdParams& p, int slot, int h, 
     const uint8_t* src = tile_ptr(p, slot, h);
     mbar_arrive_expect_tx(bar, ST_BYTES);
     bulk_g2s(dst + ST_NM, src + TILE_NM, KD * KD * 2, bar);
-    bulk_g2s(dst + ST_QE, src + TILE_QE, BT * KD * 2, bar);
     bulk_g2s(dst + ST_BC, src + TILE_BC + vt * BC_PIECE, BC_PIECE, bar);
     bulk_g2s(dst + ST_DG, src + TILE_DG, KD * 4, bar);
 }
 
-__device__ __forceinline__ void load_oi(const FwdParams& p, int slot, int h, int vt, uint32_t dst, uint32_t bar) {
-    mbar_arrive_expect_tx(bar, OI_PIECE);
-    bulk_g2s(dst, tile_ptr(p, slot, h) + TILE_OI + vt * OI_PIECE, OI_PIECE, bar);
+__device__ __forceinline__ void load_piece(const uint8_t* src, uint32_t bytes, uint32_t dst, uint32_t bar) {
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(dst, src, bytes, bar);
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
@@ -99,11 +101,13 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
 
     const uint32_t bars = sbase + S_BAR;
     auto full = [&](int s) { return bars + B_FULL + 8u * (uint32_t)s; };
+    auto qfull = [&](int s) { return bars + B_QFULL + 8u * (uint32_t)s; };
     auto oifull = [&](int r) { return bars + B_OIFULL + 8u * (uint32_t)r; };
     auto oifree = [&](int r) { return bars + B_OIFREE + 8u * (uint32_t)r; };
     auto mmao = [&](int b) { return bars + B_MMAO + 8u * (uint32_t)b; };
     auto ofree = [&](int b) { return bars + B_OFREE + 8u * (uint32_t)b; };
     auto sfree = [&](int s) { return bars + B_SFREE + 8u * (uint32_t)s; };
+    auto s16buf = [&](int j) { return S_S16 + (uint32_t)(j % 3) * 8192u; };
     const uint32_t mmas = bars + B_MMAS, s16rdy = bars + B_S16;
     volatile uint32_t* sFlag = reinterpret_cast<volatile uint32_t*>(sm + S_FLAG);
     if (warp == 0) {
@@ -113,6 +117,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(full(i), 1);
+            mbar_init(qfull(i), 1);
             mbar_init(mmao(i), 1);
             mbar_init(ofree(i), 1);
             mbar_init(sfree(i), 1);
@@ -140,7 +145,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
         }
 #pragma unroll
         for (int j = 0; j < BV; j += 8)
-            *reinterpret_cast<uint4*>(sm + S_S16 + sw64_off(row, j)) =
+            *reinterpret_cast<uint4*>(sm + s16buf(0) + sw64_off(row, j)) =
                 make_uint4(pack_f16x2(S[j], S[j + 1]), pack_f16x2(S[j + 2], S[j + 3]),
                            pack_f16x2(S[j + 4], S[j + 5]), pack_f16x2(S[j + 6], S[j + 7]));
     }
@@ -160,7 +165,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
         // State: S' = Dg S + Nm S + Bc, row d = tid.
         // ------------------------------------------------------------------
         for (int j = 0; j < nch; ++j) {
-            const int s = j & 1, b = j & 1;
+            const int s = j & 1;
             wait(full(s), (uint32_t)(j >> 1) & 1u);   // Bc / Dg of this chunk have landed
             wait(mmas, (uint32_t)j & 1u);
             tc_fence_after();
@@ -183,9 +188,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
                 S[c8 + 6] = fmaf(Dd, S[c8 + 6], x[c8 + 6] + b3.x);
                 S[c8 + 7] = fmaf(Dd, S[c8 + 7], x[c8 + 7] + b3.y);
             }
-            // next chunk's fp16 state copy goes to the other buffer: the MMAs
-            // that read it one chunk ago precede mma_s in issue order
-            uint8_t* s16 = sm + S_S16 + (uint32_t)(b ^ 1) * 8192u;
+            // the copy for chunk j + 1 goes to buffer (j + 1) % 3, last read
+            // by the products of chunk j - 2: Nm S(j - 2) and Qe S(j - 2),
+            // both issued before Nm S(j), whose commit we waited for
+            uint8_t* s16 = sm + s16buf(j + 1);
 #pragma unroll
             for (int c8 = 0; c8 < BV; c8 += 8)
                 *reinterpret_cast<uint4*>(s16 + sw64_off(row, c8)) =
@@ -196,7 +202,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
             bar_sync_named(1, 128);
             if (tid == 0) {
                 mbar_arrive(s16rdy);      // next chunk's MMAs may start
-                mbar_arrive(sfree(s));    // Bc / Dg of stage s are read
+                mbar_arrive(sfree(s));    // Nm / Bc / Dg of stage s are consumed
             }
         }
         if (p.ht != nullptr) {
@@ -243,53 +249,68 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
         }
     } else if (warp == 8) {
         // ------------------------------------------------------------------
-        // MMA issue (one thread).
+        // MMA issue (one thread): Nm S(j), then Qe S(j - 1).
         // ------------------------------------------------------------------
         if (lane == 0) {
             const uint32_t id = idesc_f16(T_F16, 128, BV, false, true);
             // per k-step only the start-address field of these advances
             const uint64_t a_nm0 = smem_desc(sbase + ST_NM, 16u, 1024u, SW_128B);
             const uint64_t a_nm1 = smem_desc(sbase + ST_STRIDE + ST_NM, 16u, 1024u, SW_128B);
-            const uint64_t a_qe0 = smem_desc(sbase + ST_QE, 16u, 1024u, SW_128B);
-            const uint64_t a_qe1 = smem_desc(sbase + ST_STRIDE + ST_QE, 16u, 1024u, SW_128B);
-            const uint64_t b_s0 = smem_desc(sbase + S_S16, 512u, 512u, SW_64B);
-            const uint64_t b_s1 = smem_desc(sbase + S_S16 + 8192u, 512u, 512u, SW_64B);
-            for (int j = 0; j < nch; ++j) {
-                const int s = j & 1, b = j & 1;
-                wait(full(s), (uint32_t)(j >> 1) & 1u);
-                if (j >= 1) wait(s16rdy, (uint32_t)(j - 1) & 1u);
-                tc_fence_after();
-                const uint64_t a_nm = s ? a_nm1 : a_nm0, a_qe = s ? a_qe1 : a_qe0, b_s = b ? b_s1 : b_s0;
+            const uint64_t a_qe0 = smem_desc(sbase + S_QE, 16u, 1024u, SW_128B);
+            const uint64_t a_qe1 = smem_desc(sbase + S_QE + 32768u, 16u, 1024u, SW_128B);
+            for (int j = 0; j <= nch; ++j) {
+                if (j < nch) {
+                    const int s = j & 1;
+                    wait(full(s), (uint32_t)(j >> 1) & 1u);
+                    if (j >= 1) wait(s16rdy, (uint32_t)(j - 1) & 1u);
+                    tc_fence_after();
+                    const uint64_t a_nm = s ? a_nm1 : a_nm0;
+                    const uint64_t b_s = smem_desc(sbase + s16buf(j), 512u, 512u, SW_64B);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)   // critical chain first: Nm S -> cols [0,32)
-                    mma_f16(tmem, a_nm + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), b_s + (uint64_t)(ks * 64), id,
-                            ks > 0);
-                mma_commit(mmas);
-                if (j >= 2) wait(ofree(b), (uint32_t)((j - 2) >> 1) & 1u);
-                tc_fence_after();
+                    for (int ks = 0; ks < 8; ++ks)   // critical chain: Nm S -> cols [0,32)
+                        mma_f16(tmem, a_nm + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), b_s + (uint64_t)(ks * 64),
+                                id, ks > 0);
+                    mma_commit(mmas);
+                }
+                if (j >= 1) {
+                    const int c = j - 1, b = c & 1;
+                    wait(qfull(b), (uint32_t)(c >> 1) & 1u);
+                    if (c >= 2) wait(ofree(b), (uint32_t)((c - 2) >> 1) & 1u);
+                    tc_fence_after();
+                    const uint64_t a_qe = b ? a_qe1 : a_qe0;
+                    const uint64_t b_s = smem_desc(sbase + s16buf(c), 512u, 512u, SW_64B);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)   // output product Qe S -> buffer b
-                    mma_f16(tmem + 32u + 32u * (uint32_t)b, a_qe + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
-                            b_s + (uint64_t)(ks * 64), id, ks > 0);
-                mma_commit(mmao(b));
+                    for (int ks = 0; ks < 8; ++ks)   // output product Qe S(c) -> buffer b
+                        mma_f16(tmem + 32u + 32u * (uint32_t)b, a_qe + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
+                                b_s + (uint64_t)(ks * 64), id, ks > 0);
+                    mma_commit(mmao(b));
+                }
             }
         }
     } else {
         // ------------------------------------------------------------------
-        // Loads (one thread): chunk tiles two chunks ahead.
+        // Loads, from two warps so that the critical-path tiles never queue
+        // behind the lagging output product (two spinning lanes of one warp
+        // would serialise):
+        //   warp 9:  the stage (Nm, Bc, Dg) two chunks ahead, once the state
+        //            warps are done with it;
+        //   warp 10: Qe once its product of two chunks back has completed,
+        //            Oi once its slot has been read.
         // ------------------------------------------------------------------
-        if (lane == 0) {
+        if (warp == 9 && lane == 0) {
+            for (int c = 0; c < nch; ++c) {
+                const int s = c & 1;
+                if (c >= 2) wait(sfree(s), (uint32_t)((c - 2) >> 1) & 1u);
+                load_stage(p, chunk_slot(p, n, c), h, vt, sbase + (uint32_t)s * ST_STRIDE, full(s));
+            }
+        } else if (warp == 10 && lane == 0) {
             for (int c = 0; c < nch; ++c) {
                 const int s = c & 1, r = c & 3;
-                if (c >= 2) {
-                    // stage s held chunk c-2: its MMAs (Qe S last) and the
-                    // state warps' Bc / Dg reads are done
-                    wait(mmao(s), (uint32_t)((c - 2) >> 1) & 1u);
-                    wait(sfree(s), (uint32_t)((c - 2) >> 1) & 1u);
-                }
-                load_stage(p, chunk_slot(p, n, c), h, vt, sbase + (uint32_t)s * ST_STRIDE, full(s));
+                const uint8_t* src = tile_ptr(p, chunk_slot(p, n, c), h);
+                if (c >= 2) wait(mmao(s), (uint32_t)((c - 2) >> 1) & 1u);
+                load_piece(src + TILE_QE, BT * KD * 2, sbase + S_QE + (uint32_t)s * 32768u, qfull(s));
                 if (c >= 4) wait(oifree(r), (uint32_t)((c - 4) >> 2) & 1u);
-                load_oi(p, chunk_slot(p, n, c), h, vt, sbase + S_OI + (uint32_t)r * OI_PIECE, oifull(r));
+                load_piece(src + TILE_OI + vt * OI_PIECE, OI_PIECE, sbase + S_OI + (uint32_t)r * OI_PIECE, oifull(r));
             }
         }
     }
