@@ -28,7 +28,6 @@ _STATUS = {
     0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
     4: "invalid cu_seqlens", 5: "device wait timed out", 6: "too large for the no-alloc scratch",
     7: "state slot index or accepted-token count out of range",
-    8: "gate decay beyond the exact range (results approximate)",
 }
 
 RECURRENT_WORKSPACE_BYTES = 256

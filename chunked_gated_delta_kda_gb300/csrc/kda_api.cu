@@ -10,6 +10,7 @@
 namespace kda {
 cudaError_t launch_prep(const FwdParams& p, bool l2norm, cudaStream_t stream);
 cudaError_t launch_scan(const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_exact(const FwdParams& p, const uint32_t* flags, bool l2norm, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
@@ -28,10 +29,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 extern "C" {
 
+// Bytes of the per-(sequence, head) exact-recompute flags after the tiles.
+static unsigned long long flags_bytes(int H, int N) {
+    return (((unsigned long long)N * (unsigned long long)H * 4ull + 255ull) / 256ull) * 256ull;
+}
+
 size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int N) {
     if (B < 1 || T < 0 || H < 1 || N < 1 || K != kda::KD || V != kda::VD) return 0;
     const unsigned long long items = (unsigned long long)max_slots(B, T, N) * (unsigned long long)H;
-    return (size_t)(kda::ws_tiles_offset(items) + items * kda::TILE_BYTES);
+    return (size_t)(kda::ws_tiles_offset(items) + items * kda::TILE_BYTES + flags_bytes(H, N));
 }
 
 static kda_status fwd_impl(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -74,6 +80,8 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const fl
     p.wide_count = static_cast<uint32_t*>(workspace) + 1;
     p.wide_list = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + kda::WS_HEADER);
     p.tiles = static_cast<uint8_t*>(workspace) + kda::ws_tiles_offset(items);
+    p.exact_flags =
+        reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + kda::ws_tiles_offset(items) + items * kda::TILE_BYTES);
     p.scale = scale;
     p.T = T;
     p.H = H;
@@ -87,12 +95,15 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const fl
     }
 
     if (cudaMemsetAsync(workspace, 0, kda::WS_CLEAR, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaMemsetAsync(p.exact_flags, 0, (size_t)N * H * 4, stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (p.nslots > 0) {
         if (kda::launch_prep(p, (flags & KDA_FLAG_QK_L2NORM) != 0u, stream) != cudaSuccess) return KDA_ERR_CUDA;
     }
     if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::launch_scan(p, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::launch_exact(p, p.exact_flags, (flags & KDA_FLAG_QK_L2NORM) != 0u, stream) != cudaSuccess)
+        return KDA_ERR_CUDA;
     if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }
@@ -121,7 +132,6 @@ kda_status kda_get_status(const void* workspace, cudaStream_t stream) {
     if (word & kda::STATUS_BAD_CU) return KDA_ERR_BAD_CU_SEQLENS;
     if (word & kda::STATUS_TIMEOUT) return KDA_ERR_TIMEOUT;
     if (word & kda::STATUS_BAD_INDEX) return KDA_ERR_BAD_STATE_INDEX;
-    if (word & kda::STATUS_DECAY_RANGE) return KDA_ERR_DECAY_RANGE;
     return KDA_OK;
 }
 
@@ -135,8 +145,6 @@ const char* kda_status_str(kda_status status) {
         case KDA_ERR_TIMEOUT: return "a bounded device wait ran out";
         case KDA_ERR_TOO_LARGE: return "problem too large for the static no-alloc scratch";
         case KDA_ERR_BAD_STATE_INDEX: return "device found a state slot index or accepted-token count out of range";
-        case KDA_ERR_DECAY_RANGE:
-            return "a chunk's gate decay exceeded the range of exact factored products; results are approximate";
     }
     return "unknown status";
 }

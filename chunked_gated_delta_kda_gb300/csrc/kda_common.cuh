@@ -54,7 +54,6 @@ constexpr uint32_t TILE_BYTES = TILE_DG + KD * 4;            // 131584
 constexpr uint32_t STATUS_BAD_CU = 1u;
 constexpr uint32_t STATUS_TIMEOUT = 2u;
 constexpr uint32_t STATUS_BAD_INDEX = 4u;   // token-by-token kernel: a state slot out of range
-constexpr uint32_t STATUS_DECAY_RANGE = 8u; // a chunk's in-chunk decay exceeded the exact range
 constexpr uint32_t WS_HEADER = 256;
 constexpr uint32_t WS_CLEAR = 16;
 
@@ -80,6 +79,7 @@ struct FwdParams {
     uint32_t* status;       // workspace status word
     uint32_t* wide_count;   // number of work items queued for the wide-range path
     int32_t* wide_list;     // their ids (slot * H + head)
+    uint32_t* exact_flags;  // [N][H]: 1 where a chunk exceeded the exact factoring range
     float scale;
     int T;                  // per-sequence length (fixed) or packed length (varlen)
     int H;

@@ -28,7 +28,9 @@
 //   * wide (bf16 gated operands): chunks whose factors would overflow fp16
 //     (strong decay inside the chunk) are queued by the fast kernel and
 //     redone by this variant, which builds exp(G) k, kg, qg and beta v as
-//     separate fp16 tiles.
+//     separate fp16 tiles.  A chunk whose decay from the pivot row exceeds
+//     the factor cap is flagged: its (sequence, head) is then recomputed
+//     exactly, token by token, after the scan.
 //
 // GB300 mapping.  Persistent kernels: one 512-thread CTA per SM walks the
 // work items.  The 128-wide contractions run on tcgen05 tensor cores with
@@ -612,12 +614,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             __syncthreads();
             const float P0 = sG64[d0], P1 = sG64[d0 + 1];
             {   // beyond |G - P| = EXP2_CAP the capped factors no longer
-                // multiply back to exp(G_c - G_i): flag the result approximate
+                // multiply back to exp(G_c - G_i): this (sequence, head) is
+                // recomputed token by token after the scan
                 bool far = false;
 #pragma unroll
                 for (int r = 0; r < 16; ++r)
                     far = far || fabsf(G0[r] - P0) > EXP2_CAP || fabsf(G1[r] - P1) > EXP2_CAP;
-                if (__any_sync(0xffffffffu, far) && lane == 0) atomicOr(p.status, STATUS_DECAY_RANGE);
+                if (__any_sync(0xffffffffu, far) && lane == 0) p.exact_flags[(size_t)c.n * H + h] = 1u;
             }
             const float eP0 = ex2(P0), eP1 = ex2(P1);
             const float cL0 = ex2(fminf(sGL[d0] - P0, EXP2_CAP)), cL1 = ex2(fminf(sGL[d0 + 1] - P1, EXP2_CAP));

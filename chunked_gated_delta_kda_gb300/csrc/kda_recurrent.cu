@@ -106,6 +106,73 @@ __device__ __forceinline__ void zero_output(const RecParams& p, long long bos, i
         *reinterpret_cast<uint4*>(p.o + ((size_t)(bos + t) * p.H + h) * VD + v0) = make_uint4(0, 0, 0, 0);
 }
 
+// One token of the recurrence on this warp's 8 value rows (row v0 + r in
+// s[r], lane owning K entries 4 lane .. 4 lane + 3): decay, delta update,
+// read-out; lane 0 writes the 8 bf16 outputs.  `tok` indexes (token, head).
+__device__ __forceinline__ void rec_token(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+                                          const uint16_t* __restrict__ v, const float* __restrict__ g,
+                                          const float* __restrict__ beta, uint16_t* __restrict__ o, float scale,
+                                          bool l2norm, size_t tok, int v0, int lane, float (&s)[REC_ROWS][4]) {
+    float qv[4], kv[4];
+    load4_bf16(q + tok * KD + 4 * lane, qv);
+    load4_bf16(k + tok * KD + 4 * lane, kv);
+    const float4 gv = *reinterpret_cast<const float4*>(g + tok * KD + 4 * lane);
+    const float bt = beta[tok];
+    const uint4 vu = *reinterpret_cast<const uint4*>(v + tok * VD + v0);
+    float vv[REC_ROWS];
+    vv[0] = __uint_as_float(vu.x << 16); vv[1] = __uint_as_float(vu.x & 0xffff0000u);
+    vv[2] = __uint_as_float(vu.y << 16); vv[3] = __uint_as_float(vu.y & 0xffff0000u);
+    vv[4] = __uint_as_float(vu.z << 16); vv[5] = __uint_as_float(vu.z & 0xffff0000u);
+    vv[6] = __uint_as_float(vu.w << 16); vv[7] = __uint_as_float(vu.w & 0xffff0000u);
+
+    float qs = scale, ks = 1.f;
+    if (l2norm) {   // x / sqrt(sum x^2 + 1e-6), section "测试与验证体系"
+        const float sq = warp_sum(qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3]);
+        const float sk = warp_sum(kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3]);
+        qs *= rsqrtf(sq + 1e-6f);
+        ks = rsqrtf(sk + 1e-6f);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        qv[i] *= qs;
+        kv[i] *= ks;
+    }
+    const float e[4] = {__expf(gv.x), __expf(gv.y), __expf(gv.z), __expf(gv.w)};
+
+    // decay, then k . s_v
+    float dot[REC_ROWS];
+#pragma unroll
+    for (int r = 0; r < REC_ROWS; ++r) {
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            s[r][i] *= e[i];
+            acc = fmaf(kv[i], s[r][i], acc);
+        }
+        dot[r] = acc;
+    }
+    warp_sum8(dot, lane);
+    // delta update, then q . s_v
+#pragma unroll
+    for (int r = 0; r < REC_ROWS; ++r) {
+        const float delta = bt * (vv[r] - dot[r]);
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            s[r][i] = fmaf(kv[i], delta, s[r][i]);
+            acc = fmaf(qv[i], s[r][i], acc);
+        }
+        dot[r] = acc;
+    }
+    warp_sum8(dot, lane);
+    if (lane == 0) {
+        __nv_bfloat162 o2[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o2[j] = __floats2bfloat162_rn(dot[2 * j], dot[2 * j + 1]);
+        *reinterpret_cast<uint4*>(o + tok * VD + v0) = *reinterpret_cast<const uint4*>(o2);
+    }
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(REC_THREADS) kda_recurrent_kernel(const RecParams p) {
@@ -173,70 +240,49 @@ __global__ void __launch_bounds__(REC_THREADS) kda_recurrent_kernel(const RecPar
 
     for (int t = 0; t < len; ++t) {
         const size_t tok = (size_t)(bos + t) * H + h;
-        float qv[4], kv[4];
-        load4_bf16(p.q + tok * KD + 4 * lane, qv);
-        load4_bf16(p.k + tok * KD + 4 * lane, kv);
-        const float4 gv = *reinterpret_cast<const float4*>(p.g + tok * KD + 4 * lane);
-        const float bt = p.beta[tok];
-        const uint4 vu = *reinterpret_cast<const uint4*>(p.v + tok * VD + v0);
-        float vv[REC_ROWS];
-        vv[0] = __uint_as_float(vu.x << 16); vv[1] = __uint_as_float(vu.x & 0xffff0000u);
-        vv[2] = __uint_as_float(vu.y << 16); vv[3] = __uint_as_float(vu.y & 0xffff0000u);
-        vv[4] = __uint_as_float(vu.z << 16); vv[5] = __uint_as_float(vu.z & 0xffff0000u);
-        vv[6] = __uint_as_float(vu.w << 16); vv[7] = __uint_as_float(vu.w & 0xffff0000u);
-
-        float qs = p.scale, ks = 1.f;
-        if (p.l2norm) {   // x / sqrt(sum x^2 + 1e-6), section "测试与验证体系"
-            const float sq = warp_sum(qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3]);
-            const float sk = warp_sum(kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3]);
-            qs *= rsqrtf(sq + 1e-6f);
-            ks = rsqrtf(sk + 1e-6f);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            qv[i] *= qs;
-            kv[i] *= ks;
-        }
-        const float e[4] = {__expf(gv.x), __expf(gv.y), __expf(gv.z), __expf(gv.w)};
-
-        // decay, then k . s_v
-        float dot[REC_ROWS];
-#pragma unroll
-        for (int r = 0; r < REC_ROWS; ++r) {
-            float acc = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                s[r][i] *= e[i];
-                acc = fmaf(kv[i], s[r][i], acc);
-            }
-            dot[r] = acc;
-        }
-        warp_sum8(dot, lane);
-        // delta update, then q . s_v
-#pragma unroll
-        for (int r = 0; r < REC_ROWS; ++r) {
-            const float delta = bt * (vv[r] - dot[r]);
-            float acc = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                s[r][i] = fmaf(kv[i], delta, s[r][i]);
-                acc = fmaf(qv[i], s[r][i], acc);
-            }
-            dot[r] = acc;
-        }
-        warp_sum8(dot, lane);
-        if (lane == 0) {
-            __nv_bfloat162 o2[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) o2[j] = __floats2bfloat162_rn(dot[2 * j], dot[2 * j + 1]);
-            *reinterpret_cast<uint4*>(p.o + tok * VD + v0) = *reinterpret_cast<const uint4*>(o2);
-        }
+        rec_token(p.q, p.k, p.v, p.g, p.beta, p.o, p.scale, p.l2norm != 0, tok, v0, lane, s);
         if (p.nacc != nullptr) {   // speculative mode: the state after token t goes to slot row[t]
             const int ws = row[t];
             if (ws >= 0) store_rows(p.pool + (((size_t)ws * H + h) * VD + v0) * KD, s, lane);
         }
     }
     if (p.nacc == nullptr) store_rows(p.pool + (((size_t)rslot * H + h) * VD + v0) * KD, s, lane);
+}
+
+// Exact recomputation for the chunked forward (one (sequence, head) per
+// blockIdx.y/z, 32 value rows per CTA): the (sequence, head) units in which
+// some chunk's in-chunk decay exceeded the range of exact factored products
+// (flagged by the chunk-parallel kernel) are recomputed here token by token,
+// from h0, overwriting the chunked result's o and final state.  The
+// recurrence is the same per-token rule, so it is exact for any decay.
+__global__ void __launch_bounds__(REC_THREADS) kda_exact_kernel(const FwdParams p, const uint32_t* flags,
+                                                                int l2norm) {
+    const int h = (int)blockIdx.y, n = (int)blockIdx.z;
+    const int H = p.H;
+    if (flags[(size_t)n * H + h] == 0u) return;   // uniform
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int v0 = (int)blockIdx.x * REC_ROWS_CTA + warp * REC_ROWS;
+    long long bos;
+    int len;
+    if (!seq_bounds(p, n, bos, len)) return;
+    const size_t st = (((size_t)n * H + h) * VD + v0) * KD;
+    float s[REC_ROWS][4];
+#pragma unroll
+    for (int r = 0; r < REC_ROWS; ++r) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.h0 != nullptr) x = *reinterpret_cast<const float4*>(p.h0 + st + (size_t)r * KD + 4 * lane);
+        s[r][0] = x.x; s[r][1] = x.y; s[r][2] = x.z; s[r][3] = x.w;
+    }
+    for (int t = 0; t < len; ++t)
+        rec_token(p.q, p.k, p.v, p.g, p.beta, p.o, p.scale, l2norm != 0, (size_t)(bos + t) * H + h, v0, lane, s);
+    if (p.ht != nullptr) store_rows(p.ht + st, s, lane);
+}
+
+cudaError_t launch_exact(const FwdParams& p, const uint32_t* flags, bool l2norm, cudaStream_t stream) {
+    if (p.N == 0) return cudaSuccess;
+    const dim3 grid((unsigned)(VD / REC_ROWS_CTA), (unsigned)p.H, (unsigned)p.N);
+    kda_exact_kernel<<<grid, REC_THREADS, 0, stream>>>(p, flags, l2norm ? 1 : 0);
+    return cudaGetLastError();
 }
 
 }  // namespace kda

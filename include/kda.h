@@ -48,12 +48,8 @@ typedef enum {
     KDA_ERR_TIMEOUT = 5,         /* a bounded device wait ran out (via kda_get_status) */
     KDA_ERR_TOO_LARGE = 6,       /* kda_fwd_noalloc: the problem needs more workspace than
                                     the library's static scratch holds */
-    KDA_ERR_BAD_STATE_INDEX = 7, /* kda_fused_recurrent: device found a state slot index or an
+    KDA_ERR_BAD_STATE_INDEX = 7  /* kda_fused_recurrent: device found a state slot index or an
                                     accepted-token count out of range (via kda_get_status) */
-    KDA_ERR_DECAY_RANGE = 8      /* kda_fwd: some chunk's gate decay between its middle row and
-                                    its first or last row exceeded ~80 (natural-log units) in a
-                                    dimension; the outputs are written but approximate (via
-                                    kda_get_status) */
 } kda_status;
 
 /* Apply the per-token L2 normalisation x / sqrt(sum(x^2) + 1e-6) to q and k
@@ -64,7 +60,7 @@ typedef enum {
  * Bytes of device workspace kda_fwd needs for these sizes (an upper bound
  * that covers both fixed-length and varlen packing).  0 on invalid sizes.
  * Layout: a 256-byte status header, then one 131584-byte tile per
- * (128-token chunk slot, head).
+ * (128-token chunk slot, head), then one flag word per (sequence, head).
  */
 size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int N);
 
@@ -95,11 +91,12 @@ size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int N);
  * state; tensor-core products take fp16 operands with fp32 accumulation
  * (bf16 operands for the gated q.k / k.k products of chunks whose in-chunk
  * decay is too strong for fp16 factors).
- * The gated products are factored around the chunk's middle row; factors are
- * capped at e^80, so results are exact (up to rounding) while the gate decay
- * over any 64 tokens of a chunk stays below 80 in each dimension.  Chunks
- * beyond that range are still computed, with the capped factors, and flagged
- * in the status word (KDA_ERR_DECAY_RANGE).
+ * The gated products are factored around the chunk's middle row with
+ * factors capped at e^80, exact (up to rounding) while the gate decay between
+ * that row and the chunk's first or last row stays below 80 in each
+ * dimension.  A (sequence, head) containing a chunk beyond that range is
+ * recomputed exactly after the scan by the token-by-token recurrence (same
+ * precision as kda_fused_recurrent), at token-by-token speed.
  */
 kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                    float scale, const float* h0, const int32_t* cu_seqlens, void* o, float* ht, int B,
@@ -122,9 +119,8 @@ kda_status kda_fwd_timed(const void* q, const void* k, const void* v, const floa
 /*
  * Synchronise `stream`, then read the device status word that the last
  * kda_fwd or kda_fused_recurrent on this workspace wrote.  Returns KDA_OK,
- * KDA_ERR_BAD_CU_SEQLENS, KDA_ERR_TIMEOUT, KDA_ERR_BAD_STATE_INDEX,
- * KDA_ERR_DECAY_RANGE (in that order of precedence), or KDA_ERR_CUDA if
- * synchronising or reading failed.
+ * KDA_ERR_BAD_CU_SEQLENS, KDA_ERR_TIMEOUT, KDA_ERR_BAD_STATE_INDEX (in that
+ * order of precedence), or KDA_ERR_CUDA if synchronising or reading failed.
  */
 kda_status kda_get_status(const void* workspace, cudaStream_t stream);
 

@@ -31,17 +31,19 @@ def test_workspace_bytes():
     from chunked_gated_delta_kda_gb300 import binding
     lib = binding.load_library()
     tile = 131584
-    # fixed length: B * T/128 slots; varlen bound: T/128 + N + 1
-    assert lib.kda_fwd_workspace_bytes(1, 65536, 32, 128, 128, 1) == 256 + ((514 * 32 * 4 + 255) // 256) * 256 + 514 * 32 * tile
-    assert lib.kda_fwd_workspace_bytes(4, 8192, 16, 128, 128, 4) == 256 + ((256 * 16 * 4 + 255) // 256) * 256 + 256 * 16 * tile
-    assert lib.kda_fwd_workspace_bytes(1, 9192, 32, 128, 128, 6) == 256 + ((78 * 32 * 4 + 255) // 256) * 256 + 78 * 32 * tile
+    r256 = lambda b: (b + 255) // 256 * 256
+    # header, wide queue, tiles (fixed length: B * T/128 slots; varlen bound:
+    # T/128 + N + 1), then one flag word per (sequence, head)
+    assert lib.kda_fwd_workspace_bytes(1, 65536, 32, 128, 128, 1) == 256 + r256(514 * 32 * 4) + 514 * 32 * tile + r256(32 * 4)
+    assert lib.kda_fwd_workspace_bytes(4, 8192, 16, 128, 128, 4) == 256 + r256(256 * 16 * 4) + 256 * 16 * tile + r256(64 * 4)
+    assert lib.kda_fwd_workspace_bytes(1, 9192, 32, 128, 128, 6) == 256 + r256(78 * 32 * 4) + 78 * 32 * tile + r256(192 * 4)
     assert lib.kda_fwd_workspace_bytes(1, 256, 1, 64, 128, 1) == 0
 
 
 def test_status_strings():
     from chunked_gated_delta_kda_gb300 import binding
     lib = binding.load_library()
-    for code in range(9):
+    for code in range(8):
         assert lib.kda_status_str(code)
     assert b"unknown" in lib.kda_status_str(99)
 
