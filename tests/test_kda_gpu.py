@@ -228,3 +228,23 @@ def test_host_validation_on_device():
     with pytest.raises(binding.KdaError) as e:   # fixed length needs T % 128 == 0
         binding.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], None, None, None, o, None, 1, 0, ws)
     assert e.value.code == 1
+
+
+def test_many_short_sequences():
+    """200 packed sequences of lengths 0..300 (many chunk slots, many tails,
+    empty sequences), 3 heads, initial states."""
+    rng = np.random.default_rng(7)
+    lens = [int(x) for x in rng.integers(0, 301, 200)]
+    w = custom("many", B=1, T=sum(lens), H=3, seqlens=lens, with_h0=True, seed=51)
+    x = make_inputs(w)
+    o, ht = run_gpu(x)
+    o_ref, ht_ref = run_oracle(x)
+    assert_within(compare(o, ht, o_ref, ht_ref))
+
+
+def test_many_heads_short_sequence():
+    x = make_inputs(custom("heads", B=2, T=256, H=64, with_h0=True, seed=52))
+    o, ht = run_gpu(x)
+    units = [(n, h) for n in range(2) for h in (0, 17, 63)]
+    o_ref, ht_ref = run_oracle(x, units=units)
+    assert_within(compare(o, ht, o_ref, ht_ref, units=units))
