@@ -105,6 +105,13 @@ struct Map {
     static constexpr uint32_t ST_OI = FAST ? 98304 : 131072;
 };
 
+// max that propagates NaN (an operand 0 * inf must not pass the range check)
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -516,9 +523,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 sEP[tid] = ex2(P);
                 sCL[tid] = ex2(fminf(sGL[tid] - P, EXP2_CAP));
             }
-            float P[8];
+            // only G - P is needed from here on: fold the pivot in once
 #pragma unroll
-            for (int j = 0; j < 8; ++j) P[j] = sG64[d8 + j];
+            for (int j = 0; j < 8; ++j) {
+                const float P = sG64[d8 + j];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) G[r][j] -= P;
+            }
             float m = 0.f;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
@@ -541,15 +552,15 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 uint32_t lk[4], lqv[4], rk[4], v16[4];
 #pragma unroll
                 for (int j = 0; j < 8; j += 2) {
-                    const float E0 = ex2(fminf(G[r][j] - P[j], EXP2_CAP));
-                    const float E1 = ex2(fminf(G[r][j + 1] - P[j + 1], EXP2_CAP));
-                    const float F0 = ex2(fminf(P[j] - G[r][j], EXP2_CAP));
-                    const float F1 = ex2(fminf(P[j + 1] - G[r][j + 1], EXP2_CAP));
+                    // uncapped: a factor that overflows makes an operand
+                    // infinite, which the range check sends to the wide variant
+                    const float E0 = ex2(G[r][j]), E1 = ex2(G[r][j + 1]);
+                    const float F0 = ex2(-G[r][j]), F1 = ex2(-G[r][j + 1]);
                     const float k0 = kf[j] * ik, k1 = kf[j + 1] * ik;
                     const float q0 = qf[j] * iq, q1 = qf[j + 1] * iq;
                     const float a0 = k0 * E0, a1 = k1 * E1, b0 = q0 * E0, b1 = q1 * E1, c0 = k0 * F0, c1 = k1 * F1;
-                    m = fmaxf(m, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(b0), fabsf(b1))));
-                    m = fmaxf(m, fmaxf(fmaxf(fabsf(c0), fabsf(c1)), fmaxf(fabsf(vf[j]), fabsf(vf[j + 1]))));
+                    m = fmax_nan(m, fmax_nan(fmax_nan(fabsf(a0), fabsf(a1)), fmax_nan(fabsf(b0), fabsf(b1))));
+                    m = fmax_nan(m, fmax_nan(fmax_nan(fabsf(c0), fabsf(c1)), fmax_nan(fabsf(vf[j]), fabsf(vf[j + 1]))));
                     lk[j / 2] = pack_f16(a0, a1);
                     lqv[j / 2] = pack_f16(b0, b1);
                     rk[j / 2] = pack_f16(c0, c1);
