@@ -722,11 +722,21 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 // warps whose block lies above the diagonal (row < 64, col >= 64) skip
                 if (!(trow < 64 && col0 >= 64)) {
                     float x[32];
-                    tmem_ld32(tmem + lane_off + (uint32_t)col0, x);
-                    tmem_ld_wait();
-                    const float b = sBeta[trow];
+                    if (lq < cg) {            // above the diagonal (inside a 64-block): zeros
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) x[j] = (col0 + j < trow) ? b * x[j] : 0.f;
+                        for (int j = 0; j < 32; ++j) x[j] = 0.f;
+                    } else {
+                        tmem_ld32(tmem + lane_off + (uint32_t)col0, x);
+                        tmem_ld_wait();
+                        const float b = sBeta[trow];
+                        if (lq > cg) {        // below the diagonal: no mask needed
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) x[j] *= b;
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) x[j] = (col0 + j < trow) ? b * x[j] : 0.f;
+                        }
+                    }
                     if (trow >= 64 && col0 < 64) {
 #pragma unroll
                         for (int j = 0; j < 32; j += 8)
