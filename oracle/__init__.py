@@ -6,7 +6,7 @@ headers, helpers, tables or constants) and neither imports the other.  Only
 ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline and
 reference legs may import it; the product path never does.
 
-Two independent forms:
+Independent forms:
   * ``kda_recurrent``: the per-token recurrence in plain C, fp64, OpenMP over
     (sequence, head) units (``kda_recurrent.c``).  This is the definition of
     the result.
@@ -16,8 +16,12 @@ Two independent forms:
   * ``fused_recurrent``: the token-by-token recurrence with an in-place state
     pool, slot indices and speculative-decoding checkpoints, numpy fp64
     (``decode.py``): the oracle of the decode entry point.
+  * ``kcp_forward``: the KCP forward simulated rank by rank (``kcp.py``).
+  * ``backward.kda_backward``: gradients of <do, o> + <dht, ht> by fp64
+    torch autograd through the per-token recurrence (``backward.py``): the
+    oracle of the backward entry point.
 
-Parity pins live in ``tests/test_oracle.py`` and ``tests/test_oracle_decode.py``.
+Parity pins live in ``tests/test_oracle*.py``.
 """
 
 from __future__ import annotations
