@@ -67,6 +67,11 @@ def load_library(path: Optional[str] = None):
     lib.kda_kcp_workspace_bytes.argtypes = [i, i, i, i, i, i]
     lib.kda_kcp_fwd.restype = ctypes.c_int
     lib.kda_kcp_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, i, i, i, i, i, i, u, vp, sz, vp]
+    lib.kda_bwd_workspace_bytes.restype = sz
+    lib.kda_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    lib.kda_bwd.restype = ctypes.c_int
+    lib.kda_bwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                            i, i, i, i, i, i, u, vp, sz, vp]
     lib.kda_status_str.restype = ctypes.c_char_p
     lib.kda_status_str.argtypes = [i]
     _lib = lib
@@ -300,3 +305,67 @@ def kcp_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
     if rc != 0:
         raise KdaError(rc, "kda_kcp_fwd")
     return o, ht
+
+
+def bwd_workspace_bytes(B: int, T: int, H: int, N: int, K: int = 128, V: int = 128) -> int:
+    return int(load_library().kda_bwd_workspace_bytes(B, T, H, K, V, N))
+
+
+def kda_bwd(q, k, v, g, beta, scale, h0, cu_seqlens, dout, dht, dq, dk, dv, dg, dbeta, dh0, N: int, flags: int,
+            workspace: torch.Tensor) -> None:
+    """Direct call of the backward entry point on caller-provided tensors.
+    Raises KdaError on a non-zero status."""
+    lib = load_library()
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    rc = lib.kda_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale if scale is not None else -1.0),
+                     _ptr(h0), _ptr(cu_seqlens), _ptr(dout), _ptr(dht), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+                     _ptr(dbeta), _ptr(dh0), B, T, H, K, V, N, flags, _ptr(workspace),
+                     workspace.numel() * workspace.element_size(), _stream_handle(q.device))
+    if rc != 0:
+        raise KdaError(rc, "kda_bwd")
+
+
+def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+        do: torch.Tensor, scale: Optional[float] = None, initial_state: Optional[torch.Tensor] = None,
+        dht: Optional[torch.Tensor] = None, use_qk_l2norm_in_kernel: bool = False,
+        cu_seqlens: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """KDA backward of ``fwd`` with the same arguments: the gradients of
+    <do, o> + <dht, ht>.  do: bf16 [B,T,H,V]; dht: fp32 [N,H,V,K] or None.
+    Returns fp32 (dq, dk, dv, dg, dbeta, dh0) with the shapes of q, k, v, g,
+    beta and the state [N,H,V,K]."""
+    for name, t, dt, nd in (("q", q, torch.bfloat16, 4), ("k", k, torch.bfloat16, 4), ("v", v, torch.bfloat16, 4),
+                            ("g", g, torch.float32, 4), ("beta", beta, torch.float32, 3),
+                            ("do", do, torch.bfloat16, 4)):
+        _check(name, t, dt, nd)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if (k.shape != q.shape or g.shape != q.shape or v.shape[:3] != q.shape[:3] or beta.shape != q.shape[:3]
+            or do.shape != v.shape):
+        raise ValueError("shape mismatch among q, k, v, g, beta, do")
+    if cu_seqlens is not None:
+        _check("cu_seqlens", cu_seqlens, torch.int32, 1)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    for name, t in (("initial_state", initial_state), ("dht", dht)):
+        if t is not None:
+            _check(name, t, torch.float32, 4)
+            if tuple(t.shape) != (N, H, V, K):
+                raise ValueError(f"{name} must be {(N, H, V, K)}, got {tuple(t.shape)}")
+    dev = q.device
+    q, k, v, g, beta, do = (t.contiguous() for t in (q, k, v, g, beta, do))
+    h0 = initial_state.contiguous() if initial_state is not None else None
+    dht = dht.contiguous() if dht is not None else None
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq, dk, dg = (torch.empty((B, T, H, K), **f32) for _ in range(3))
+    dv = torch.empty((B, T, H, V), **f32)
+    dbeta = torch.empty((B, T, H), **f32)
+    dh0 = torch.empty((N, H, V, K), **f32)
+    need = bwd_workspace_bytes(B, T, H, N, K, V)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    flags = KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0
+    with torch.cuda.device(dev):
+        kda_bwd(q, k, v, g, beta, scale, h0, cu_seqlens, do, dht, dq, dk, dv, dg, dbeta, dh0, N, flags, workspace)
+    return dq, dk, dv, dg, dbeta, dh0

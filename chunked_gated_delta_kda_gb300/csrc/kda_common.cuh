@@ -57,6 +57,56 @@ constexpr uint32_t STATUS_BAD_INDEX = 4u;   // token-by-token kernel: a state sl
 constexpr uint32_t WS_HEADER = 256;
 constexpr uint32_t WS_CLEAR = 16;
 
+// ---- warp helpers of the token-by-token kernels ----
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+    return x;
+}
+
+// All-reduce eight per-lane partial sums over the warp: a reduce-scatter by
+// halving (xor 16, 8, 4: each step keeps half of the rows and adds the
+// partner's half), a butterfly over the last two lane bits, then a gather of
+// the eight totals.  17 shuffles instead of 40.
+__device__ __forceinline__ void warp_sum8(float (&a)[8], int lane) {
+    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4;
+    float b[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float send = h16 ? a[j] : a[j + 4];
+        const float keep = h16 ? a[j + 4] : a[j];
+        b[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    float c[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float send = h8 ? b[j] : b[j + 2];
+        const float keep = h8 ? b[j + 2] : b[j];
+        c[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float d;
+    {
+        const float send = h4 ? c[0] : c[1];
+        const float keep = h4 ? c[1] : c[0];
+        d = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    d += __shfl_xor_sync(0xffffffffu, d, 2);
+    d += __shfl_xor_sync(0xffffffffu, d, 1);
+    // lane holds the total of row 4*h16 + 2*h8 + h4; fetch every row's total
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+        a[r] = __shfl_sync(0xffffffffu, d, ((r >> 2) << 4) | (((r >> 1) & 1) << 3) | ((r & 1) << 2));
+}
+
+__device__ __forceinline__ void load4_bf16(const uint16_t* p, float (&x)[4]) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    x[0] = __uint_as_float(u.x << 16);
+    x[1] = __uint_as_float(u.x & 0xffff0000u);
+    x[2] = __uint_as_float(u.y << 16);
+    x[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+
 // Bytes before the tiles for a workspace holding `items` (slot, head) tiles.
 __host__ __device__ constexpr unsigned long long ws_tiles_offset(unsigned long long items) {
     return WS_HEADER + ((items * 4ull + 255ull) / 256ull) * 256ull;

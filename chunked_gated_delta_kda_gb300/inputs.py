@@ -12,6 +12,9 @@ workload's seed draws, in this order and in fp32,
   g = logsigmoid(N(0,1)) / 16 per dimension [B,T,H,K], fp32 (so g <= 0);
   beta = sigmoid(N(0,1)) [B,T,H], fp32;
   h0 = 0.1 * N(0,1) [N,H,V,K], fp32, for the workloads that carry one.
+The backward's upstream gradients (``make_grad_inputs``) come from a second
+generator seeded with seed + 7919: do ~ N(0,1) [B,T,H,V] cast to bf16, then
+dht = 0.1 * N(0,1) [N,H,V,K] fp32 (the scale of h0).
 This follows the operator page's "stable inputs" convention (log-sigmoid
 gates, sigmoid beta) with the scalings that the five named workloads fix.
 """
@@ -104,6 +107,23 @@ def make_inputs(w: Workload, device: str = "cpu", draw_on_device: bool = False, 
         assert B == 1 and sum(w.seqlens) == T
         cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=gdev)
     out = dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, cu_seqlens=cu, scale=None, N=w.N)
+    if device != gdev:
+        out = {kk: (vv.to(device) if isinstance(vv, torch.Tensor) else vv) for kk, vv in out.items()}
+    return out
+
+
+def make_grad_inputs(w: Workload, device: str = "cpu", draw_on_device: bool = False, seed_offset: int = 0,
+                     with_dht: bool = True):
+    """Upstream gradients for the backward of ``make_inputs(w)``: a dict with
+    do (bf16 [B,T,H,V]) and dht (fp32 [N,H,V,K] or None)."""
+    gdev = device if draw_on_device else "cpu"
+    gen = torch.Generator(device=gdev)
+    gen.manual_seed(int(w.seed) + 7919 + int(seed_offset))
+    do = torch.randn((w.B, w.T, w.H, w.V), generator=gen, dtype=torch.float32, device=gdev).to(torch.bfloat16)
+    dht = None
+    if with_dht:
+        dht = 0.1 * torch.randn((w.N, w.H, w.V, w.K), generator=gen, dtype=torch.float32, device=gdev)
+    out = dict(do=do, dht=dht)
     if device != gdev:
         out = {kk: (vv.to(device) if isinstance(vv, torch.Tensor) else vv) for kk, vv in out.items()}
     return out

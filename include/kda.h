@@ -118,7 +118,7 @@ kda_status kda_fwd_timed(const void* q, const void* k, const void* v, const floa
 
 /*
  * Synchronise `stream`, then read the device status word that the last
- * kda_fwd or kda_fused_recurrent on this workspace wrote.  Returns KDA_OK,
+ * kda_fwd, kda_bwd or kda_fused_recurrent on this workspace wrote.  Returns KDA_OK,
  * KDA_ERR_BAD_CU_SEQLENS, KDA_ERR_TIMEOUT, KDA_ERR_BAD_STATE_INDEX (in that
  * order of precedence), or KDA_ERR_CUDA if synchronising or reading failed.
  */
@@ -242,6 +242,56 @@ kda_status kda_kcp_fwd(const void* q, const void* k, const void* v, const float*
                        const float* h0, const int32_t* cu_seqlens_host, void* o, float* ht, int T, int H, int K,
                        int V, int N, int world_size, unsigned flags, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream);
+
+/*
+ * Number of CTAs (and of 8 MiB per-CTA scratch buffers) the token-by-token
+ * backward runs at most.
+ */
+#define KDA_BWD_EXACT_MAX_CTAS 152
+
+/*
+ * Bytes of device workspace kda_bwd needs for these sizes (0 on invalid
+ * sizes).  Layout: a 256-byte status header, one fp32 K x V state per
+ * (128-token chunk slot, head), then min(N H, KDA_BWD_EXACT_MAX_CTAS)
+ * scratch buffers of 128 states each.
+ */
+size_t kda_bwd_workspace_bytes(int B, int T, int H, int K, int V, int N);
+
+/*
+ * KDA backward: the gradients of L = sum_t <dout_t, o_t> + sum_n <dht_n, ht_n>
+ * with respect to q, k, v, g, beta and h0, where (o, ht) is the kda_fwd
+ * forward of the same arguments.  The page lists the backward kernels of the
+ * training path (dv, dq/dk/dw/dg, the state gradient dh and the WY
+ * back-propagation) but gives no formulas; this entry point computes their
+ * plain definition, the vector-Jacobian product of the per-token recurrence
+ * documented at the top of this file.
+ *   q, k, v, g, beta, scale, h0, cu_seqlens, B, T, H, K, V, N, flags
+ *               as for kda_fwd (the same forward is differentiated)
+ *   dout        bf16 [B, T, H, V]   dL/do
+ *   dht         fp32 [N, H, V, K]   dL/dht, or NULL for zero
+ *   dq, dk      fp32 [B, T, H, K]   written for every valid token (with
+ *               KDA_FLAG_QK_L2NORM: gradients with respect to the raw,
+ *               unnormalised q and k)
+ *   dv          fp32 [B, T, H, V]
+ *   dg          fp32 [B, T, H, K]
+ *   dbeta       fp32 [B, T, H]
+ *   dh0         fp32 [N, H, V, K]   dL/dh0 (also when h0 is NULL: the
+ *               gradient at the zero state), or NULL to skip it
+ *   workspace   device scratch of at least kda_bwd_workspace_bytes(...)
+ *               bytes, 256-byte aligned, contents need not be initialised;
+ *               calls sharing it must not overlap in time
+ * Method: the forward is replayed token by token in fp32 (the state entering
+ * every 128-token chunk is kept in the workspace, the states inside a chunk
+ * are replayed into a per-CTA scratch), and the chain rule of the token
+ * rule is applied backwards, one (sequence, head) per CTA.  Exact (fp32
+ * arithmetic, fp32 state) for any gate decay.
+ * Errors: as for kda_fwd; an invalid cu_seqlens is reported through
+ * kda_get_status(workspace).
+ */
+kda_status kda_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
+                   const float* h0, const int32_t* cu_seqlens, const void* dout, const float* dht, float* dq,
+                   float* dk, float* dv, float* dg, float* dbeta, float* dh0, int B, int T, int H, int K, int V,
+                   int N, unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Static English description of a status code. */
 const char* kda_status_str(kda_status status);

@@ -1,0 +1,94 @@
+"""GPU parity of the backward entry point (kda_bwd, through the C ABI)
+against the fp64 gradient oracle (``oracle.backward``: torch autograd through
+the per-token recurrence, pinned in ``test_oracle_backward.py``).
+
+Tolerance.  The backward evaluates the chain rule in fp32 from the same bf16
+inputs, so its error is fp32 rounding accumulated along the sequence (the
+state recurrence is contracting for g <= 0, 0 <= beta <= 1 and unit k).  The
+bound is elementwise, |d - d_ref| <= 1e-3 (|d_ref| + rms(d_ref)), i.e. about
+1e-3 of the gradient's typical size, for dq, dk, dv, dg, dbeta and dh0
+(rms over the whole tensor).  Inputs: ``inputs.make_inputs`` and
+``inputs.make_grad_inputs``.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from chunked_gated_delta_kda_gb300.inputs import custom, make_grad_inputs, make_inputs
+from kda_cases import to_np
+from oracle import backward as obw
+
+pytestmark = pytest.mark.gpu
+
+G_RTOL = 1e-3
+NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
+
+
+def run_gpu(x, gr, l2norm=False):
+    from chunked_gated_delta_kda_gb300 import binding
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in {**x, **gr}.items()}
+    out = binding.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["do"], scale=d.get("scale"),
+                      initial_state=d["h0"], dht=d["dht"], use_qk_l2norm_in_kernel=l2norm,
+                      cu_seqlens=d["cu_seqlens"])
+    torch.cuda.synchronize()
+    return [to_np(t).astype(np.float64) for t in out]
+
+
+def run_ref(x, gr, l2norm=False):
+    cu = None if x["cu_seqlens"] is None else x["cu_seqlens"].numpy()
+    return obw.kda_backward(*(to_np(x[n]) for n in ("q", "k", "v", "g", "beta")), to_np(gr["do"]),
+                            scale=x.get("scale"), h0=to_np(x["h0"]), dht=to_np(gr["dht"]), cu_seqlens=cu,
+                            l2norm=l2norm)
+
+
+def check(got, ref, mask=None):
+    """Max ratio of error to bound per gradient (<= 1 passes)."""
+    ratios = {}
+    for name, a, b in zip(NAMES, got, ref):
+        assert np.isfinite(a).all(), f"non-finite {name}"
+        if mask is not None and name != "dh0":
+            a, b = a[mask[name]], b[mask[name]]
+        if b.size == 0:
+            continue
+        rms = float(np.sqrt(np.mean(b * b))) + 1e-30
+        ratios[name] = float((np.abs(a - b) / (G_RTOL * (np.abs(b) + rms))).max())
+    bad = {k: v for k, v in ratios.items() if v > 1.0}
+    assert not bad, ratios
+    return ratios
+
+
+CASES = {
+    "fixed_b2_t256_h2_h0": (custom("b", B=2, T=256, H=2, with_h0=True, seed=11), True),
+    "varlen_ragged_empty": (custom("v", B=1, T=530, H=2, seqlens=(100, 1, 0, 300, 129), with_h0=True, seed=12), True),
+    "no_h0_no_dht": (custom("z", B=1, T=384, H=3, seed=13), False),
+    "t640_h3_five_chunks": (custom("m", B=1, T=640, H=3, with_h0=True, seed=14), True),
+}
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_bwd_matches_oracle(case):
+    w, with_dht = CASES[case]
+    x = make_inputs(w)
+    gr = make_grad_inputs(w, with_dht=with_dht)
+    print(case, check(run_gpu(x, gr), run_ref(x, gr)))
+
+
+def test_bwd_l2norm():
+    w = custom("l2", B=1, T=300, H=2, seqlens=(170, 130), with_h0=True, seed=15)
+    x = make_inputs(w)
+    gen = torch.Generator().manual_seed(5)
+    for n in ("q", "k"):   # unnormalised rows so that the normalisation matters
+        x[n] = (x[n].float() * (0.5 + 2 * torch.rand(x[n].shape[:3] + (1,), generator=gen))).bfloat16()
+    gr = make_grad_inputs(w)
+    print(check(run_gpu(x, gr, l2norm=True), run_ref(x, gr, l2norm=True)))
+
+
+@pytest.mark.parametrize("gate_div", [0.5, 0.1])
+def test_bwd_strong_decay(gate_div):
+    """Decay far beyond the chunked forward's factoring range: the backward
+    replays the forward token by token and stays exact."""
+    w = custom("sd", B=1, T=256, H=2, with_h0=True, seed=16, gate_div=gate_div)
+    x = make_inputs(w)
+    gr = make_grad_inputs(w)
+    print(check(run_gpu(x, gr), run_ref(x, gr)))

@@ -134,3 +134,43 @@ def test_kcp_workspace_and_host_checks():
     assert lib.kda_kcp_fwd(*args) == 4          # offsets not non-decreasing
     args[12] = 64
     assert lib.kda_kcp_fwd(*args) == 2          # K != 128
+
+
+def test_bwd_workspace_and_host_checks():
+    """kda_bwd's workspace formula and its host-side checks (all fail before
+    any CUDA call)."""
+    from chunked_gated_delta_kda_gb300 import binding
+    lib = binding.load_library()
+    state = 128 * 128 * 4
+    # header, one state per (chunk slot, head), then min(N H, 152) scratch buffers of 128 states
+    assert lib.kda_bwd_workspace_bytes(1, 65536, 32, 128, 128, 1) == 256 + 514 * 32 * state + 32 * 128 * state
+    assert lib.kda_bwd_workspace_bytes(4, 8192, 16, 128, 128, 4) == 256 + 256 * 16 * state + 64 * 128 * state
+    assert lib.kda_bwd_workspace_bytes(1, 9192, 32, 128, 128, 6) == 256 + 78 * 32 * state + 152 * 128 * state
+    assert lib.kda_bwd_workspace_bytes(1, 256, 1, 64, 128, 1) == 0
+    if torch.cuda.is_available():
+        return
+    buf = (ctypes.c_uint8 * 4096)()
+    p = ctypes.cast(ctypes.addressof(buf) + (-ctypes.addressof(buf) % 256), ctypes.c_void_p)
+    ws = lib.kda_bwd_workspace_bytes(1, 256, 1, 128, 128, 1)
+
+    def call(**kw):
+        a = dict(q=p, k=p, v=p, g=p, beta=p, scale=0.0, h0=None, cu=None, do=p, dht=None, dq=p, dk=p, dv=p,
+                 dg=p, db=p, dh0=None, B=1, T=256, H=1, K=128, V=128, N=1, flags=0, ws=p, wsb=ws)
+        a.update(kw)
+        return lib.kda_bwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["h0"], a["cu"], a["do"],
+                           a["dht"], a["dq"], a["dk"], a["dv"], a["dg"], a["db"], a["dh0"], a["B"], a["T"], a["H"],
+                           a["K"], a["V"], a["N"], a["flags"], a["ws"], a["wsb"], None)
+
+    assert call(K=64) == 2
+    assert call(do=None) == 1
+    assert call(dg=None) == 1
+    assert call(db=None) == 1
+    assert call(T=200) == 1
+    assert call(N=2) == 1
+    assert call(B=2, N=2, cu=p) == 1
+    assert call(wsb=ws - 1) == 1
+    assert call(flags=8) == 1
+    misaligned = ctypes.c_void_p(p.value + 8)
+    assert call(dq=misaligned) == 1
+    assert call(dh0=misaligned) == 1
+    assert call(ws=misaligned) == 1
