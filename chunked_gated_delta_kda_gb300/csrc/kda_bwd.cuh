@@ -23,8 +23,10 @@ struct BwdParams {
     float* dg;              // fp32 [B*T, H, K]
     float* dbeta;           // fp32 [B*T, H]
     float* dh0;             // fp32 [N, H, V, K] or null
-    float* ckpt;            // fp32 [nslots][H][V][K]: state entering each chunk
-    float* scratch;         // fp32 [ctas][BT][V][K]: states entering each token of a chunk
+    float* ckpt;            // token-by-token kernel: fp32 [nslots][H][V][K], state entering each chunk
+    float* scratch;         // fp32 [ctas][BT][V][K]: states entering tokens of a chunk
+    const float* ckpt_s;    // chunk kernel: fp32 [nslots][H][K][V], S entering each chunk (forward scan)
+    const float* ckpt_d;    // chunk kernel: fp32 [nslots][H][K][V], dS at the end of the mirrored chunk
     uint32_t* status;
     float scale;
     int T, H, N;
@@ -32,6 +34,9 @@ struct BwdParams {
     int l2norm;
 };
 
+struct FwdParams;
+cudaError_t launch_bwd_tiles(const FwdParams& fp, uint8_t* btiles, const uint16_t* dout, cudaStream_t stream);
+cudaError_t launch_bwd_chunk(const BwdParams& p, const FwdParams& fp, int ctas, cudaStream_t stream);
 cudaError_t launch_bwd_exact(const BwdParams& p, const uint32_t* only, int ctas, cudaStream_t stream);
 cudaError_t launch_l2norm_bwd(const BwdParams& p, long long rows, cudaStream_t stream);
 

@@ -1,11 +1,27 @@
 // C ABI of the KDA backward: argument checks, workspace layout and the
 // launch sequence.  See include/kda.h for the contract.
+//
+// Chunked path (default), on the caller's stream:
+//   1. the forward's chunk-parallel kernel (transition tiles, exact flags);
+//   2. the forward's scan in state-only mode, storing S entering each chunk;
+//   3. kda_bwd_tiles_kernel: Nm^T, Qe^T do, Dg at mirrored chunk positions;
+//   4. the scan again on those tiles from dht: dS at every chunk end, dh0;
+//   5. kda_bwd_chunk_kernel: per-chunk fp32 replay and chain rule;
+//   6. the token-by-token backward for the (sequence, head) units the
+//      forward flagged as beyond its factoring range;
+//   7. the q/k normalisation chain rule when requested.
+// KDA_FLAG_BWD_TOKEN_EXACT runs the token-by-token backward for every unit.
 #include <cmath>
 #include <cstdint>
 
 #include "../../include/kda.h"
 #include "kda_bwd.cuh"
 #include "kda_common.cuh"
+
+namespace kda {
+cudaError_t launch_prep(const FwdParams& p, bool l2norm, cudaStream_t stream);
+cudaError_t launch_scan(const FwdParams& p, cudaStream_t stream);
+}  // namespace kda
 
 namespace {
 
@@ -15,9 +31,35 @@ long long bwd_slots(int B, int T, int N, bool varlen) {
     return varlen ? (long long)(T / kda::BT) + N + 1 : (long long)B * ((T + kda::BT - 1) / kda::BT);
 }
 
-int exact_ctas(int H, int N) {
-    const long long units = (long long)N * H;
-    return (int)(units < KDA_BWD_EXACT_MAX_CTAS ? units : KDA_BWD_EXACT_MAX_CTAS);
+long long max_slots(int B, int T, int N) {
+    const long long a = bwd_slots(B, T, N, false), b = bwd_slots(B, T, N, true);
+    return a > b ? a : b;
+}
+
+unsigned long long r256(unsigned long long x) { return (x + 255ull) / 256ull * 256ull; }
+
+// Scratch buffers (one per resident CTA of the per-chunk and token-by-token kernels).
+int scratch_ctas(long long items, int H, int N) {
+    long long u = items > (long long)N * H ? items : (long long)N * H;
+    return (int)(u < KDA_BWD_EXACT_MAX_CTAS ? u : KDA_BWD_EXACT_MAX_CTAS);
+}
+
+struct Layout {
+    unsigned long long tiles, flags, btiles, ckpt_s, ckpt_d, ckpt_x, scratch, total;
+};
+
+Layout layout(int B, int T, int H, int N) {
+    const unsigned long long items = (unsigned long long)max_slots(B, T, N) * (unsigned long long)H;
+    Layout L;
+    L.tiles = kda::ws_tiles_offset(items);
+    L.flags = L.tiles + items * kda::TILE_BYTES;
+    L.btiles = L.flags + r256((unsigned long long)N * H * 4ull);
+    L.ckpt_s = L.btiles + items * kda::TILE_BYTES;
+    L.ckpt_d = L.ckpt_s + items * STATE_BYTES;
+    L.ckpt_x = L.ckpt_d + items * STATE_BYTES;
+    L.scratch = L.ckpt_x + items * STATE_BYTES;
+    L.total = L.scratch + (unsigned long long)scratch_ctas((long long)items, H, N) * kda::BT * STATE_BYTES;
+    return L;
 }
 
 bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -28,11 +70,7 @@ extern "C" {
 
 size_t kda_bwd_workspace_bytes(int B, int T, int H, int K, int V, int N) {
     if (B < 1 || T < 0 || H < 1 || N < 1 || K != kda::KD || V != kda::VD) return 0;
-    long long slots = bwd_slots(B, T, N, false);
-    const long long vs = bwd_slots(B, T, N, true);
-    if (vs > slots) slots = vs;
-    return (size_t)(kda::WS_HEADER + (unsigned long long)slots * H * STATE_BYTES +
-                    (unsigned long long)exact_ctas(H, N) * kda::BT * STATE_BYTES);
+    return (size_t)layout(B, T, H, N).total;
 }
 
 kda_status kda_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
@@ -42,7 +80,7 @@ kda_status kda_bwd(const void* q, const void* k, const void* v, const float* g, 
     if (K != kda::KD || V != kda::VD) return KDA_ERR_UNSUPPORTED;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return KDA_ERR_INVALID_ARG;
     if (B < 1 || T < 0 || H < 1 || N < 1 || H > 65535 || N > 65535) return KDA_ERR_INVALID_ARG;
-    if ((flags & ~KDA_FLAG_QK_L2NORM) != 0u) return KDA_ERR_INVALID_ARG;
+    if ((flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_BWD_TOKEN_EXACT)) != 0u) return KDA_ERR_INVALID_ARG;
     if (cu_seqlens == nullptr) {
         if (N != B || T % kda::BT != 0) return KDA_ERR_INVALID_ARG;
     } else if (B != 1) {
@@ -60,10 +98,39 @@ kda_status kda_bwd(const void* q, const void* k, const void* v, const float* g, 
     if ((long long)B * T * H * kda::KD >= (1ll << 62)) return KDA_ERR_INVALID_ARG;
     if (!(scale > 0.f) || std::isnan(scale)) scale = 1.0f / std::sqrt((float)K);
 
+    const bool varlen = cu_seqlens != nullptr;
+    const bool l2norm = (flags & KDA_FLAG_QK_L2NORM) != 0u;
+    const unsigned long long items = (unsigned long long)max_slots(B, T, N) * (unsigned long long)H;
+    const Layout L = layout(B, T, H, N);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+    kda::FwdParams fp{};
+    fp.q = static_cast<const uint16_t*>(q);
+    fp.k = static_cast<const uint16_t*>(k);
+    fp.v = static_cast<const uint16_t*>(v);
+    fp.g = g;
+    fp.beta = beta;
+    fp.h0 = h0;
+    fp.cu = cu_seqlens;
+    fp.o = nullptr;
+    fp.ht = nullptr;
+    fp.status = reinterpret_cast<uint32_t*>(ws);
+    fp.wide_count = reinterpret_cast<uint32_t*>(ws) + 1;
+    fp.wide_list = reinterpret_cast<int32_t*>(ws + kda::WS_HEADER);
+    fp.tiles = ws + L.tiles;
+    fp.exact_flags = reinterpret_cast<uint32_t*>(ws + L.flags);
+    fp.ckpt = reinterpret_cast<float*>(ws + L.ckpt_s);
+    fp.scale = scale;
+    fp.T = T;
+    fp.H = H;
+    fp.N = N;
+    fp.NT = varlen ? 0 : T / kda::BT;
+    fp.nslots = varlen ? T / kda::BT + N + 1 : N * (T / kda::BT);
+
     kda::BwdParams p{};
-    p.q = static_cast<const uint16_t*>(q);
-    p.k = static_cast<const uint16_t*>(k);
-    p.v = static_cast<const uint16_t*>(v);
+    p.q = fp.q;
+    p.k = fp.k;
+    p.v = fp.v;
     p.g = g;
     p.beta = beta;
     p.h0 = h0;
@@ -76,22 +143,38 @@ kda_status kda_bwd(const void* q, const void* k, const void* v, const float* g, 
     p.dg = dg;
     p.dbeta = dbeta;
     p.dh0 = dh0;
-    const bool varlen = cu_seqlens != nullptr;
-    const long long slots = bwd_slots(B, T, N, varlen);
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    p.status = reinterpret_cast<uint32_t*>(ws);
-    p.ckpt = reinterpret_cast<float*>(ws + kda::WS_HEADER);
-    p.scratch = reinterpret_cast<float*>(ws + kda::WS_HEADER + (unsigned long long)slots * H * STATE_BYTES);
+    p.ckpt = reinterpret_cast<float*>(ws + L.ckpt_x);
+    p.scratch = reinterpret_cast<float*>(ws + L.scratch);
+    p.ckpt_s = reinterpret_cast<const float*>(ws + L.ckpt_s);
+    p.ckpt_d = reinterpret_cast<const float*>(ws + L.ckpt_d);
+    p.status = fp.status;
     p.scale = scale;
     p.T = T;
     p.H = H;
     p.N = N;
-    p.NT = varlen ? 0 : T / kda::BT;
-    p.l2norm = (flags & KDA_FLAG_QK_L2NORM) ? 1 : 0;
+    p.NT = fp.NT;
+    p.l2norm = l2norm ? 1 : 0;
+    const int ctas = scratch_ctas((long long)items, H, N);
 
     if (cudaMemsetAsync(workspace, 0, kda::WS_CLEAR, stream) != cudaSuccess) return KDA_ERR_CUDA;
-    if (kda::launch_bwd_exact(p, nullptr, exact_ctas(H, N), stream) != cudaSuccess) return KDA_ERR_CUDA;
-    if (p.l2norm && kda::launch_l2norm_bwd(p, (long long)B * T * H, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (flags & KDA_FLAG_BWD_TOKEN_EXACT) {
+        if (kda::launch_bwd_exact(p, nullptr, ctas < N * H ? ctas : N * H, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    } else {
+        if (cudaMemsetAsync(fp.exact_flags, 0, (size_t)N * H * 4, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        if (fp.nslots > 0 && kda::launch_prep(fp, l2norm, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        if (kda::launch_scan(fp, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        if (kda::launch_bwd_tiles(fp, ws + L.btiles, p.dout, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        kda::FwdParams rp = fp;   // the reverse state pass
+        rp.tiles = ws + L.btiles;
+        rp.h0 = dht;
+        rp.ht = dh0;
+        rp.ckpt = reinterpret_cast<float*>(ws + L.ckpt_d);
+        if (kda::launch_scan(rp, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        if (kda::launch_bwd_chunk(p, fp, ctas, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        if (kda::launch_bwd_exact(p, fp.exact_flags, ctas < N * H ? ctas : N * H, stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    }
+    if (l2norm && kda::launch_l2norm_bwd(p, (long long)B * T * H, stream) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }
 

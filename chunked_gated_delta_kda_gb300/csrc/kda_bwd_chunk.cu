@@ -1,0 +1,391 @@
+// Chunk-parallel KDA backward.
+//
+// The forward in the transition form (section "算法原理" M4 of the page
+// "PyPTO-Gym chunk_kda operator: an NPU forward of chunked gated delta-rule
+// linear attention"), per 128-token chunk c with entering state S_c (K x V):
+//   S_{c+1} = Dg_c * S_c + Nm_c S_c + Bc_c,     o_c = Qe_c S_c + Oi_c
+// so the state gradient obeys, from dS_N = dht backwards,
+//   dS_c = Dg_c * dS_{c+1} + Nm_c^T dS_{c+1} + Qe_c^T do_c.
+// That is the forward's state recurrence again, on the tiles (Nm^T, Qe^T do,
+// Dg) in reverse chunk order.  kda_bwd_tiles_kernel builds those tiles from
+// the forward's; the forward's scan kernel then runs it (state-only mode) and
+// stores dS_{c+1} for every chunk.  With S_c (stored by the forward scan) and
+// dS_{c+1} known, every chunk is independent: kda_bwd_chunk_kernel replays
+// its 128 tokens forward in fp32 and applies the per-token chain rule
+// backwards (the same rule as the token-by-token backward kernel).
+//
+// Replaying backwards needs the state entering each token.  The kernel keeps
+// the delta residual r_t = v_t - k_t.(exp(g_t) S_{t-1}) of every token (64
+// KiB of shared memory per chunk) and a copy of the state every 16 tokens
+// (in a per-CTA global scratch that stays in L2), and reconstructs
+//   exp(g_t) S_{t-1} = S_t - beta_t k_t r_t^T,   S_{t-1} = exp(-g_t) (that)
+// which multiplies rounding errors by exp(-g) per token; the 16-token copies
+// bound the growth to exp(sum of -g over 16 tokens).  A chunk where that sum
+// exceeds EXACT_WINDOW_DECAY in some dimension stores the state entering
+// every token instead (8 MiB of scratch) and needs no division.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kda.h"
+#include "kda_bwd.cuh"
+#include "kda_common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace kda {
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// Transposed tiles
+// ---------------------------------------------------------------------------
+constexpr int BT_THREADS = 256;
+constexpr int QF_LD = KD + 4;                        // padded fp32 rows
+constexpr uint32_t BT_SMEM = 2u * BT * QF_LD * 4u;   // Qe (fp32) and do (fp32)
+
+__device__ __forceinline__ float2 h2f(uint32_t u) {
+    __half2 h = *reinterpret_cast<__half2*>(&u);
+    return __half22float2(h);
+}
+__device__ __forceinline__ uint32_t f2h(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+}  // namespace
+
+// One CTA per (chunk slot, head): writes, at the mirrored chunk position of
+// the same sequence, the tile the reverse state pass reads: Nm^T (same fp16
+// 128-byte-swizzled layout as Nm), Qe^T do as the four fp16 Bc pieces, Dg.
+__global__ void __launch_bounds__(BT_THREADS) kda_bwd_tiles_kernel(const FwdParams fp, uint8_t* btiles,
+                                                                   const uint16_t* __restrict__ dout) {
+    extern __shared__ __align__(16) float bsm[];
+    float* qf = bsm;                   // Qe[t][d], fp32
+    float* df = bsm + BT * QF_LD;      // do[t][v], fp32 (first: raw Nm bytes)
+    const int slot = (int)blockIdx.x, h = (int)blockIdx.y;
+    const int tid = threadIdx.x;
+    const int H = fp.H;
+    ChunkRef c;
+    if (!slot_chunk(fp, slot, c)) return;
+    long long bos;
+    int len;
+    if (!seq_bounds(fp, c.n, bos, len)) return;
+    const int nch = (len + BT - 1) / BT;
+    const uint8_t* src = tile_ptr(fp, slot, h);
+    uint8_t* dst = btiles + ((size_t)chunk_slot(fp, c.n, nch - 1 - c.j) * H + h) * TILE_BYTES;
+
+    // Nm^T: stage the raw tile, then write (d, e) <- Nm(e, d) in 16-byte runs
+    uint8_t* raw = reinterpret_cast<uint8_t*>(df);
+    for (int i = tid; i < KD * KD * 2 / 16; i += BT_THREADS)
+        reinterpret_cast<uint4*>(raw)[i] = reinterpret_cast<const uint4*>(src + TILE_NM)[i];
+    if (tid < KD / 4)
+        reinterpret_cast<float4*>(dst + TILE_DG)[tid] = reinterpret_cast<const float4*>(src + TILE_DG)[tid];
+    __syncthreads();
+    for (int i = tid; i < KD * KD / 8; i += BT_THREADS) {
+        const int d = i >> 4, e0 = (i & 15) * 8;
+        uint16_t x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = *reinterpret_cast<const uint16_t*>(raw + sw128_off(e0 + u, d, 128));
+        *reinterpret_cast<uint4*>(dst + TILE_NM + sw128_off(d, e0, 128)) =
+            make_uint4(x[0] | ((uint32_t)x[1] << 16), x[2] | ((uint32_t)x[3] << 16), x[4] | ((uint32_t)x[5] << 16),
+                       x[6] | ((uint32_t)x[7] << 16));
+    }
+    __syncthreads();
+
+    // Qe and do of the chunk's valid rows, fp32
+    for (int i = tid; i < BT * KD / 8; i += BT_THREADS) {
+        const int t = i >> 4, c8 = (i & 15) * 8;
+        float qv[8], dv[8];
+        if (t < c.len) {
+            const uint4 a = *reinterpret_cast<const uint4*>(src + TILE_QE + sw128_off(t, c8, 128));
+            const float2 a0 = h2f(a.x), a1 = h2f(a.y), a2 = h2f(a.z), a3 = h2f(a.w);
+            qv[0] = a0.x; qv[1] = a0.y; qv[2] = a1.x; qv[3] = a1.y; qv[4] = a2.x; qv[5] = a2.y; qv[6] = a3.x; qv[7] = a3.y;
+            const uint4 b = *reinterpret_cast<const uint4*>(dout + ((size_t)(c.tok0 + t) * H + h) * VD + c8);
+            dv[0] = __uint_as_float(b.x << 16); dv[1] = __uint_as_float(b.x & 0xffff0000u);
+            dv[2] = __uint_as_float(b.y << 16); dv[3] = __uint_as_float(b.y & 0xffff0000u);
+            dv[4] = __uint_as_float(b.z << 16); dv[5] = __uint_as_float(b.z & 0xffff0000u);
+            dv[6] = __uint_as_float(b.w << 16); dv[7] = __uint_as_float(b.w & 0xffff0000u);
+        } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) qv[u] = dv[u] = 0.f;
+        }
+        float4* qd = reinterpret_cast<float4*>(qf + t * QF_LD + c8);
+        float4* dd = reinterpret_cast<float4*>(df + t * QF_LD + c8);
+        qd[0] = make_float4(qv[0], qv[1], qv[2], qv[3]);
+        qd[1] = make_float4(qv[4], qv[5], qv[6], qv[7]);
+        dd[0] = make_float4(dv[0], dv[1], dv[2], dv[3]);
+        dd[1] = make_float4(dv[4], dv[5], dv[6], dv[7]);
+    }
+    __syncthreads();
+
+    // Bq[d][v] = sum_t Qe[t][d] do[t][v]: thread owns d0..d0+7 x v0..v0+7
+    const int d0 = (tid >> 4) * 8, v0 = (tid & 15) * 8;
+    float acc[8][8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[r][u] = 0.f;
+    const int rows = c.len;
+#pragma unroll 2
+    for (int t = 0; t < rows; ++t) {
+        const float4 a0 = *reinterpret_cast<const float4*>(qf + t * QF_LD + d0);
+        const float4 a1 = *reinterpret_cast<const float4*>(qf + t * QF_LD + d0 + 4);
+        const float4 b0 = *reinterpret_cast<const float4*>(df + t * QF_LD + v0);
+        const float4 b1 = *reinterpret_cast<const float4*>(df + t * QF_LD + v0 + 4);
+        const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc[r][u] = fmaf(a[r], b[u], acc[r][u]);
+    }
+    uint8_t* piece = dst + TILE_BC + (v0 / BV) * BC_PIECE;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+        *reinterpret_cast<uint4*>(piece + sw64_off(d0 + r, v0 % BV)) =
+            make_uint4(f2h(acc[r][0], acc[r][1]), f2h(acc[r][2], acc[r][3]), f2h(acc[r][4], acc[r][5]),
+                       f2h(acc[r][6], acc[r][7]));
+}
+
+// ---------------------------------------------------------------------------
+// Chunk-local backward
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int CB_THREADS = 512;
+constexpr int CB_WARPS = CB_THREADS / 32;
+constexpr int CB_ROWS = 8;
+constexpr int CB_RED = 3 * KD + 4;
+constexpr int CB_WIN = 16;                          // tokens between stored states
+constexpr float EXACT_WINDOW_DECAY = 7.0f;          // max sum of -g over a window before exact mode
+constexpr uint32_t CB_RED_BYTES = 2u * CB_WARPS * CB_RED * 4u;
+constexpr uint32_t CB_SMEM = CB_RED_BYTES + BT * VD * 4u;   // + residuals r[t][v]
+
+struct Tok {
+    float q[4], k[4], e[4], ie[4];
+    float beta;
+    float v[CB_ROWS];
+};
+
+__device__ __forceinline__ void rows8_bf16(const uint16_t* p, float (&x)[CB_ROWS]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
+    x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xffff0000u);
+    x[4] = __uint_as_float(u.z << 16); x[5] = __uint_as_float(u.z & 0xffff0000u);
+    x[6] = __uint_as_float(u.w << 16); x[7] = __uint_as_float(u.w & 0xffff0000u);
+}
+
+__device__ __forceinline__ void tok_load(const BwdParams& p, size_t tok, int v0, int lane, Tok& in) {
+    load4_bf16(p.q + tok * KD + 4 * lane, in.q);
+    load4_bf16(p.k + tok * KD + 4 * lane, in.k);
+    const float4 gv = *reinterpret_cast<const float4*>(p.g + tok * KD + 4 * lane);
+    in.beta = p.beta[tok];
+    rows8_bf16(p.v + tok * VD + v0, in.v);
+    float qs = p.scale, ks = 1.f;
+    if (p.l2norm) {   // x / sqrt(sum x^2 + 1e-6), section "测试与验证体系"
+        const float sq = warp_sum(in.q[0] * in.q[0] + in.q[1] * in.q[1] + in.q[2] * in.q[2] + in.q[3] * in.q[3]);
+        const float sk = warp_sum(in.k[0] * in.k[0] + in.k[1] * in.k[1] + in.k[2] * in.k[2] + in.k[3] * in.k[3]);
+        qs *= rsqrtf(sq + 1e-6f);
+        ks = rsqrtf(sk + 1e-6f);
+    }
+    const float g[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        in.q[i] *= qs;
+        in.k[i] *= ks;
+        in.e[i] = __expf(g[i]);
+        in.ie[i] = __expf(-g[i]);
+    }
+}
+
+// state rows v0..v0+7, K entries 4 lane..+3, from a [K][V] fp32 slab
+__device__ __forceinline__ void load_kv(const float* slab, int v0, int lane, float (&s)[CB_ROWS][4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 a = *reinterpret_cast<const float4*>(slab + (size_t)(4 * lane + i) * VD + v0);
+        const float4 b = *reinterpret_cast<const float4*>(slab + (size_t)(4 * lane + i) * VD + v0 + 4);
+        s[0][i] = a.x; s[1][i] = a.y; s[2][i] = a.z; s[3][i] = a.w;
+        s[4][i] = b.x; s[5][i] = b.y; s[6][i] = b.z; s[7][i] = b.w;
+    }
+}
+
+// own entries of a [V][K] fp32 state (each thread reads back what it wrote)
+__device__ __forceinline__ void put_vk(float* slab, int v0, int lane, const float (&s)[CB_ROWS][4]) {
+#pragma unroll
+    for (int r = 0; r < CB_ROWS; ++r)
+        *reinterpret_cast<float4*>(slab + (size_t)(v0 + r) * KD + 4 * lane) = make_float4(s[r][0], s[r][1], s[r][2], s[r][3]);
+}
+__device__ __forceinline__ void get_vk(const float* slab, int v0, int lane, float (&s)[CB_ROWS][4]) {
+#pragma unroll
+    for (int r = 0; r < CB_ROWS; ++r) {
+        const float4 x = *reinterpret_cast<const float4*>(slab + (size_t)(v0 + r) * KD + 4 * lane);
+        s[r][0] = x.x; s[r][1] = x.y; s[r][2] = x.z; s[r][3] = x.w;
+    }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(CB_THREADS, 1) kda_bwd_chunk_kernel(const BwdParams p, const FwdParams fp) {
+    extern __shared__ __align__(16) float csm[];
+    float* red = csm;                                   // [2][CB_WARPS][CB_RED]
+    float* rres = csm + CB_RED_BYTES / 4;               // [BT][VD]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int v0 = warp * CB_ROWS;
+    const int H = p.H;
+    const long long items = (long long)fp.nslots * H;
+    float* scratch = p.scratch + (size_t)blockIdx.x * BT * VD * KD;
+
+    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+        const int slot = (int)(it / H), h = (int)(it % H);
+        ChunkRef c;
+        if (!slot_chunk(fp, slot, c)) continue;                    // uniform
+        if (fp.exact_flags[(size_t)c.n * H + h] != 0u) continue;   // replayed by the token-by-token kernel
+        long long bos;
+        int len;
+        if (!seq_bounds(fp, c.n, bos, len)) continue;
+        const int nch = (len + BT - 1) / BT;
+        const int rows = c.len;
+
+        // window decay check: warp w < 8 sums max(-g, 0) over tokens [16 w, 16 w + 16)
+        bool big = false;
+        if (warp < BT / CB_WIN) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int t = warp * CB_WIN; t < min(rows, (warp + 1) * CB_WIN); ++t) {
+                const float4 gv = *reinterpret_cast<const float4*>(p.g + ((size_t)(c.tok0 + t) * H + h) * KD + 4 * lane);
+                acc[0] += fmaxf(-gv.x, 0.f); acc[1] += fmaxf(-gv.y, 0.f);
+                acc[2] += fmaxf(-gv.z, 0.f); acc[3] += fmaxf(-gv.w, 0.f);
+            }
+            big = fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])) > EXACT_WINDOW_DECAY ||
+                  !(acc[0] + acc[1] + acc[2] + acc[3] < 3.0e38f);
+        }
+        const int win = __syncthreads_or(big) ? 1 : CB_WIN;
+
+        // phase A: replay the chunk forward from S_c, keeping r_t and the stored states
+        float s[CB_ROWS][4];
+        load_kv(p.ckpt_s + ((size_t)slot * H + h) * KD * VD, v0, lane, s);
+        for (int t = 0; t < rows; ++t) {
+            if (t % win == 0) put_vk(scratch + (size_t)(t / win) * VD * KD, v0, lane, s);
+            Tok in;
+            tok_load(p, (size_t)(c.tok0 + t) * H + h, v0, lane, in);
+            float dot[CB_ROWS];
+#pragma unroll
+            for (int r = 0; r < CB_ROWS; ++r) {
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    s[r][i] *= in.e[i];
+                    acc = fmaf(in.k[i], s[r][i], acc);
+                }
+                dot[r] = acc;
+            }
+            warp_sum8(dot, lane);
+#pragma unroll
+            for (int r = 0; r < CB_ROWS; ++r) {
+                dot[r] = in.v[r] - dot[r];
+                const float br = in.beta * dot[r];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) s[r][i] = fmaf(in.k[i], br, s[r][i]);
+            }
+            if (lane == 0) {
+                float4* rr = reinterpret_cast<float4*>(rres + (size_t)t * VD + v0);
+                rr[0] = make_float4(dot[0], dot[1], dot[2], dot[3]);
+                rr[1] = make_float4(dot[4], dot[5], dot[6], dot[7]);
+            }
+        }
+        __syncthreads();
+
+        // phase B: the chain rule backwards from dS_{c+1}
+        float d[CB_ROWS][4];
+        load_kv(p.ckpt_d + ((size_t)chunk_slot(fp, c.n, nch - 1 - c.j) * H + h) * KD * VD, v0, lane, d);
+        for (int t = rows - 1; t >= 0; --t) {
+            const size_t tok = (size_t)(c.tok0 + t) * H + h;
+            Tok in;
+            tok_load(p, tok, v0, lane, in);
+            float dov[CB_ROWS], rr[CB_ROWS], gk[CB_ROWS];
+            rows8_bf16(p.dout + tok * VD + v0, dov);
+            {
+                const float4 a = *reinterpret_cast<const float4*>(rres + (size_t)t * VD + v0);
+                const float4 b = *reinterpret_cast<const float4*>(rres + (size_t)t * VD + v0 + 4);
+                rr[0] = a.x; rr[1] = a.y; rr[2] = a.z; rr[3] = a.w; rr[4] = b.x; rr[5] = b.y; rr[6] = b.z; rr[7] = b.w;
+            }
+            float pdq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int r = 0; r < CB_ROWS; ++r) {
+                const float br = in.beta * rr[r];
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    pdq[i] = fmaf(dov[r], s[r][i], pdq[i]);        // do_v s_v'
+                    s[r][i] = fmaf(-br, in.k[i], s[r][i]);          // a_v = s_v' - beta r_v k
+                    d[r][i] = fmaf(dov[r], in.q[i], d[r][i]);       // G_v
+                    acc = fmaf(d[r][i], in.k[i], acc);
+                }
+                gk[r] = acc;
+            }
+            warp_sum8(gk, lane);
+            float pdk[4] = {0.f, 0.f, 0.f, 0.f}, pdg[4] = {0.f, 0.f, 0.f, 0.f};
+            float pdb = 0.f;
+#pragma unroll
+            for (int r = 0; r < CB_ROWS; ++r) {
+                pdb = fmaf(rr[r], gk[r], pdb);
+                const float bg = in.beta * gk[r];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    pdk[i] = fmaf(rr[r], d[r][i], fmaf(-gk[r], s[r][i], pdk[i]));
+                    d[r][i] = fmaf(-bg, in.k[i], d[r][i]);          // dA_v
+                    pdg[i] = fmaf(d[r][i], s[r][i], pdg[i]);
+                    d[r][i] *= in.e[i];                              // dL/ds_v before the token
+                }
+            }
+            if (lane < 2) {
+                const int r0 = 4 * lane;
+                *reinterpret_cast<float4*>(p.dv + tok * VD + v0 + r0) =
+                    make_float4(in.beta * gk[r0], in.beta * gk[r0 + 1], in.beta * gk[r0 + 2], in.beta * gk[r0 + 3]);
+            }
+            // the state entering token t: stored, or exp(-g) a
+            if (t % win == 0) {
+                if (t > 0) get_vk(scratch + (size_t)(t / win) * VD * KD, v0, lane, s);
+            } else {
+#pragma unroll
+                for (int r = 0; r < CB_ROWS; ++r)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) s[r][i] *= in.ie[i];
+            }
+            float* buf = red + ((size_t)(t & 1) * CB_WARPS + warp) * CB_RED;
+            *reinterpret_cast<float4*>(buf + 4 * lane) = make_float4(pdq[0], pdq[1], pdq[2], pdq[3]);
+            *reinterpret_cast<float4*>(buf + KD + 4 * lane) = make_float4(pdk[0], pdk[1], pdk[2], pdk[3]);
+            *reinterpret_cast<float4*>(buf + 2 * KD + 4 * lane) = make_float4(pdg[0], pdg[1], pdg[2], pdg[3]);
+            if (lane == 0) buf[3 * KD] = pdb;
+            __syncthreads();
+            const int i = threadIdx.x;
+            if (i <= 3 * KD) {
+                const float* col = red + (size_t)(t & 1) * CB_WARPS * CB_RED + i;
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < CB_WARPS; ++w) sum += col[(size_t)w * CB_RED];
+                if (i < KD) p.dq[tok * KD + i] = p.scale * sum;
+                else if (i < 2 * KD) p.dk[tok * KD + i - KD] = in.beta * sum;
+                else if (i < 3 * KD) p.dg[tok * KD + i - 2 * KD] = sum;
+                else p.dbeta[tok] = sum;
+            }
+        }
+        __syncthreads();   // this chunk's last reduction and residuals are read
+    }
+}
+
+cudaError_t launch_bwd_tiles(const FwdParams& fp, uint8_t* btiles, const uint16_t* dout, cudaStream_t stream) {
+    if (fp.nslots == 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kda_bwd_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BT_SMEM);
+    if (e != cudaSuccess) return e;
+    kda_bwd_tiles_kernel<<<dim3((unsigned)fp.nslots, (unsigned)fp.H), BT_THREADS, BT_SMEM, stream>>>(fp, btiles, dout);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_chunk(const BwdParams& p, const FwdParams& fp, int ctas, cudaStream_t stream) {
+    if (fp.nslots == 0 || ctas == 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kda_bwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CB_SMEM);
+    if (e != cudaSuccess) return e;
+    kda_bwd_chunk_kernel<<<ctas, CB_THREADS, CB_SMEM, stream>>>(p, fp);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

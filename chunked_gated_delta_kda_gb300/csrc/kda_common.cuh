@@ -130,6 +130,7 @@ struct FwdParams {
     uint32_t* wide_count;   // number of work items queued for the wide-range path
     int32_t* wide_list;     // their ids (slot * H + head)
     uint32_t* exact_flags;  // [N][H]: 1 where a chunk exceeded the exact factoring range
+    float* ckpt;            // scan: fp32 [nslots][H][K][V], the state entering each chunk, or null
     float scale;
     int T;                  // per-sequence length (fixed) or packed length (varlen)
     int H;

@@ -2,6 +2,9 @@
 // head, 32-wide value tile) it walks the chunks in order carrying the state
 // S (K x 32, fp32, one row per thread) and produces the output rows:
 //   S' = Dg * S + Nm S + Bc,     o = Qe S + Oi
+// With o null it runs the state recurrence alone (the backward runs it on
+// transposed tiles in reverse chunk order to carry the state gradient), and
+// with ckpt set it also stores the fp32 state entering every chunk.
 // which is step M4 of the page "PyPTO-Gym chunk_kda operator: an NPU forward
 // of chunked gated delta-rule linear attention" (section "算法原理") in the
 // exact re-associated form set out in kda_common.cuh.  The initial and final
@@ -166,6 +169,13 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
         // ------------------------------------------------------------------
         for (int j = 0; j < nch; ++j) {
             const int s = j & 1;
+            if (p.ckpt != nullptr) {   // the state entering chunk j, row d, [K][V] layout
+                float4* ck = reinterpret_cast<float4*>(p.ckpt + (((size_t)chunk_slot(p, n, j) * H + h) * KD + row) * VD +
+                                                       vt * BV);
+#pragma unroll
+                for (int c4 = 0; c4 < BV / 4; ++c4)
+                    ck[c4] = make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]);
+            }
             wait(full(s), (uint32_t)(j >> 1) & 1u);   // Bc / Dg of this chunk have landed
             wait(mmas, (uint32_t)j & 1u);
             tc_fence_after();
@@ -211,9 +221,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
         }
     } else if (warp < 8) {
         // ------------------------------------------------------------------
-        // Output: o rows of chunk j from TMEM buffer j & 1 plus Oi.
+        // Output: o rows of chunk j from TMEM buffer j & 1 plus Oi (none
+        // when o is null: a state-only pass).
         // ------------------------------------------------------------------
-        for (int j = 0; j < nch; ++j) {
+        for (int j = 0; j < (p.o != nullptr ? nch : 0); ++j) {
             const int b = j & 1, r = j & 3;
             wait(mmao(b), (uint32_t)(j >> 1) & 1u);
             tc_fence_after();
@@ -272,7 +283,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
                                 id, ks > 0);
                     mma_commit(mmas);
                 }
-                if (j >= 1) {
+                if (j >= 1 && p.o != nullptr) {
                     const int c = j - 1, b = c & 1;
                     wait(qfull(b), (uint32_t)(c >> 1) & 1u);
                     if (c >= 2) wait(ofree(b), (uint32_t)((c - 2) >> 1) & 1u);
@@ -303,7 +314,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
                 if (c >= 2) wait(sfree(s), (uint32_t)((c - 2) >> 1) & 1u);
                 load_stage(p, chunk_slot(p, n, c), h, vt, sbase + (uint32_t)s * ST_STRIDE, full(s));
             }
-        } else if (warp == 10 && lane == 0) {
+        } else if (warp == 10 && lane == 0 && p.o != nullptr) {
             for (int c = 0; c < nch; ++c) {
                 const int s = c & 1, r = c & 3;
                 const uint8_t* src = tile_ptr(p, chunk_slot(p, n, c), h);

@@ -56,6 +56,10 @@ typedef enum {
  * inside the kernel, before the scale (section "测试与验证体系" of the page). */
 #define KDA_FLAG_QK_L2NORM 1u
 
+/* kda_bwd only: run the token-by-token backward for every (sequence, head)
+ * instead of the chunked one (fp32 throughout; slower). */
+#define KDA_FLAG_BWD_TOKEN_EXACT 2u
+
 /*
  * Bytes of device workspace kda_fwd needs for these sizes (an upper bound
  * that covers both fixed-length and varlen packing).  0 on invalid sizes.

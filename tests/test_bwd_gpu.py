@@ -2,13 +2,16 @@
 against the fp64 gradient oracle (``oracle.backward``: torch autograd through
 the per-token recurrence, pinned in ``test_oracle_backward.py``).
 
-Tolerance.  The backward evaluates the chain rule in fp32 from the same bf16
-inputs, so its error is fp32 rounding accumulated along the sequence (the
-state recurrence is contracting for g <= 0, 0 <= beta <= 1 and unit k).  The
-bound is elementwise, |d - d_ref| <= 1e-3 (|d_ref| + rms(d_ref)), i.e. about
-1e-3 of the gradient's typical size, for dq, dk, dv, dg, dbeta and dh0
-(rms over the whole tensor).  Inputs: ``inputs.make_inputs`` and
-``inputs.make_grad_inputs``.
+Two paths are checked.  The token-by-token path evaluates the chain rule in
+fp32 from the same bf16 inputs, so its error is fp32 rounding accumulated
+along the sequence (the state recurrence is contracting for g <= 0,
+0 <= beta <= 1 and unit k): bound |d - d_ref| <= 1e-3 (|d_ref| + rms(d_ref))
+elementwise (rms over the whole tensor), about 1e-3 of the gradient's typical
+size.  The chunked path starts every chunk from the state the forward's scan
+carries (fp16 operands, fp32 accumulation: ~1e-3 relative, the forward's own
+state tolerance) and carries the state gradient with the same products, so
+its bound is ten times wider, 1e-2 (|d_ref| + rms(d_ref)), the forward's
+tolerance on o.  Inputs: ``inputs.make_inputs`` and ``inputs.make_grad_inputs``.
 """
 
 import numpy as np
@@ -21,16 +24,16 @@ from oracle import backward as obw
 
 pytestmark = pytest.mark.gpu
 
-G_RTOL = 1e-3
+G_RTOL = {"token": 1e-3, "chunk": 1e-2}
 NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
 
 
-def run_gpu(x, gr, l2norm=False):
+def run_gpu(x, gr, l2norm=False, path="chunk"):
     from chunked_gated_delta_kda_gb300 import binding
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in {**x, **gr}.items()}
     out = binding.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["do"], scale=d.get("scale"),
                       initial_state=d["h0"], dht=d["dht"], use_qk_l2norm_in_kernel=l2norm,
-                      cu_seqlens=d["cu_seqlens"])
+                      cu_seqlens=d["cu_seqlens"], token_exact=(path == "token"))
     torch.cuda.synchronize()
     return [to_np(t).astype(np.float64) for t in out]
 
@@ -42,7 +45,7 @@ def run_ref(x, gr, l2norm=False):
                             l2norm=l2norm)
 
 
-def check(got, ref, mask=None):
+def check(got, ref, path, mask=None):
     """Max ratio of error to bound per gradient (<= 1 passes)."""
     ratios = {}
     for name, a, b in zip(NAMES, got, ref):
@@ -52,7 +55,7 @@ def check(got, ref, mask=None):
         if b.size == 0:
             continue
         rms = float(np.sqrt(np.mean(b * b))) + 1e-30
-        ratios[name] = float((np.abs(a - b) / (G_RTOL * (np.abs(b) + rms))).max())
+        ratios[name] = float((np.abs(a - b) / (G_RTOL[path] * (np.abs(b) + rms))).max())
     bad = {k: v for k, v in ratios.items() if v > 1.0}
     assert not bad, ratios
     return ratios
@@ -66,12 +69,17 @@ CASES = {
 }
 
 
+PATHS = ["chunk", "token"]
+
+
 @pytest.mark.parametrize("case", list(CASES))
 def test_bwd_matches_oracle(case):
     w, with_dht = CASES[case]
     x = make_inputs(w)
     gr = make_grad_inputs(w, with_dht=with_dht)
-    print(case, check(run_gpu(x, gr), run_ref(x, gr)))
+    ref = run_ref(x, gr)
+    for path in PATHS:
+        print(case, path, check(run_gpu(x, gr, path=path), ref, path))
 
 
 def test_bwd_l2norm():
@@ -81,14 +89,19 @@ def test_bwd_l2norm():
     for n in ("q", "k"):   # unnormalised rows so that the normalisation matters
         x[n] = (x[n].float() * (0.5 + 2 * torch.rand(x[n].shape[:3] + (1,), generator=gen))).bfloat16()
     gr = make_grad_inputs(w)
-    print(check(run_gpu(x, gr, l2norm=True), run_ref(x, gr, l2norm=True)))
+    ref = run_ref(x, gr, l2norm=True)
+    for path in PATHS:
+        print(path, check(run_gpu(x, gr, l2norm=True, path=path), ref, path))
 
 
 @pytest.mark.parametrize("gate_div", [0.5, 0.1])
 def test_bwd_strong_decay(gate_div):
-    """Decay far beyond the chunked forward's factoring range: the backward
-    replays the forward token by token and stays exact."""
+    """Decay far beyond the chunked forward's factoring range: those units
+    go to the token-by-token backward, and chunks whose 16-token windows
+    decay strongly keep every token's state; the result stays exact."""
     w = custom("sd", B=1, T=256, H=2, with_h0=True, seed=16, gate_div=gate_div)
     x = make_inputs(w)
     gr = make_grad_inputs(w)
-    print(check(run_gpu(x, gr), run_ref(x, gr)))
+    ref = run_ref(x, gr)
+    for path in PATHS:
+        print(path, check(run_gpu(x, gr, path=path), ref, path))

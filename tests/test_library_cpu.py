@@ -142,10 +142,22 @@ def test_bwd_workspace_and_host_checks():
     from chunked_gated_delta_kda_gb300 import binding
     lib = binding.load_library()
     state = 128 * 128 * 4
-    # header, one state per (chunk slot, head), then min(N H, 152) scratch buffers of 128 states
-    assert lib.kda_bwd_workspace_bytes(1, 65536, 32, 128, 128, 1) == 256 + 514 * 32 * state + 32 * 128 * state
-    assert lib.kda_bwd_workspace_bytes(4, 8192, 16, 128, 128, 4) == 256 + 256 * 16 * state + 64 * 128 * state
-    assert lib.kda_bwd_workspace_bytes(1, 9192, 32, 128, 128, 6) == 256 + 78 * 32 * state + 152 * 128 * state
+    tile = 131584
+    r256 = lambda b: (b + 255) // 256 * 256
+
+    def expect(slots, H, N):
+        # header + wide queue, forward tiles, exact flags, reversed tiles,
+        # three state checkpoints per (slot, head), then min(max(items, N H), 152)
+        # scratch buffers of 128 states
+        items = slots * H
+        ctas = min(max(items, N * H), 152)
+        return 256 + r256(items * 4) + items * tile + r256(N * H * 4) + items * tile + 3 * items * state + \
+            ctas * 128 * state
+
+    assert lib.kda_bwd_workspace_bytes(1, 65536, 32, 128, 128, 1) == expect(514, 32, 1)
+    assert lib.kda_bwd_workspace_bytes(4, 8192, 16, 128, 128, 4) == expect(256, 16, 4)
+    assert lib.kda_bwd_workspace_bytes(1, 9192, 32, 128, 128, 6) == expect(78, 32, 6)
+    assert lib.kda_bwd_workspace_bytes(1, 128, 1, 128, 128, 1) == expect(3, 1, 1)   # varlen bound T/128 + N + 1
     assert lib.kda_bwd_workspace_bytes(1, 256, 1, 64, 128, 1) == 0
     if torch.cuda.is_available():
         return
@@ -170,6 +182,7 @@ def test_bwd_workspace_and_host_checks():
     assert call(B=2, N=2, cu=p) == 1
     assert call(wsb=ws - 1) == 1
     assert call(flags=8) == 1
+    assert call(flags=4) == 1
     misaligned = ctypes.c_void_p(p.value + 8)
     assert call(dq=misaligned) == 1
     assert call(dh0=misaligned) == 1
