@@ -366,6 +366,157 @@ def run_decode(args, rank, world, local):
 
 
 # ---------------------------------------------------------------------------
+# Backward (gradients of <do, o> + <dht, ht>)
+# ---------------------------------------------------------------------------
+
+BWD_METRIC = "KDA bwd (dq, dk, dv, dg, dbeta, dh0) token*heads/s at T=64K H=32 K=V=128"
+# The per-chunk chain-rule kernel's algorithmic work per token-head: one
+# forward replay (decay, k.a, delta update: 5 flop per state entry) and the
+# per-token chain rule (18 flop per state entry), over the K x V state.
+BWD_CHUNK_FLOP_PER_TH = 23 * N128 * N128
+# FP32 CUDA-core peak: 152 SMs x 128 lanes x 2 flop per FMA at the maximum SM clock.
+FP32_LANES = 152 * 128
+
+
+def bwd_oracle_rate(w, target_s):
+    """The gradient oracle (torch fp64 autograd, as it stands) on the first
+    Ts tokens of the workload, all heads."""
+    from oracle import backward as obw
+    from chunked_gated_delta_kda_gb300.inputs import make_grad_inputs
+    Ts, dt = 4, 0.0
+    while True:
+        x = make_inputs(custom("sample", B=1, T=Ts, H=w.H, seed=w.seed))
+        gr = make_grad_inputs(custom("sample", B=1, T=Ts, H=w.H, seed=w.seed))
+        a = [x[n].float().numpy() for n in ("q", "k", "v", "g", "beta")]
+        t0 = time.perf_counter()
+        obw.kda_backward(*a, gr["do"].float().numpy(), dht=gr["dht"].numpy())
+        dt = time.perf_counter() - t0
+        # the autograd graph grows with T, so the cost is superlinear: double
+        # only while the next run is predicted to stay within the target
+        if dt * 4 > target_s or Ts >= w.T:
+            break
+        Ts = min(w.T, Ts * 2)
+    return {"value": Ts * w.H / dt, "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle",
+            "sample": f"fp64 torch autograd through the per-token recurrence on the first {Ts} tokens x {w.H} heads "
+                      f"of the {w.name} workload ({dt:.1f} s)"}
+
+
+def run_bwd(args, rank, world, local, w):
+    from chunked_gated_delta_kda_gb300 import binding
+    from chunked_gated_delta_kda_gb300.inputs import make_grad_inputs
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        cb = bwd_oracle_rate(w, target_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
+        line = {"impl": "reference", "metric": BWD_METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": 0,
+                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": w.name},
+                "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load_library()
+    x = make_inputs(w, device=str(dev), draw_on_device=True, seed_offset=rank)
+    gr = make_grad_inputs(w, device=str(dev), draw_on_device=True, seed_offset=rank)
+    B, T, H, N = w.B, w.T, w.H, w.N
+    q, k, v, g, beta, h0, cu = (x[n] for n in ("q", "k", "v", "g", "beta", "h0", "cu_seqlens"))
+    do, dht = gr["do"], gr["dht"]
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq, dk, dg = (torch.empty((B, T, H, 128), **f32) for _ in range(3))
+    dv = torch.empty((B, T, H, 128), **f32)
+    dbeta = torch.empty((B, T, H), **f32)
+    dh0 = torch.empty((N, H, 128, 128), **f32)
+    ws = torch.empty(binding.bwd_workspace_bytes(B, T, H, N), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    for six in ev:             # torch creates the CUDA event on first record
+        for e in six:
+            e.record(stream)
+
+    def step(i, timed):
+        args_ = (q, k, v, g, beta, None, h0, cu, do, dht, dq, dk, dv, dg, dbeta, dh0, N, 0, ws)
+        if timed:
+            binding.kda_bwd_timed(*args_, ev[i])
+        else:
+            binding.kda_bwd(*args_)
+
+    for i in range(args.warmup):
+        step(i, False)
+    assert binding.get_status(ws) == 0
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i, True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_end = time.time()
+    clocks.stop()
+    assert binding.get_status(ws) == 0
+    ms = max_over_ranks(e0.elapsed_time(e1), dev, world) / args.steps
+    stages = ["forward_replay", "transposed_tiles", "reverse_state_pass", "chunk_chain_rule", "rest"]
+    stage_ms = {nm: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j, nm in enumerate(stages)}
+    th = B * T * H
+    ck = clocks.summary(t_start, t_end)
+    sm_max = ck.get("sm_max_mhz") or 2070.0
+    peak = FP32_LANES * 2 * sm_max * 1e6 / 1e12
+    achieved = th * BWD_CHUNK_FLOP_PER_TH / (stage_ms["chunk_chain_rule"] * 1e-3) / 1e12
+    line = {"metric": BWD_METRIC, "value": job_rate(th, world, ms), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "T": T, "H": H, "K": 128, "V": 128,
+                       "l2_between_steps": "inputs and workspace (several GB) exceed L2; no flush"},
+            "stage_ms": stage_ms,
+            "roofline": {"kernel": "kda_bwd_chunk_kernel", "bound": "alu", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "peak_basis": f"fp32 FMA: 152 SMs x 128 lanes x 2 flop x {sm_max:.0f} MHz",
+                         "alg_flop_per_launch": th * BWD_CHUNK_FLOP_PER_TH,
+                         "ms_per_launch": stage_ms["chunk_chain_rule"]},
+            "gpu_launches": 7 * args.steps}
+    if args.e2e_steps > 0:
+        host_in = {n: t.cpu().pin_memory() for n, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta),
+                                                        ("do", do), ("dht", dht))}
+        dbuf = {n: torch.empty_like(t, device=dev) for n, t in host_in.items()}
+        outs = (dq, dk, dv, dg, dbeta, dh0)
+        host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        f0.record(stream)
+        for i in range(args.e2e_steps):
+            for n, t in host_in.items():
+                dbuf[n].copy_(t, non_blocking=True)
+            binding.kda_bwd(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], None, h0, cu, dbuf["do"],
+                            dbuf["dht"], dq, dk, dv, dg, dbeta, dh0, N, 0, ws)
+            for ho, t in zip(host_out, outs):
+                ho.copy_(t, non_blocking=True)
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        te = max_over_ranks(f0.elapsed_time(f1) / args.e2e_steps, dev, world)
+        line["e2e"] = {"value": job_rate(th, world, te), "unit": UNIT,
+                       "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in.values()),
+                       "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out), "ms_per_step": te,
+                       "note": "serial per step: inputs in, backward, gradients out, on one stream"}
+    line["clocks"] = ck
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = bwd_oracle_rate(w, target_s=min(args.cpu_seconds, 10.0))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+# ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
 
@@ -379,8 +530,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--op", choices=["fwd", "decode"], default="fwd",
-                    help="fwd: the chunked forward (default); decode: the token-by-token entry point")
+    ap.add_argument("--op", choices=["fwd", "decode", "bwd"], default="fwd",
+                    help="fwd: the chunked forward (default); decode: the token-by-token entry point; "
+                         "bwd: the chunked backward")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
@@ -389,6 +541,8 @@ def main():
 
     if args.op == "decode":
         return run_decode(args, rank, world, local)
+    if args.op == "bwd":
+        return run_bwd(args, rank, world, local, w)
     if args.impl == "reference":
         return run_reference(args, w, rank, world)
 

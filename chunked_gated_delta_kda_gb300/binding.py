@@ -73,6 +73,8 @@ def load_library(path: Optional[str] = None):
     lib.kda_bwd.restype = ctypes.c_int
     lib.kda_bwd.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                             i, i, i, i, i, i, u, vp, sz, vp]
+    lib.kda_bwd_timed.restype = ctypes.c_int
+    lib.kda_bwd_timed.argtypes = lib.kda_bwd.argtypes + [vp]
     lib.kda_status_str.restype = ctypes.c_char_p
     lib.kda_status_str.argtypes = [i]
     _lib = lib
@@ -325,6 +327,23 @@ def kda_bwd(q, k, v, g, beta, scale, h0, cu_seqlens, dout, dht, dq, dk, dv, dg, 
                      workspace.numel() * workspace.element_size(), _stream_handle(q.device))
     if rc != 0:
         raise KdaError(rc, "kda_bwd")
+
+
+def kda_bwd_timed(q, k, v, g, beta, scale, h0, cu_seqlens, dout, dht, dq, dk, dv, dg, dbeta, dh0, N: int,
+                  flags: int, workspace: torch.Tensor, events) -> None:
+    """kda_bwd that also records six torch.cuda.Event objects at its stage
+    boundaries on torch's current stream."""
+    lib = load_library()
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    ev = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    rc = lib.kda_bwd_timed(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                           float(scale if scale is not None else -1.0), _ptr(h0), _ptr(cu_seqlens), _ptr(dout),
+                           _ptr(dht), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0), B, T, H, K, V,
+                           N, flags, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                           _stream_handle(q.device), ev)
+    if rc != 0:
+        raise KdaError(rc, "kda_bwd_timed")
 
 
 def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,

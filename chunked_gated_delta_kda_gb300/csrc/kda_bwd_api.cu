@@ -73,10 +73,11 @@ size_t kda_bwd_workspace_bytes(int B, int T, int H, int K, int V, int N) {
     return (size_t)layout(B, T, H, N).total;
 }
 
-kda_status kda_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
-                   const float* h0, const int32_t* cu_seqlens, const void* dout, const float* dht, float* dq, float* dk,
-                   float* dv, float* dg, float* dbeta, float* dh0, int B, int T, int H, int K, int V, int N,
-                   unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+static kda_status bwd_impl(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
+                           const float* h0, const int32_t* cu_seqlens, const void* dout, const float* dht, float* dq,
+                           float* dk, float* dv, float* dg, float* dbeta, float* dh0, int B, int T, int H, int K,
+                           int V, int N, unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                           cudaEvent_t* ev) {
     if (K != kda::KD || V != kda::VD) return KDA_ERR_UNSUPPORTED;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return KDA_ERR_INVALID_ARG;
     if (B < 1 || T < 0 || H < 1 || N < 1 || H > 65535 || N > 65535) return KDA_ERR_INVALID_ARG;
@@ -156,26 +157,54 @@ kda_status kda_bwd(const void* q, const void* k, const void* v, const float* g, 
     p.l2norm = l2norm ? 1 : 0;
     const int ctas = scratch_ctas((long long)items, H, N);
 
+    auto mark = [&](int i) { return ev == nullptr || cudaEventRecord(ev[i], stream) == cudaSuccess; };
     if (cudaMemsetAsync(workspace, 0, kda::WS_CLEAR, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (!mark(0)) return KDA_ERR_CUDA;
     if (flags & KDA_FLAG_BWD_TOKEN_EXACT) {
         if (kda::launch_bwd_exact(p, nullptr, ctas < N * H ? ctas : N * H, stream) != cudaSuccess) return KDA_ERR_CUDA;
     } else {
         if (cudaMemsetAsync(fp.exact_flags, 0, (size_t)N * H * 4, stream) != cudaSuccess) return KDA_ERR_CUDA;
         if (fp.nslots > 0 && kda::launch_prep(fp, l2norm, stream) != cudaSuccess) return KDA_ERR_CUDA;
         if (kda::launch_scan(fp, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        if (!mark(1)) return KDA_ERR_CUDA;
         if (kda::launch_bwd_tiles(fp, ws + L.btiles, p.dout, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        if (!mark(2)) return KDA_ERR_CUDA;
         kda::FwdParams rp = fp;   // the reverse state pass
         rp.tiles = ws + L.btiles;
         rp.h0 = dht;
         rp.ht = dh0;
         rp.ckpt = reinterpret_cast<float*>(ws + L.ckpt_d);
         if (kda::launch_scan(rp, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        if (!mark(3)) return KDA_ERR_CUDA;
         if (kda::launch_bwd_chunk(p, fp, ctas, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        if (!mark(4)) return KDA_ERR_CUDA;
         if (kda::launch_bwd_exact(p, fp.exact_flags, ctas < N * H ? ctas : N * H, stream) != cudaSuccess)
             return KDA_ERR_CUDA;
     }
     if (l2norm && kda::launch_l2norm_bwd(p, (long long)B * T * H, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (!mark(5)) return KDA_ERR_CUDA;
     return KDA_OK;
+}
+
+kda_status kda_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
+                   const float* h0, const int32_t* cu_seqlens, const void* dout, const float* dht, float* dq, float* dk,
+                   float* dv, float* dg, float* dbeta, float* dh0, int B, int T, int H, int K, int V, int N,
+                   unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return bwd_impl(q, k, v, g, beta, scale, h0, cu_seqlens, dout, dht, dq, dk, dv, dg, dbeta, dh0, B, T, H, K, V, N,
+                    flags, workspace, workspace_bytes, stream, nullptr);
+}
+
+kda_status kda_bwd_timed(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
+                         const float* h0, const int32_t* cu_seqlens, const void* dout, const float* dht, float* dq,
+                         float* dk, float* dv, float* dg, float* dbeta, float* dh0, int B, int T, int H, int K, int V,
+                         int N, unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                         cudaEvent_t* stage_events) {
+    if (!stage_events) return KDA_ERR_INVALID_ARG;
+    for (int i = 0; i < 6; ++i)
+        if (!stage_events[i]) return KDA_ERR_INVALID_ARG;
+    if (flags & KDA_FLAG_BWD_TOKEN_EXACT) return KDA_ERR_INVALID_ARG;
+    return bwd_impl(q, k, v, g, beta, scale, h0, cu_seqlens, dout, dht, dq, dk, dv, dg, dbeta, dh0, B, T, H, K, V, N,
+                    flags, workspace, workspace_bytes, stream, stage_events);
 }
 
 }  // extern "C"

@@ -255,9 +255,12 @@ kda_status kda_kcp_fwd(const void* q, const void* k, const void* v, const float*
 
 /*
  * Bytes of device workspace kda_bwd needs for these sizes (0 on invalid
- * sizes).  Layout: a 256-byte status header, one fp32 K x V state per
- * (128-token chunk slot, head), then min(N H, KDA_BWD_EXACT_MAX_CTAS)
- * scratch buffers of 128 states each.
+ * sizes).  Layout: the kda_fwd workspace (status header, forward tiles,
+ * flags), a second tile per (128-token chunk slot, head) for the reverse
+ * state pass, three fp32 K x V states per (chunk slot, head) (chunk states,
+ * state gradients, and the token-by-token path's chunk states), then
+ * min(max(chunk slots x H, N x H), KDA_BWD_EXACT_MAX_CTAS) scratch buffers of
+ * 128 states.
  */
 size_t kda_bwd_workspace_bytes(int B, int T, int H, int K, int V, int N);
 
@@ -284,11 +287,19 @@ size_t kda_bwd_workspace_bytes(int B, int T, int H, int K, int V, int N);
  *   workspace   device scratch of at least kda_bwd_workspace_bytes(...)
  *               bytes, 256-byte aligned, contents need not be initialised;
  *               calls sharing it must not overlap in time
- * Method: the forward is replayed token by token in fp32 (the state entering
- * every 128-token chunk is kept in the workspace, the states inside a chunk
- * are replayed into a per-CTA scratch), and the chain rule of the token
- * rule is applied backwards, one (sequence, head) per CTA.  Exact (fp32
- * arithmetic, fp32 state) for any gate decay.
+ * Method (chunked path, the default): the forward's chunk-parallel kernel
+ * and its scan (state only) give the fp32 state entering every 128-token
+ * chunk; the state gradient obeys the same recurrence with the transposed
+ * transition, dS_c = Dg_c dS_{c+1} + Nm_c^T dS_{c+1} + Qe_c^T do_c, which the
+ * same scan evaluates on transposed tiles in reverse chunk order; then every
+ * chunk replays its tokens in fp32 from its entering state and applies the
+ * per-token chain rule backwards from its exit state gradient.  Precision:
+ * the chunk states and state gradients carry the forward's product
+ * precision (fp16 operands, fp32 accumulation), the per-token part is fp32.
+ * (sequence, head) units the forward flags as beyond its factoring range go
+ * to the token-by-token path, which replays the forward in fp32 one token at
+ * a time (exact for any decay, one unit per CTA: slow); with
+ * KDA_FLAG_BWD_TOKEN_EXACT every unit takes it.
  * Errors: as for kda_fwd; an invalid cu_seqlens is reported through
  * kda_get_status(workspace).
  */
@@ -296,6 +307,22 @@ kda_status kda_bwd(const void* q, const void* k, const void* v, const float* g, 
                    const float* h0, const int32_t* cu_seqlens, const void* dout, const float* dht, float* dq,
                    float* dk, float* dv, float* dg, float* dbeta, float* dh0, int B, int T, int H, int K, int V,
                    int N, unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * kda_bwd (chunked path), additionally recording six caller-created CUDA
+ * events on `stream`: [0] at the start, [1] after the forward replay (the
+ * chunk-parallel kernel and the state pass that stores the chunk states),
+ * [2] after the transposed tiles, [3] after the reverse state pass, [4] after
+ * the per-chunk chain-rule kernel, [5] at the end (after the token-by-token
+ * kernel for flagged units and the normalisation chain rule).  Same
+ * arguments and contract as kda_bwd; INVALID_ARG if any event is null or
+ * KDA_FLAG_BWD_TOKEN_EXACT is set.
+ */
+kda_status kda_bwd_timed(const void* q, const void* k, const void* v, const float* g, const float* beta, float scale,
+                         const float* h0, const int32_t* cu_seqlens, const void* dout, const float* dht, float* dq,
+                         float* dk, float* dv, float* dg, float* dbeta, float* dh0, int B, int T, int H, int K, int V,
+                         int N, unsigned flags, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                         cudaEvent_t* stage_events);
 
 /* Static English description of a status code. */
 const char* kda_status_str(kda_status status);
