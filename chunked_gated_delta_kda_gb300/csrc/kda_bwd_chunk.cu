@@ -158,7 +158,13 @@ constexpr int CB_RED = 3 * KD + 4;
 constexpr int CB_WIN = 16;                          // tokens between stored states
 constexpr float EXACT_WINDOW_DECAY = 7.0f;          // max sum of -g over a window before exact mode
 constexpr uint32_t CB_RED_BYTES = 2u * CB_WARPS * CB_RED * 4u;
-constexpr uint32_t CB_SMEM = CB_RED_BYTES + BT * VD * 4u;   // + residuals r[t][v]
+// Per-warp ring of token inputs, filled by cp.async CB_AHEAD tokens ahead of
+// use: q (256 B) | k (256 B) | g (512 B) | the warp's 8 v (16 B) | 8 do (16 B) | beta.
+constexpr int CB_RING = 4;
+constexpr int CB_AHEAD = 2;
+constexpr uint32_t TS_Q = 0, TS_K = 256, TS_G = 512, TS_V = 1024, TS_DO = 1040, TS_B = 1056, TS_BYTES = 1072;
+constexpr uint32_t CB_RING_BYTES = (uint32_t)CB_WARPS * CB_RING * TS_BYTES;
+constexpr uint32_t CB_SMEM = CB_RED_BYTES + BT * VD * 4u + CB_RING_BYTES;   // + residuals r[t][v] + rings
 
 struct Tok {
     float q[4], k[4], e[4], ie[4];
@@ -174,12 +180,34 @@ __device__ __forceinline__ void rows8_bf16(const uint16_t* p, float (&x)[CB_ROWS
     x[6] = __uint_as_float(u.w << 16); x[7] = __uint_as_float(u.w & 0xffff0000u);
 }
 
-__device__ __forceinline__ void tok_load(const BwdParams& p, size_t tok, int v0, int lane, Tok& in) {
-    load4_bf16(p.q + tok * KD + 4 * lane, in.q);
-    load4_bf16(p.k + tok * KD + 4 * lane, in.k);
-    const float4 gv = *reinterpret_cast<const float4*>(p.g + tok * KD + 4 * lane);
-    in.beta = p.beta[tok];
-    rows8_bf16(p.v + tok * VD + v0, in.v);
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_ahead() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(CB_AHEAD) : "memory");
+}
+
+// Copy one token's inputs into a ring slot (every lane issues its share).
+__device__ __forceinline__ void tok_fetch(const BwdParams& p, size_t tok, int v0, int lane, uint32_t slot) {
+    if (lane < 16) cp_async16(slot + TS_Q + 16u * lane, p.q + tok * KD + 8 * lane);
+    else cp_async16(slot + TS_K + 16u * (lane - 16), p.k + tok * KD + 8 * (lane - 16));
+    cp_async16(slot + TS_G + 16u * lane, p.g + tok * KD + 4 * lane);
+    if (lane == 0) cp_async16(slot + TS_V, p.v + tok * VD + v0);
+    if (lane == 1) cp_async16(slot + TS_DO, p.dout + tok * VD + v0);
+    if (lane == 2) cp_async4(slot + TS_B, p.beta + tok);
+}
+
+// A token's inputs from its ring slot (generic pointer `ts`).
+__device__ __forceinline__ void tok_load(const BwdParams& p, const uint8_t* ts, int lane, Tok& in) {
+    load4_bf16(reinterpret_cast<const uint16_t*>(ts + TS_Q) + 4 * lane, in.q);
+    load4_bf16(reinterpret_cast<const uint16_t*>(ts + TS_K) + 4 * lane, in.k);
+    const float4 gv = *reinterpret_cast<const float4*>(ts + TS_G + 16 * lane);
+    in.beta = *reinterpret_cast<const float*>(ts + TS_B);
+    rows8_bf16(reinterpret_cast<const uint16_t*>(ts + TS_V), in.v);
     float qs = p.scale, ks = 1.f;
     if (p.l2norm) {   // x / sqrt(sum x^2 + 1e-6), section "测试与验证体系"
         const float sq = warp_sum(in.q[0] * in.q[0] + in.q[1] * in.q[1] + in.q[2] * in.q[2] + in.q[3] * in.q[3]);
@@ -229,6 +257,8 @@ __global__ void __launch_bounds__(CB_THREADS, 1) kda_bwd_chunk_kernel(const BwdP
     float* red = csm;                                   // [2][CB_WARPS][CB_RED]
     float* rres = csm + CB_RED_BYTES / 4;               // [BT][VD]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* ring = reinterpret_cast<uint8_t*>(csm) + CB_RED_BYTES + BT * VD * 4u + (size_t)warp * CB_RING * TS_BYTES;
+    const uint32_t ring_s = smem_u32(ring);
     const int v0 = warp * CB_ROWS;
     const int H = p.H;
     const long long items = (long long)fp.nslots * H;
@@ -259,13 +289,32 @@ __global__ void __launch_bounds__(CB_THREADS, 1) kda_bwd_chunk_kernel(const BwdP
         }
         const int win = __syncthreads_or(big) ? 1 : CB_WIN;
 
+        // Token inputs stream through the warp's ring in the order the two
+        // phases use them: t = 0 .. rows-1, then rows-1 .. 0 (step i).
+        const int steps = 2 * rows;
+        auto fetch = [&](int i) {
+            if (i < steps) {
+                const int t = i < rows ? i : steps - 1 - i;
+                tok_fetch(p, (size_t)(c.tok0 + t) * H + h, v0, lane, ring_s + (uint32_t)(i % CB_RING) * TS_BYTES);
+            }
+            cp_async_commit();   // one group per step, empty past the end
+        };
+        auto slot_of = [&](int i) -> const uint8_t* {
+            __syncwarp();
+            fetch(i + CB_AHEAD);   // the slot it fills was last read at step i + CB_AHEAD - CB_RING < i
+            cp_async_wait_ahead();
+            __syncwarp();
+            return ring + (size_t)(i % CB_RING) * TS_BYTES;
+        };
+        for (int i = 0; i < CB_AHEAD; ++i) fetch(i);
+
         // phase A: replay the chunk forward from S_c, keeping r_t and the stored states
         float s[CB_ROWS][4];
         load_kv(p.ckpt_s + ((size_t)slot * H + h) * KD * VD, v0, lane, s);
         for (int t = 0; t < rows; ++t) {
             if (t % win == 0) put_vk(scratch + (size_t)(t / win) * VD * KD, v0, lane, s);
             Tok in;
-            tok_load(p, (size_t)(c.tok0 + t) * H + h, v0, lane, in);
+            tok_load(p, slot_of(t), lane, in);
             float dot[CB_ROWS];
 #pragma unroll
             for (int r = 0; r < CB_ROWS; ++r) {
@@ -299,9 +348,10 @@ __global__ void __launch_bounds__(CB_THREADS, 1) kda_bwd_chunk_kernel(const BwdP
         for (int t = rows - 1; t >= 0; --t) {
             const size_t tok = (size_t)(c.tok0 + t) * H + h;
             Tok in;
-            tok_load(p, tok, v0, lane, in);
+            const uint8_t* ts = slot_of(steps - 1 - t);
+            tok_load(p, ts, lane, in);
             float dov[CB_ROWS], rr[CB_ROWS], gk[CB_ROWS];
-            rows8_bf16(p.dout + tok * VD + v0, dov);
+            rows8_bf16(reinterpret_cast<const uint16_t*>(ts + TS_DO), dov);
             {
                 const float4 a = *reinterpret_cast<const float4*>(rres + (size_t)t * VD + v0);
                 const float4 b = *reinterpret_cast<const float4*>(rres + (size_t)t * VD + v0 + 4);
