@@ -478,7 +478,9 @@ def run_bwd(args, rank, world, local, w):
                        "l2_between_steps": "inputs and workspace (several GB) exceed L2; no flush"},
             "stage_ms": stage_ms,
             "roofline": {"kernel": "kda_bwd_chunk_kernel", "bound": "alu", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": (tr * th if (tr := load_traffic().get("kda_bwd_chunk_kernel")) is not None
+                                     else None),
                          "peak_basis": f"fp32 FMA: 152 SMs x 128 lanes x 2 flop x {sm_max:.0f} MHz",
                          "alg_flop_per_launch": th * BWD_CHUNK_FLOP_PER_TH,
                          "ms_per_launch": stage_ms["chunk_chain_rule"]},
