@@ -27,6 +27,7 @@ struct BwdParams {
     float* scratch;         // fp32 [ctas][BT][V][K]: states entering tokens of a chunk
     const float* ckpt_s;    // chunk kernel: fp32 [nslots][H][K][V], S entering each chunk (forward scan)
     const float* ckpt_d;    // chunk kernel: fp32 [nslots][H][K][V], dS at the end of the mirrored chunk
+    uint32_t* tc_skip;      // [nslots * H]: 1 where the tensor-core kernel left the chunk to the per-token kernel
     uint32_t* status;
     float scale;
     int T, H, N;
@@ -37,6 +38,7 @@ struct BwdParams {
 struct FwdParams;
 cudaError_t launch_bwd_tiles(const FwdParams& fp, uint8_t* btiles, const uint16_t* dout, cudaStream_t stream);
 cudaError_t launch_bwd_chunk(const BwdParams& p, const FwdParams& fp, int ctas, cudaStream_t stream);
+cudaError_t launch_bwd_tc(const BwdParams& p, const FwdParams& fp, int ctas, cudaStream_t stream);
 cudaError_t launch_bwd_exact(const BwdParams& p, const uint32_t* only, int ctas, cudaStream_t stream);
 cudaError_t launch_l2norm_bwd(const BwdParams& p, long long rows, cudaStream_t stream);
 

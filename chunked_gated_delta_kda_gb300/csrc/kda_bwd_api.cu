@@ -6,7 +6,10 @@
 //   2. the forward's scan in state-only mode, storing S entering each chunk;
 //   3. kda_bwd_tiles_kernel: Nm^T, Qe^T do, Dg at mirrored chunk positions;
 //   4. the scan again on those tiles from dht: dS at every chunk end, dh0;
-//   5. kda_bwd_chunk_kernel: per-chunk fp32 replay and chain rule;
+//   5. kda_bwd_tc_kernel: the per-chunk chain rule in chunked form on the
+//      tensor cores; kda_bwd_chunk_kernel (per-token fp32 replay) takes the
+//      chunks whose decay leaves its range (or every chunk, with
+//      KDA_FLAG_BWD_CHUNK_FP32);
 //   6. the token-by-token backward for the (sequence, head) units the
 //      forward flagged as beyond its factoring range;
 //   7. the q/k normalisation chain rule when requested.
@@ -45,7 +48,7 @@ int scratch_ctas(long long items, int H, int N) {
 }
 
 struct Layout {
-    unsigned long long tiles, flags, btiles, ckpt_s, ckpt_d, ckpt_x, scratch, total;
+    unsigned long long tiles, flags, btiles, ckpt_s, ckpt_d, ckpt_x, skip, scratch, total;
 };
 
 Layout layout(int B, int T, int H, int N) {
@@ -57,7 +60,8 @@ Layout layout(int B, int T, int H, int N) {
     L.ckpt_s = L.btiles + items * kda::TILE_BYTES;
     L.ckpt_d = L.ckpt_s + items * STATE_BYTES;
     L.ckpt_x = L.ckpt_d + items * STATE_BYTES;
-    L.scratch = L.ckpt_x + items * STATE_BYTES;
+    L.skip = L.ckpt_x + items * STATE_BYTES;
+    L.scratch = L.skip + r256(items * 4ull);
     L.total = L.scratch + (unsigned long long)scratch_ctas((long long)items, H, N) * kda::BT * STATE_BYTES;
     return L;
 }
@@ -81,7 +85,8 @@ static kda_status bwd_impl(const void* q, const void* k, const void* v, const fl
     if (K != kda::KD || V != kda::VD) return KDA_ERR_UNSUPPORTED;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return KDA_ERR_INVALID_ARG;
     if (B < 1 || T < 0 || H < 1 || N < 1 || H > 65535 || N > 65535) return KDA_ERR_INVALID_ARG;
-    if ((flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_BWD_TOKEN_EXACT)) != 0u) return KDA_ERR_INVALID_ARG;
+    if ((flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_BWD_TOKEN_EXACT | KDA_FLAG_BWD_CHUNK_FP32)) != 0u)
+        return KDA_ERR_INVALID_ARG;
     if (cu_seqlens == nullptr) {
         if (N != B || T % kda::BT != 0) return KDA_ERR_INVALID_ARG;
     } else if (B != 1) {
@@ -148,6 +153,7 @@ static kda_status bwd_impl(const void* q, const void* k, const void* v, const fl
     p.scratch = reinterpret_cast<float*>(ws + L.scratch);
     p.ckpt_s = reinterpret_cast<const float*>(ws + L.ckpt_s);
     p.ckpt_d = reinterpret_cast<const float*>(ws + L.ckpt_d);
+    p.tc_skip = nullptr;
     p.status = fp.status;
     p.scale = scale;
     p.T = T;
@@ -176,7 +182,16 @@ static kda_status bwd_impl(const void* q, const void* k, const void* v, const fl
         rp.ckpt = reinterpret_cast<float*>(ws + L.ckpt_d);
         if (kda::launch_scan(rp, stream) != cudaSuccess) return KDA_ERR_CUDA;
         if (!mark(3)) return KDA_ERR_CUDA;
-        if (kda::launch_bwd_chunk(p, fp, ctas, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        if (flags & KDA_FLAG_BWD_CHUNK_FP32) {
+            if (kda::launch_bwd_chunk(p, fp, ctas, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        } else {
+            // tensor-core chunks first; the per-token kernel takes the chunks it left
+            kda::BwdParams tp = p;
+            tp.tc_skip = reinterpret_cast<uint32_t*>(ws + L.skip);
+            if (cudaMemsetAsync(tp.tc_skip, 0, (size_t)items * 4, stream) != cudaSuccess) return KDA_ERR_CUDA;
+            if (kda::launch_bwd_tc(tp, fp, ctas, stream) != cudaSuccess) return KDA_ERR_CUDA;
+            if (kda::launch_bwd_chunk(tp, fp, ctas, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        }
         if (!mark(4)) return KDA_ERR_CUDA;
         if (kda::launch_bwd_exact(p, fp.exact_flags, ctas < N * H ? ctas : N * H, stream) != cudaSuccess)
             return KDA_ERR_CUDA;

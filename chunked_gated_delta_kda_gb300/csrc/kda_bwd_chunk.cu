@@ -269,6 +269,7 @@ __global__ void __launch_bounds__(CB_THREADS, 1) kda_bwd_chunk_kernel(const BwdP
         ChunkRef c;
         if (!slot_chunk(fp, slot, c)) continue;                    // uniform
         if (fp.exact_flags[(size_t)c.n * H + h] != 0u) continue;   // replayed by the token-by-token kernel
+        if (p.tc_skip != nullptr && p.tc_skip[it] == 0u) continue;   // done by the tensor-core kernel
         long long bos;
         int len;
         if (!seq_bounds(fp, c.n, bos, len)) continue;

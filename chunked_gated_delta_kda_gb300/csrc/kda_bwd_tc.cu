@@ -1,0 +1,643 @@
+// Chunk-parallel KDA backward on the tensor cores: the chunked form of the
+// per-token chain rule (the same gradients as kda_bwd_chunk_kernel).
+//
+// Per 128-token chunk with entering state S0 (K x V), exit state gradient Z
+// and n valid rows, with G the in-chunk inclusive prefix sum of g and a pivot
+// P = G at row min(n - 1, 64) (the pivot of the forward's chunk-parallel
+// kernel, section "算法原理" of the page "PyPTO-Gym chunk_kda operator: an NPU
+// forward of chunked gated delta-rule linear attention"):
+//   qh = scale q e^{G-P},  kh = k e^{G-P},  kc = k e^{P-G}
+//   Sp = e^{P} S0 (rows),  Ze = e^{G_last - P} Z (rows)
+//   Pm = strict_tril(kh kc^T),  Aqk = tril(qh kc^T),  Lb = I + diag(beta) Pm
+//   y0 = v - kh Sp,  rho = Lb^{-1} diag(beta) y0          (rho_t = beta_t r_t)
+// so that o = qh Sp + Aqk rho and the exit state is e^{G_last} S0 + (e^{G_last-P} kc)^T rho.
+// Differentiating those products (P cancels from the loss and is held fixed):
+//   W = tril(do rho^T),  drho = Aqk^T do + kc Ze,  dy = Lb^{-T} drho
+//   X = strict_tril(dy rho^T)
+//   dv = beta dy,  dbeta = rowsum(dy * y0) - rowsum(X * Pm)
+//   dqh = do Sp^T + W kc
+//   dkh = -diag(beta) dy Sp^T - diag(beta) X kc
+//   dkc = W^T qh + rho Ze^T - X^T diag(beta) kh
+//   dG = qh dqh + kh dkh - kc dkc, plus at the last row
+//        colsum(kc * (rho Ze^T)) + e^{G_last} rowsum(Z * S0)
+//   dg = reverse prefix sum of dG;  dq = scale dqh e^{G-P};  dk = dkh e^{G-P} + dkc e^{P-G}
+// Every product is a 128 x 128 x 128 (or triangular) one, evaluated with
+// warp-level TF32 tensor-core instructions (mma.sync m16n8k8, fp32
+// accumulation; TF32 keeps fp32's exponent range, so the pivot-factored
+// operands need no cap while the forward's factoring range holds).  The
+// inverse of the unit lower-triangular Lb is blocked: 16 x 16 diagonal blocks
+// by forward substitution, then merges 16 -> 32 -> 64 -> 128 with
+// inv([[A, 0], [C, D]]) = [[A^-1, 0], [-D^-1 C A^-1, D^-1]].
+//
+// A chunk whose factors would leave fp32's range (in-chunk decay beyond e^60
+// from the pivot row, or a pivot or exit decay below e^-60) is not computed
+// here: it is marked in tc_skip for the per-token chunk kernel, which is exact
+// for any decay.
+//
+// One CTA of 16 warps per chunk (persistent over chunks), three 128 x 132
+// fp32 shared-memory operand buffers; every product's 128 x 128 result is one
+// 32 x 32 tile per warp, held in registers until a barrier, so an epilogue
+// may overwrite the buffers the product read.  Matrices needed again later
+// live in a per-CTA global scratch (about 1 MB per CTA, mostly L2-resident).
+#include <cuda_bf16.h>
+
+#include "kda.h"
+#include "kda_bwd.cuh"
+#include "kda_common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int TC_THREADS = 512;
+constexpr int TC_WARPS = TC_THREADS / 32;
+constexpr int LD = 132;                                 // padded row length of the shared buffers
+constexpr int MAT = BT * LD;                            // floats per shared buffer
+constexpr int NVEC = 8;                                 // 128-float vectors in shared memory
+constexpr uint32_t TC_SMEM = (3u * MAT + NVEC * 128u) * 4u;
+constexpr float TC_RANGE = 60.f;                        // |exponent| bound of the factored operands
+
+// per-CTA global scratch: 128 x 128 fp32 matrices (row length 128)
+enum : int { SC_G = 0, SC_QH, SC_KH, SC_KC, SC_AQK, SC_PM, SC_LI, SC_Y0, SC_RHO, SC_W, SC_DY, SC_X,
+             SC_DQH, SC_DKH, SC_DKC, SC_COUNT };
+constexpr size_t SC_MAT = (size_t)BT * 128;
+
+// shared vectors
+enum : int { V_BETA = 0, V_PIV, V_GLAST, V_EXIT, V_DB, V_NQ, V_NK, V_TMP };
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// acc (a 32 x 32 tile at rows i0, cols j0) += opA(i0.., 0..kd) opB(0..kd, j0..) with
+// opA(i, l) = TA ? A[l][i] : A[i][l] and opB(l, j) = TB ? B[j][l] : B[l][j], shared
+// buffers of row length LD.  Fragment layouts of m16n8k8 (g = lane / 4, t = lane % 4):
+// A: (g, t) (g+8, t) (g, t+4) (g+8, t+4); B: (t, g) (t+4, g); D: (g, 2t) (g, 2t+1) (g+8, 2t) (g+8, 2t+1).
+template <bool TA, bool TB>
+__device__ __forceinline__ void tile_mm(const float* A, const float* B, int i0, int j0, int kd, int lane,
+                                        float (&acc)[2][4][4]) {
+    const int g = lane >> 2, t = lane & 3;
+    auto opA = [&](int i, int l) { return TA ? A[l * LD + i] : A[i * LD + l]; };
+    auto opB = [&](int l, int j) { return TB ? B[j * LD + l] : B[l * LD + j]; };
+#pragma unroll 2
+    for (int k0 = 0; k0 < kd; k0 += 8) {
+        uint32_t a[2][4], b[4][2];
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi) {
+            const int r = i0 + 16 * mi + g;
+            a[mi][0] = to_tf32(opA(r, k0 + t));
+            a[mi][1] = to_tf32(opA(r + 8, k0 + t));
+            a[mi][2] = to_tf32(opA(r, k0 + t + 4));
+            a[mi][3] = to_tf32(opA(r + 8, k0 + t + 4));
+        }
+#pragma unroll
+        for (int nj = 0; nj < 4; ++nj) {
+            const int c = j0 + 8 * nj + g;
+            b[nj][0] = to_tf32(opB(k0 + t, c));
+            b[nj][1] = to_tf32(opB(k0 + t + 4, c));
+        }
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+            for (int nj = 0; nj < 4; ++nj) mma_tf32(acc[mi][nj], a[mi], b[nj]);
+    }
+}
+
+__device__ __forceinline__ void zero_acc(float (&acc)[2][4][4]) {
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int nj = 0; nj < 4; ++nj) acc[mi][nj][0] = acc[mi][nj][1] = acc[mi][nj][2] = acc[mi][nj][3] = 0.f;
+}
+
+// Visit the elements of a warp's 32 x 32 tile: f(i, j, value).
+template <class F>
+__device__ __forceinline__ void tile_for(const float (&acc)[2][4][4], int i0, int j0, int lane, F f) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int nj = 0; nj < 4; ++nj) {
+            const int i = i0 + 16 * mi + g, j = j0 + 8 * nj + 2 * t;
+            f(i, j, acc[mi][nj][0]);
+            f(i, j + 1, acc[mi][nj][1]);
+            f(i + 8, j, acc[mi][nj][2]);
+            f(i + 8, j + 1, acc[mi][nj][3]);
+        }
+}
+
+// Full 128 x 128 x 128 product: warp w owns the tile at rows 32 (w / 4), cols 32 (w % 4).
+template <bool TA, bool TB>
+__device__ __forceinline__ void mm128(const float* A, const float* B, int warp, int lane, float (&acc)[2][4][4]) {
+    tile_mm<TA, TB>(A, B, 32 * (warp >> 2), 32 * (warp & 3), BT, lane, acc);
+}
+
+// global (row length 128) <-> shared (row length LD), with an optional element transform
+__device__ __forceinline__ void stage(float* dst, const float* __restrict__ src, int tid) {
+    for (int i = tid; i < BT * 32; i += TC_THREADS) {
+        const int r = i >> 5, c4 = (i & 31) * 4;
+        *reinterpret_cast<float4*>(dst + r * LD + c4) = *reinterpret_cast<const float4*>(src + r * 128 + c4);
+    }
+}
+__device__ __forceinline__ void spill(float* dst, const float* src, int tid) {
+    for (int i = tid; i < BT * 32; i += TC_THREADS) {
+        const int r = i >> 5, c4 = (i & 31) * 4;
+        *reinterpret_cast<float4*>(dst + r * 128 + c4) = *reinterpret_cast<const float4*>(src + r * LD + c4);
+    }
+}
+
+// 16 x 16 tiles for the inverse's merges: acc (m16 x n16) += opA opB over kd.
+template <bool TA, bool TB>
+__device__ __forceinline__ void tile16_mm(const float* A, const float* B, int kd, int lane, float (&acc)[2][4]) {
+    const int g = lane >> 2, t = lane & 3;
+    for (int k0 = 0; k0 < kd; k0 += 8) {
+        uint32_t a[4], b[2][2];
+        auto opA = [&](int i, int l) { return TA ? A[l * LD + i] : A[i * LD + l]; };
+        auto opB = [&](int l, int j) { return TB ? B[j * LD + l] : B[l * LD + j]; };
+        a[0] = to_tf32(opA(g, k0 + t));
+        a[1] = to_tf32(opA(g + 8, k0 + t));
+        a[2] = to_tf32(opA(g, k0 + t + 4));
+        a[3] = to_tf32(opA(g + 8, k0 + t + 4));
+#pragma unroll
+        for (int nj = 0; nj < 2; ++nj) {
+            b[nj][0] = to_tf32(opB(k0 + t, 8 * nj + g));
+            b[nj][1] = to_tf32(opB(k0 + t + 4, 8 * nj + g));
+        }
+        mma_tf32(acc[0], a, b[0]);
+        mma_tf32(acc[1], a, b[1]);
+    }
+}
+
+// In-place inverse of the unit lower-triangular 128 x 128 matrix in L (row length LD).
+// The strictly upper part must be zero on entry; it stays zero.
+__device__ void invert_unit_lower(float* L, int warp, int lane, int tid) {
+    // level 0: the eight 16 x 16 diagonal blocks, one warp each, lane j = column j
+    if (warp < 8 && lane < 16) {
+        float* blk = L + (16 * warp) * LD + 16 * warp;
+        const int j = lane;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
+#pragma unroll
+        for (int i = 1; i < 16; ++i) {
+            float s = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+                if (m < i) s = fmaf(blk[i * LD + m], x[m], s);
+            if (i > j) x[i] = -s;
+        }
+        __syncwarp(0xffffu);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (i >= j) blk[i * LD + j] = x[i];
+    }
+    __syncthreads();
+    // merges: for block size s, pairs at a = 2 p s: C = L[a+s.., a..] -> -D^-1 C A^-1
+    for (int s = 16; s < BT; s *= 2) {
+        const int pairs = BT / (2 * s);
+        const int tiles = pairs * (s / 16) * (s / 16);   // 16 x 16 output tiles over all pairs
+        // T = C A^-1 (into registers), then written over C
+        float acc[2][2][4];
+        int nt = 0;
+        for (int tI = warp; tI < tiles; tI += TC_WARPS, ++nt) {
+            const int per = (s / 16) * (s / 16);
+            const int pr = tI / per, rem = tI % per;
+            const int a = 2 * pr * s, ti = rem / (s / 16), tj = rem % (s / 16);
+            float(&c)[2][4] = acc[nt];
+            for (int u = 0; u < 2; ++u) c[u][0] = c[u][1] = c[u][2] = c[u][3] = 0.f;
+            tile16_mm<false, false>(L + (a + s + 16 * ti) * LD + a, L + a * LD + a + 16 * tj, s, lane, c);
+        }
+        __syncthreads();
+        nt = 0;
+        for (int tI = warp; tI < tiles; tI += TC_WARPS, ++nt) {
+            const int per = (s / 16) * (s / 16);
+            const int pr = tI / per, rem = tI % per;
+            const int a = 2 * pr * s, ti = rem / (s / 16), tj = rem % (s / 16);
+            const int g = lane >> 2, t = lane & 3;
+            float* dst = L + (a + s + 16 * ti) * LD + a + 16 * tj;
+            for (int u = 0; u < 2; ++u) {
+                dst[g * LD + 8 * u + 2 * t] = acc[nt][u][0];
+                dst[g * LD + 8 * u + 2 * t + 1] = acc[nt][u][1];
+                dst[(g + 8) * LD + 8 * u + 2 * t] = acc[nt][u][2];
+                dst[(g + 8) * LD + 8 * u + 2 * t + 1] = acc[nt][u][3];
+            }
+        }
+        __syncthreads();
+        // C' = -D^-1 T
+        nt = 0;
+        for (int tI = warp; tI < tiles; tI += TC_WARPS, ++nt) {
+            const int per = (s / 16) * (s / 16);
+            const int pr = tI / per, rem = tI % per;
+            const int a = 2 * pr * s, ti = rem / (s / 16), tj = rem % (s / 16);
+            float(&c)[2][4] = acc[nt];
+            for (int u = 0; u < 2; ++u) c[u][0] = c[u][1] = c[u][2] = c[u][3] = 0.f;
+            tile16_mm<false, false>(L + (a + s + 16 * ti) * LD + a + s, L + (a + s) * LD + a + 16 * tj, s, lane, c);
+        }
+        __syncthreads();
+        nt = 0;
+        for (int tI = warp; tI < tiles; tI += TC_WARPS, ++nt) {
+            const int per = (s / 16) * (s / 16);
+            const int pr = tI / per, rem = tI % per;
+            const int a = 2 * pr * s, ti = rem / (s / 16), tj = rem % (s / 16);
+            const int g = lane >> 2, t = lane & 3;
+            float* dst = L + (a + s + 16 * ti) * LD + a + 16 * tj;
+            for (int u = 0; u < 2; ++u) {
+                dst[g * LD + 8 * u + 2 * t] = -acc[nt][u][0];
+                dst[g * LD + 8 * u + 2 * t + 1] = -acc[nt][u][1];
+                dst[(g + 8) * LD + 8 * u + 2 * t] = -acc[nt][u][2];
+                dst[(g + 8) * LD + 8 * u + 2 * t + 1] = -acc[nt][u][3];
+            }
+        }
+        __syncthreads();
+    }
+    (void)tid;
+}
+
+__device__ __forceinline__ float bf16_at(const uint16_t* p, size_t i) { return __uint_as_float((uint32_t)p[i] << 16); }
+
+}  // namespace
+
+__global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdParams p, const FwdParams fp) {
+    extern __shared__ __align__(16) float tsm[];
+    float* B0 = tsm;
+    float* B1 = tsm + MAT;
+    float* B2 = tsm + 2 * MAT;
+    float* vec = tsm + 3 * MAT;
+    float* vBeta = vec + V_BETA * 128;
+    float* vPiv = vec + V_PIV * 128;
+    float* vGl = vec + V_GLAST * 128;
+    float* vExit = vec + V_EXIT * 128;
+    float* vDb = vec + V_DB * 128;
+    float* vNq = vec + V_NQ * 128;
+    float* vNk = vec + V_NK * 128;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = p.H;
+    const long long items = (long long)fp.nslots * H;
+    float* sc = p.scratch + (size_t)blockIdx.x * BT * VD * KD;
+    auto S = [&](int m) { return sc + (size_t)m * SC_MAT; };
+    const int ti0 = 32 * (warp >> 2), tj0 = 32 * (warp & 3);   // this warp's output tile
+    const float scale = p.scale;
+
+    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+        const int slot = (int)(it / H), h = (int)(it % H);
+        ChunkRef c;
+        if (!slot_chunk(fp, slot, c)) continue;                    // uniform
+        if (fp.exact_flags[(size_t)c.n * H + h] != 0u) continue;   // replayed by the token-by-token kernel
+        long long bos;
+        int len;
+        if (!seq_bounds(fp, c.n, bos, len)) continue;
+        const int nch = (len + BT - 1) / BT;
+        const int n = c.len;
+        const int piv = n - 1 < 64 ? n - 1 : 64;
+        const size_t row0 = (size_t)c.tok0 * H + h;                // (token, head) row of the chunk's first token
+        const size_t rs = (size_t)H;                               // rows between tokens
+        const float* S0 = p.ckpt_s + ((size_t)slot * H + h) * KD * VD;
+        const float* Z = p.ckpt_d + ((size_t)chunk_slot(fp, c.n, nch - 1 - c.j) * H + h) * KD * VD;
+        __syncthreads();   // the previous chunk's last reads of the shared buffers are done
+
+        // ---- gate prefix sums G (B0), beta, q/k row norms -------------------------------
+        for (int i = tid; i < BT * 32; i += TC_THREADS) {
+            const int r = i >> 5, c4 = (i & 31) * 4;
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < n) x = *reinterpret_cast<const float4*>(p.g + (row0 + r * rs) * KD + c4);
+            *reinterpret_cast<float4*>(B0 + r * LD + c4) = x;
+        }
+        if (tid < BT) vBeta[tid] = tid < n ? p.beta[row0 + tid * rs] : 0.f;
+        if (p.l2norm) {   // per-row inverse norms 1 / sqrt(sum x^2 + 1e-6), section "测试与验证体系"
+            for (int r = warp; r < BT; r += TC_WARPS) {
+                float sq = 0.f, sk = 0.f;
+                if (r < n) {
+                    float xq[4], xk[4];
+                    load4_bf16(p.q + (row0 + r * rs) * KD + 4 * lane, xq);
+                    load4_bf16(p.k + (row0 + r * rs) * KD + 4 * lane, xk);
+                    sq = xq[0] * xq[0] + xq[1] * xq[1] + xq[2] * xq[2] + xq[3] * xq[3];
+                    sk = xk[0] * xk[0] + xk[1] * xk[1] + xk[2] * xk[2] + xk[3] * xk[3];
+                }
+                sq = warp_sum(sq);
+                sk = warp_sum(sk);
+                if (lane == 0) {
+                    vNq[r] = rsqrtf(sq + 1e-6f);
+                    vNk[r] = rsqrtf(sk + 1e-6f);
+                }
+            }
+        } else if (tid < BT) {
+            vNq[tid] = 1.f;
+            vNk[tid] = 1.f;
+        }
+        __syncthreads();
+        if (tid < KD) {   // column prefix sums; rows past n hold G_last
+            float acc = 0.f;
+            for (int r = 0; r < BT; ++r) {
+                if (r < n) acc += B0[r * LD + tid];
+                B0[r * LD + tid] = acc;
+            }
+            vPiv[tid] = B0[piv * LD + tid];
+            vGl[tid] = acc;
+            vExit[tid] = 0.f;
+        }
+        if (tid >= KD && tid < 2 * KD) vDb[tid - KD] = 0.f;
+        __syncthreads();
+        // Range guard: the factors e^{+-(G-P)}, e^{P} and e^{G_last-P} must stay well
+        // inside fp32; a chunk beyond that is left to the per-token kernel.
+        bool wide = false;
+        for (int i = tid; i < n * KD; i += TC_THREADS) {
+            const int r = i >> 7, d = i & 127;
+            const float x = B0[r * LD + d] - vPiv[d];
+            wide = wide || !(fabsf(x) <= TC_RANGE);
+        }
+        if (tid < KD) wide = wide || !(vPiv[tid] >= -TC_RANGE) || !(vGl[tid] - vPiv[tid] >= -TC_RANGE);
+        if (__syncthreads_or(wide)) {
+            if (tid == 0) p.tc_skip[it] = 1u;
+            continue;
+        }
+        spill(S(SC_G), B0, tid);
+
+        // ---- gated operands: B0 = qh, B1 = kh, B2 = kc -----------------------------------
+        for (int i = tid; i < BT * KD; i += TC_THREADS) {
+            const int r = i >> 7, d = i & 127;
+            float qv = 0.f, kv = 0.f;
+            if (r < n) {
+                qv = bf16_at(p.q, (row0 + r * rs) * KD + d) * vNq[r] * scale;
+                kv = bf16_at(p.k, (row0 + r * rs) * KD + d) * vNk[r];
+            }
+            const float e = B0[r * LD + d] - vPiv[d];
+            const float ep = __expf(e), em = __expf(-e);
+            B1[r * LD + d] = kv * ep;
+            B2[r * LD + d] = kv * em;
+            B0[r * LD + d] = qv * ep;
+        }
+        __syncthreads();
+        spill(S(SC_QH), B0, tid);
+        spill(S(SC_KH), B1, tid);
+        spill(S(SC_KC), B2, tid);
+
+        float acc[2][4][4];
+        // ---- Aqk = tril(qh kc^T) -----------------------------------------------------------
+        zero_acc(acc);
+        mm128<false, true>(B0, B2, warp, lane, acc);
+        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) { S(SC_AQK)[i * 128 + j] = (j <= i) ? x : 0.f; });
+        // ---- Pm = strict_tril(kh kc^T); B0 = Lb = I + diag(beta) Pm ------------------------
+        zero_acc(acc);
+        mm128<false, true>(B1, B2, warp, lane, acc);
+        __syncthreads();
+        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) {
+            const float pm = (j < i) ? x : 0.f;
+            S(SC_PM)[i * 128 + j] = pm;
+            B0[i * LD + j] = (i == j) ? 1.f : vBeta[i] * pm;
+        });
+        __syncthreads();
+        invert_unit_lower(B0, warp, lane, tid);   // B0 = Li
+        spill(S(SC_LI), B0, tid);
+        // ---- B2 = Sp = e^P S0 (rows) ---------------------------------------------------------
+        for (int i = tid; i < KD * 32; i += TC_THREADS) {
+            const int r = i >> 5, c4 = (i & 31) * 4;
+            float4 x = *reinterpret_cast<const float4*>(S0 + r * VD + c4);
+            const float e = __expf(vPiv[r]);
+            x.x *= e; x.y *= e; x.z *= e; x.w *= e;
+            *reinterpret_cast<float4*>(B2 + r * LD + c4) = x;
+        }
+        __syncthreads();
+        // ---- y0 = v - kh Sp; B1 = y = beta y0 ----------------------------------------------
+        zero_acc(acc);
+        mm128<false, false>(B1, B2, warp, lane, acc);
+        __syncthreads();
+        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) {
+            const float vv = i < n ? bf16_at(p.v, (row0 + i * rs) * VD + j) : 0.f;
+            const float y0 = vv - x;
+            S(SC_Y0)[i * 128 + j] = y0;
+            B1[i * LD + j] = vBeta[i] * y0;
+        });
+        __syncthreads();
+        // ---- rho = Li y; B1 = rho ------------------------------------------------------------
+        zero_acc(acc);
+        mm128<false, false>(B0, B1, warp, lane, acc);
+        __syncthreads();
+        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) {
+            S(SC_RHO)[i * 128 + j] = x;
+            B1[i * LD + j] = x;
+        });
+        // ---- B0 = do; W = tril(do rho^T) ---------------------------------------------------
+        for (int i = tid; i < BT * VD; i += TC_THREADS) {
+            const int r = i >> 7, d = i & 127;
+            B0[r * LD + d] = r < n ? bf16_at(p.dout, (row0 + r * rs) * VD + d) : 0.f;
+        }
+        __syncthreads();
+        zero_acc(acc);
+        mm128<false, true>(B0, B1, warp, lane, acc);
+        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) { S(SC_W)[i * 128 + j] = (j <= i) ? x : 0.f; });
+        __syncthreads();
+        // ---- drho = Aqk^T do + kc Ze --------------------------------------------------------
+        stage(B1, S(SC_AQK), tid);
+        __syncthreads();
+        zero_acc(acc);
+        mm128<true, false>(B1, B0, warp, lane, acc);
+        __syncthreads();
+        stage(B1, S(SC_KC), tid);
+        {
+            for (int i = tid; i < KD * 32; i += TC_THREADS) {   // B2 = Ze = e^{G_last - P} Z (rows)
+                const int r = i >> 5, c4 = (i & 31) * 4;
+                float4 x = *reinterpret_cast<const float4*>(Z + r * VD + c4);
+                const float e = __expf(vGl[r] - vPiv[r]);
+                x.x *= e; x.y *= e; x.z *= e; x.w *= e;
+                *reinterpret_cast<float4*>(B2 + r * LD + c4) = x;
+            }
+        }
+        __syncthreads();
+        mm128<false, false>(B1, B2, warp, lane, acc);
+        __syncthreads();
+        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) { B1[i * LD + j] = x; });   // B1 = drho
+        stage(B0, S(SC_LI), tid);
+        __syncthreads();
+        // ---- dy = Li^T drho; dv = beta dy; dbeta += rowsum(dy y0) --------------------------
+        zero_acc(acc);
+        mm128<true, false>(B0, B1, warp, lane, acc);
+        __syncthreads();
+        {
+            float rsum[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+            tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) {
+                S(SC_DY)[i * 128 + j] = x;
+                B1[i * LD + j] = x;
+                if (i < n) p.dv[(row0 + i * rs) * VD + j] = vBeta[i] * x;
+                const int mi = (i - ti0) >> 4, hi = ((i - ti0) >> 3) & 1;
+                rsum[mi][hi] = fmaf(x, S(SC_Y0)[i * 128 + j], rsum[mi][hi]);
+            });
+            // reduce over the 4 lanes sharing a row, then across the row band's warps
+#pragma unroll
+            for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+                for (int hi = 0; hi < 2; ++hi) {
+                    float v = rsum[mi][hi];
+                    v += __shfl_xor_sync(0xffffffffu, v, 1);
+                    v += __shfl_xor_sync(0xffffffffu, v, 2);
+                    if ((lane & 3) == 0) atomicAdd(&vDb[ti0 + 16 * mi + 8 * hi + (lane >> 2)], v);
+                }
+        }
+        stage(B0, S(SC_RHO), tid);
+        __syncthreads();
+        // ---- X = strict_tril(dy rho^T); dbeta -= rowsum(X Pm) ------------------------------
+        zero_acc(acc);
+        mm128<false, true>(B1, B0, warp, lane, acc);
+        {
+            float rsum[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+            tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) {
+                const float xs = (j < i) ? x : 0.f;
+                S(SC_X)[i * 128 + j] = xs;
+                const int mi = (i - ti0) >> 4, hi = ((i - ti0) >> 3) & 1;
+                rsum[mi][hi] = fmaf(-xs, S(SC_PM)[i * 128 + j], rsum[mi][hi]);
+            });
+#pragma unroll
+            for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+                for (int hi = 0; hi < 2; ++hi) {
+                    float v = rsum[mi][hi];
+                    v += __shfl_xor_sync(0xffffffffu, v, 1);
+                    v += __shfl_xor_sync(0xffffffffu, v, 2);
+                    if ((lane & 3) == 0) atomicAdd(&vDb[ti0 + 16 * mi + 8 * hi + (lane >> 2)], v);
+                }
+        }
+        // ---- dkc = rho Ze^T (+ later terms); exit term colsum(kc * rho Ze^T) ---------------
+        zero_acc(acc);
+        mm128<false, true>(B0, B2, warp, lane, acc);
+        {
+            float csum[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+            tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) {
+                S(SC_DKC)[i * 128 + j] = x;
+                const int nj = (j - tj0) >> 3, lo = (j - tj0) & 1;
+                csum[nj][lo] = fmaf(S(SC_KC)[i * 128 + j], x, csum[nj][lo]);
+            });
+            // reduce over the 8 lanes sharing a column (lane / 4), then across warps
+#pragma unroll
+            for (int nj = 0; nj < 4; ++nj)
+#pragma unroll
+                for (int lo = 0; lo < 2; ++lo) {
+                    float v = csum[nj][lo];
+                    v += __shfl_xor_sync(0xffffffffu, v, 4);
+                    v += __shfl_xor_sync(0xffffffffu, v, 8);
+                    v += __shfl_xor_sync(0xffffffffu, v, 16);
+                    if (lane < 4) atomicAdd(&vExit[tj0 + 8 * nj + 2 * lane + lo], v);
+                }
+        }
+        __syncthreads();
+        // ---- B0 = Sp; dkh = -diag(beta) dy Sp^T -------------------------------------------
+        for (int i = tid; i < KD * 32; i += TC_THREADS) {
+            const int r = i >> 5, c4 = (i & 31) * 4;
+            float4 x = *reinterpret_cast<const float4*>(S0 + r * VD + c4);
+            const float e = __expf(vPiv[r]);
+            x.x *= e; x.y *= e; x.z *= e; x.w *= e;
+            *reinterpret_cast<float4*>(B0 + r * LD + c4) = x;
+        }
+        __syncthreads();
+        zero_acc(acc);
+        mm128<false, true>(B1, B0, warp, lane, acc);
+        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) { S(SC_DKH)[i * 128 + j] = -vBeta[i] * x; });
+        __syncthreads();
+        // ---- B1 = do; dqh = do Sp^T ----------------------------------------------------------
+        for (int i = tid; i < BT * VD; i += TC_THREADS) {
+            const int r = i >> 7, d = i & 127;
+            B1[r * LD + d] = r < n ? bf16_at(p.dout, (row0 + r * rs) * VD + d) : 0.f;
+        }
+        __syncthreads();
+        zero_acc(acc);
+        mm128<false, true>(B1, B0, warp, lane, acc);
+        __syncthreads();
+        // ---- B0 = W, B2 = kc: dqh += W kc ------------------------------------------------
+        stage(B0, S(SC_W), tid);
+        stage(B2, S(SC_KC), tid);
+        __syncthreads();
+        mm128<false, false>(B0, B2, warp, lane, acc);
+        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) { S(SC_DQH)[i * 128 + j] = x; });
+        // ---- B1 = X: dkh -= diag(beta) X kc ---------------------------------------------
+        __syncthreads();
+        stage(B1, S(SC_X), tid);
+        __syncthreads();
+        zero_acc(acc);
+        mm128<false, false>(B1, B2, warp, lane, acc);
+        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) { S(SC_DKH)[i * 128 + j] -= vBeta[i] * x; });
+        // ---- B2 = qh: dkc += W^T qh ------------------------------------------------------
+        __syncthreads();
+        stage(B2, S(SC_QH), tid);
+        __syncthreads();
+        zero_acc(acc);
+        mm128<true, false>(B0, B2, warp, lane, acc);
+        __syncthreads();
+        // ---- B0 = diag(beta) kh: dkc -= X^T (beta kh) ------------------------------------
+        for (int i = tid; i < BT * 32; i += TC_THREADS) {
+            const int r = i >> 5, c4 = (i & 31) * 4;
+            float4 x = *reinterpret_cast<const float4*>(S(SC_KH) + r * 128 + c4);
+            const float b = vBeta[r];
+            x.x *= b; x.y *= b; x.z *= b; x.w *= b;
+            *reinterpret_cast<float4*>(B0 + r * LD + c4) = x;
+        }
+        __syncthreads();
+        {
+            float acc2[2][4][4];
+            zero_acc(acc2);
+            mm128<true, false>(B1, B0, warp, lane, acc2);
+#pragma unroll
+            for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+                for (int nj = 0; nj < 4; ++nj)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) acc[mi][nj][u] -= acc2[mi][nj][u];
+        }
+        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) { S(SC_DKC)[i * 128 + j] += x; });
+        __syncthreads();
+
+        // ---- dG into B0; exit terms at the last row; reverse prefix sum; outputs -------------
+        if (tid < KD) {   // e^{G_last} rowsum(Z * S0) for row d = tid of the states
+            float s = 0.f;
+            for (int v4 = 0; v4 < VD; v4 += 4) {
+                const float4 a = *reinterpret_cast<const float4*>(Z + tid * VD + v4);
+                const float4 b = *reinterpret_cast<const float4*>(S0 + tid * VD + v4);
+                s = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, s))));
+            }
+            vExit[tid] += __expf(vGl[tid]) * s;
+        }
+        for (int i = tid; i < BT * KD; i += TC_THREADS) {
+            const int r = i >> 7, d = i & 127;
+            const size_t e = (size_t)r * 128 + d;
+            B0[r * LD + d] = S(SC_QH)[e] * S(SC_DQH)[e] + S(SC_KH)[e] * S(SC_DKH)[e] - S(SC_KC)[e] * S(SC_DKC)[e];
+        }
+        __syncthreads();
+        if (tid < KD) {   // dg = reverse prefix sum over the valid rows, the exit terms at row n - 1
+            float acc1 = vExit[tid];
+            for (int r = n - 1; r >= 0; --r) {
+                acc1 += B0[r * LD + tid];
+                B0[r * LD + tid] = acc1;
+            }
+        }
+        if (tid >= KD && tid < KD + BT && tid - KD < n) p.dbeta[row0 + (tid - KD) * rs] = vDb[tid - KD];
+        __syncthreads();
+        for (int i = tid; i < n * KD; i += TC_THREADS) {
+            const int r = i >> 7, d = i & 127;
+            const size_t e = (size_t)r * 128 + d;
+            const float x = S(SC_G)[e] - vPiv[d];
+            const float ep = __expf(x), em = __expf(-x);
+            const size_t o = (row0 + r * rs) * KD + d;
+            p.dq[o] = scale * S(SC_DQH)[e] * ep;              // with the q/k norm: w.r.t. the normalised q, k
+            p.dk[o] = S(SC_DKH)[e] * ep + S(SC_DKC)[e] * em;
+            p.dg[o] = B0[r * LD + d];
+        }
+    }
+}
+
+cudaError_t launch_bwd_tc(const BwdParams& p, const FwdParams& fp, int ctas, cudaStream_t stream) {
+    if (fp.nslots == 0 || ctas == 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kda_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    if (e != cudaSuccess) return e;
+    kda_bwd_tc_kernel<<<ctas, TC_THREADS, TC_SMEM, stream>>>(p, fp);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -60,6 +60,10 @@ typedef enum {
  * instead of the chunked one (fp32 throughout; slower). */
 #define KDA_FLAG_BWD_TOKEN_EXACT 2u
 
+/* kda_bwd only: evaluate every chunk's chain rule token by token in fp32 on
+ * the CUDA cores instead of in chunked form on the tensor cores. */
+#define KDA_FLAG_BWD_CHUNK_FP32 4u
+
 /*
  * Bytes of device workspace kda_fwd needs for these sizes (an upper bound
  * that covers both fixed-length and varlen packing).  0 on invalid sizes.
@@ -258,7 +262,8 @@ kda_status kda_kcp_fwd(const void* q, const void* k, const void* v, const float*
  * sizes).  Layout: the kda_fwd workspace (status header, forward tiles,
  * flags), a second tile per (128-token chunk slot, head) for the reverse
  * state pass, three fp32 K x V states per (chunk slot, head) (chunk states,
- * state gradients, and the token-by-token path's chunk states), then
+ * state gradients, and the token-by-token path's chunk states), one word
+ * per (chunk slot, head) marking chunks left to the per-token kernel, then
  * min(max(chunk slots x H, N x H), KDA_BWD_EXACT_MAX_CTAS) scratch buffers of
  * 128 states.
  */

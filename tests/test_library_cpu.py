@@ -147,12 +147,12 @@ def test_bwd_workspace_and_host_checks():
 
     def expect(slots, H, N):
         # header + wide queue, forward tiles, exact flags, reversed tiles,
-        # three state checkpoints per (slot, head), then min(max(items, N H), 152)
-        # scratch buffers of 128 states
+        # three state checkpoints per (slot, head), one skip word per item, then
+        # min(max(items, N H), 152) scratch buffers of 128 states
         items = slots * H
         ctas = min(max(items, N * H), 152)
         return 256 + r256(items * 4) + items * tile + r256(N * H * 4) + items * tile + 3 * items * state + \
-            ctas * 128 * state
+            r256(items * 4) + ctas * 128 * state
 
     assert lib.kda_bwd_workspace_bytes(1, 65536, 32, 128, 128, 1) == expect(514, 32, 1)
     assert lib.kda_bwd_workspace_bytes(4, 8192, 16, 128, 128, 4) == expect(256, 16, 4)
@@ -182,7 +182,7 @@ def test_bwd_workspace_and_host_checks():
     assert call(B=2, N=2, cu=p) == 1
     assert call(wsb=ws - 1) == 1
     assert call(flags=8) == 1
-    assert call(flags=4) == 1
+    assert call(flags=16) == 1
     misaligned = ctypes.c_void_p(p.value + 8)
     assert call(dq=misaligned) == 1
     assert call(dh0=misaligned) == 1
