@@ -54,13 +54,16 @@ constexpr int TC_THREADS = 512;
 constexpr int TC_WARPS = TC_THREADS / 32;
 constexpr int LD = 132;                                 // padded row length of the shared buffers
 constexpr int MAT = BT * LD;                            // floats per shared buffer
-constexpr int NVEC = 8;                                 // 128-float vectors in shared memory
+constexpr int NVEC = 9;                                 // 128-float vectors in shared memory (+ the TMEM address)
 constexpr uint32_t TC_SMEM = (3u * MAT + NVEC * 128u) * 4u;
 constexpr float TC_RANGE = 60.f;                        // |exponent| bound of the factored operands
 
 // per-CTA global scratch: 128 x 128 fp32 matrices (row length 128)
-enum : int { SC_G = 0, SC_QH, SC_KH, SC_KC, SC_AQK, SC_PM, SC_LI, SC_Y0, SC_RHO, SC_W, SC_DY, SC_X,
-             SC_DQH, SC_DKH, SC_DKC, SC_COUNT };
+enum : int { SC_QH = 0, SC_KH, SC_KC, SC_AQK, SC_PM, SC_LI, SC_Y0, SC_RHO, SC_W, SC_X, SC_COUNT };
+// TMEM columns (each a 128-column block): matrices a warp keeps in its own
+// fragment order (32 values per thread, lane 32 (warp % 4) + lane, columns
+// 32 (warp / 4) .. + 31 of the block) instead of round-tripping global memory
+constexpr uint32_t TM_G = 0, TM_DQH = 128, TM_DKH = 256, TM_DKC = 384, TM_COLS = 512;
 constexpr size_t SC_MAT = (size_t)BT * 128;
 
 // shared vectors
@@ -114,6 +117,10 @@ __device__ __forceinline__ void tile_mm(const float* A, const float* B, int i0, 
     }
 }
 
+__device__ __forceinline__ float (&flat(float (&acc)[2][4][4]))[32] {
+    return *reinterpret_cast<float(*)[32]>(&acc[0][0][0]);
+}
+
 __device__ __forceinline__ void zero_acc(float (&acc)[2][4][4]) {
 #pragma unroll
     for (int mi = 0; mi < 2; ++mi)
@@ -145,12 +152,14 @@ __device__ __forceinline__ void mm128(const float* A, const float* B, int warp, 
 
 // global (row length 128) <-> shared (row length LD), with an optional element transform
 __device__ __forceinline__ void stage(float* dst, const float* __restrict__ src, int tid) {
+#pragma unroll
     for (int i = tid; i < BT * 32; i += TC_THREADS) {
         const int r = i >> 5, c4 = (i & 31) * 4;
         *reinterpret_cast<float4*>(dst + r * LD + c4) = *reinterpret_cast<const float4*>(src + r * 128 + c4);
     }
 }
 __device__ __forceinline__ void spill(float* dst, const float* src, int tid) {
+#pragma unroll
     for (int i = tid; i < BT * 32; i += TC_THREADS) {
         const int r = i >> 5, c4 = (i & 31) * 4;
         *reinterpret_cast<float4*>(dst + r * 128 + c4) = *reinterpret_cast<const float4*>(src + r * LD + c4);
@@ -266,6 +275,40 @@ __device__ void invert_unit_lower(float* L, int warp, int lane, int tid) {
 
 __device__ __forceinline__ float bf16_at(const uint16_t* p, size_t i) { return __uint_as_float((uint32_t)p[i] << 16); }
 
+__device__ __forceinline__ void bf16x8(const uint4 u, float (&x)[8]) {
+    x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
+    x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xffff0000u);
+    x[4] = __uint_as_float(u.z << 16); x[5] = __uint_as_float(u.z & 0xffff0000u);
+    x[6] = __uint_as_float(u.w << 16); x[7] = __uint_as_float(u.w & 0xffff0000u);
+}
+
+// dst (shared) = the chunk's bf16 rows of src (token-major, rows row0 + r rs), zero past n
+__device__ __forceinline__ void stage_rows_bf16(float* dst, const uint16_t* __restrict__ src, size_t row0, size_t rs,
+                                                int n, int tid) {
+#pragma unroll
+    for (int i = tid; i < BT * 16; i += TC_THREADS) {
+        const int r = i >> 4, c8 = (i & 15) * 8;
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (r < n) u = *reinterpret_cast<const uint4*>(src + (row0 + r * rs) * 128 + c8);
+        float x[8];
+        bf16x8(u, x);
+        *reinterpret_cast<float4*>(dst + r * LD + c8) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(dst + r * LD + c8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
+    }
+}
+
+// dst (shared) = diag(exp(e[r])) src (a [K][V] fp32 state)
+__device__ __forceinline__ void stage_state_scaled(float* dst, const float* __restrict__ src, const float* e, int tid) {
+#pragma unroll
+    for (int i = tid; i < KD * 32; i += TC_THREADS) {
+        const int r = i >> 5, c4 = (i & 31) * 4;
+        float4 x = *reinterpret_cast<const float4*>(src + r * VD + c4);
+        const float f = __expf(e[r]);
+        x.x *= f; x.y *= f; x.z *= f; x.w *= f;
+        *reinterpret_cast<float4*>(dst + r * LD + c4) = x;
+    }
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdParams p, const FwdParams fp) {
@@ -281,6 +324,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
     float* vDb = vec + V_DB * 128;
     float* vNq = vec + V_NQ * 128;
     float* vNk = vec + V_NK * 128;
+    float* vTmp = vec + V_TMP * 128;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.H;
     const long long items = (long long)fp.nslots * H;
@@ -288,6 +332,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
     auto S = [&](int m) { return sc + (size_t)m * SC_MAT; };
     const int ti0 = 32 * (warp >> 2), tj0 = 32 * (warp & 3);   // this warp's output tile
     const float scale = p.scale;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(vec + 8 * 128);
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tslot), TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tslot);
+    // this thread's private 32 columns of each TMEM block
+    const uint32_t tme = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32u * (uint32_t)(warp >> 2);
+    auto tm_put = [&](uint32_t blk, float (&acc)[2][4][4]) {
+        tmem_st32(tme + blk, flat(acc));
+        tmem_st_wait();
+    };
+    auto tm_get = [&](uint32_t blk, float (&acc)[2][4][4]) {
+        tmem_ld32(tme + blk, flat(acc));
+        tmem_ld_wait();
+    };
 
     for (long long it = blockIdx.x; it < items; it += gridDim.x) {
         const int slot = (int)(it / H), h = (int)(it % H);
@@ -307,6 +370,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         __syncthreads();   // the previous chunk's last reads of the shared buffers are done
 
         // ---- gate prefix sums G (B0), beta, q/k row norms -------------------------------
+#pragma unroll
         for (int i = tid; i < BT * 32; i += TC_THREADS) {
             const int r = i >> 5, c4 = (i & 31) * 4;
             float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -344,6 +408,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
             }
             vPiv[tid] = B0[piv * LD + tid];
             vGl[tid] = acc;
+            vTmp[tid] = acc - vPiv[tid];
             vExit[tid] = 0.f;
         }
         if (tid >= KD && tid < 2 * KD) vDb[tid - KD] = 0.f;
@@ -361,21 +426,44 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
             if (tid == 0) p.tc_skip[it] = 1u;
             continue;
         }
-        spill(S(SC_G), B0, tid);
+        {   // G at this warp's fragment positions -> TMEM
+            float gf[2][4][4];
+            const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+            for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+                for (int nj = 0; nj < 4; ++nj) {
+                    const int i = ti0 + 16 * mi + g, j = tj0 + 8 * nj + 2 * t;
+                    gf[mi][nj][0] = B0[i * LD + j];
+                    gf[mi][nj][1] = B0[i * LD + j + 1];
+                    gf[mi][nj][2] = B0[(i + 8) * LD + j];
+                    gf[mi][nj][3] = B0[(i + 8) * LD + j + 1];
+                }
+            tm_put(TM_G, gf);
+        }
 
         // ---- gated operands: B0 = qh, B1 = kh, B2 = kc -----------------------------------
-        for (int i = tid; i < BT * KD; i += TC_THREADS) {
-            const int r = i >> 7, d = i & 127;
-            float qv = 0.f, kv = 0.f;
+#pragma unroll 2
+        for (int i = tid; i < BT * 16; i += TC_THREADS) {
+            const int r = i >> 4, c8 = (i & 15) * 8;
+            uint4 uq = make_uint4(0u, 0u, 0u, 0u), uk = uq;
             if (r < n) {
-                qv = bf16_at(p.q, (row0 + r * rs) * KD + d) * vNq[r] * scale;
-                kv = bf16_at(p.k, (row0 + r * rs) * KD + d) * vNk[r];
+                uq = *reinterpret_cast<const uint4*>(p.q + (row0 + r * rs) * KD + c8);
+                uk = *reinterpret_cast<const uint4*>(p.k + (row0 + r * rs) * KD + c8);
             }
-            const float e = B0[r * LD + d] - vPiv[d];
-            const float ep = __expf(e), em = __expf(-e);
-            B1[r * LD + d] = kv * ep;
-            B2[r * LD + d] = kv * em;
-            B0[r * LD + d] = qv * ep;
+            float xq[8], xk[8];
+            bf16x8(uq, xq);
+            bf16x8(uk, xk);
+            const float sq = vNq[r] * scale, sk = vNk[r];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int d = c8 + u;
+                const float e = B0[r * LD + d] - vPiv[d];
+                const float ep = __expf(e), em = __expf(-e);
+                B1[r * LD + d] = xk[u] * sk * ep;
+                B2[r * LD + d] = xk[u] * sk * em;
+                B0[r * LD + d] = xq[u] * sq * ep;
+            }
         }
         __syncthreads();
         spill(S(SC_QH), B0, tid);
@@ -400,13 +488,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         invert_unit_lower(B0, warp, lane, tid);   // B0 = Li
         spill(S(SC_LI), B0, tid);
         // ---- B2 = Sp = e^P S0 (rows) ---------------------------------------------------------
-        for (int i = tid; i < KD * 32; i += TC_THREADS) {
-            const int r = i >> 5, c4 = (i & 31) * 4;
-            float4 x = *reinterpret_cast<const float4*>(S0 + r * VD + c4);
-            const float e = __expf(vPiv[r]);
-            x.x *= e; x.y *= e; x.z *= e; x.w *= e;
-            *reinterpret_cast<float4*>(B2 + r * LD + c4) = x;
-        }
+        stage_state_scaled(B2, S0, vPiv, tid);
         __syncthreads();
         // ---- y0 = v - kh Sp; B1 = y = beta y0 ----------------------------------------------
         zero_acc(acc);
@@ -428,10 +510,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
             B1[i * LD + j] = x;
         });
         // ---- B0 = do; W = tril(do rho^T) ---------------------------------------------------
-        for (int i = tid; i < BT * VD; i += TC_THREADS) {
-            const int r = i >> 7, d = i & 127;
-            B0[r * LD + d] = r < n ? bf16_at(p.dout, (row0 + r * rs) * VD + d) : 0.f;
-        }
+        stage_rows_bf16(B0, p.dout, row0, rs, n, tid);
         __syncthreads();
         zero_acc(acc);
         mm128<false, true>(B0, B1, warp, lane, acc);
@@ -444,15 +523,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         mm128<true, false>(B1, B0, warp, lane, acc);
         __syncthreads();
         stage(B1, S(SC_KC), tid);
-        {
-            for (int i = tid; i < KD * 32; i += TC_THREADS) {   // B2 = Ze = e^{G_last - P} Z (rows)
-                const int r = i >> 5, c4 = (i & 31) * 4;
-                float4 x = *reinterpret_cast<const float4*>(Z + r * VD + c4);
-                const float e = __expf(vGl[r] - vPiv[r]);
-                x.x *= e; x.y *= e; x.z *= e; x.w *= e;
-                *reinterpret_cast<float4*>(B2 + r * LD + c4) = x;
-            }
-        }
+        stage_state_scaled(B2, Z, vTmp, tid);   // B2 = Ze = e^{G_last - P} Z (rows)
         __syncthreads();
         mm128<false, false>(B1, B2, warp, lane, acc);
         __syncthreads();
@@ -466,7 +537,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         {
             float rsum[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
             tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) {
-                S(SC_DY)[i * 128 + j] = x;
                 B1[i * LD + j] = x;
                 if (i < n) p.dv[(row0 + i * rs) * VD + j] = vBeta[i] * x;
                 const int mi = (i - ti0) >> 4, hi = ((i - ti0) >> 3) & 1;
@@ -511,8 +581,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         mm128<false, true>(B0, B2, warp, lane, acc);
         {
             float csum[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+            tm_put(TM_DKC, acc);
             tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) {
-                S(SC_DKC)[i * 128 + j] = x;
                 const int nj = (j - tj0) >> 3, lo = (j - tj0) & 1;
                 csum[nj][lo] = fmaf(S(SC_KC)[i * 128 + j], x, csum[nj][lo]);
             });
@@ -530,23 +600,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         }
         __syncthreads();
         // ---- B0 = Sp; dkh = -diag(beta) dy Sp^T -------------------------------------------
-        for (int i = tid; i < KD * 32; i += TC_THREADS) {
-            const int r = i >> 5, c4 = (i & 31) * 4;
-            float4 x = *reinterpret_cast<const float4*>(S0 + r * VD + c4);
-            const float e = __expf(vPiv[r]);
-            x.x *= e; x.y *= e; x.z *= e; x.w *= e;
-            *reinterpret_cast<float4*>(B0 + r * LD + c4) = x;
-        }
+        stage_state_scaled(B0, S0, vPiv, tid);
         __syncthreads();
         zero_acc(acc);
         mm128<false, true>(B1, B0, warp, lane, acc);
-        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) { S(SC_DKH)[i * 128 + j] = -vBeta[i] * x; });
+        {
+            const int g = lane >> 2;
+#pragma unroll
+            for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+                for (int nj = 0; nj < 4; ++nj) {
+                    const float b0 = -vBeta[ti0 + 16 * mi + g], b1 = -vBeta[ti0 + 16 * mi + g + 8];
+                    acc[mi][nj][0] *= b0; acc[mi][nj][1] *= b0; acc[mi][nj][2] *= b1; acc[mi][nj][3] *= b1;
+                }
+            tm_put(TM_DKH, acc);
+        }
         __syncthreads();
         // ---- B1 = do; dqh = do Sp^T ----------------------------------------------------------
-        for (int i = tid; i < BT * VD; i += TC_THREADS) {
-            const int r = i >> 7, d = i & 127;
-            B1[r * LD + d] = r < n ? bf16_at(p.dout, (row0 + r * rs) * VD + d) : 0.f;
-        }
+        stage_rows_bf16(B1, p.dout, row0, rs, n, tid);
         __syncthreads();
         zero_acc(acc);
         mm128<false, true>(B1, B0, warp, lane, acc);
@@ -556,14 +627,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         stage(B2, S(SC_KC), tid);
         __syncthreads();
         mm128<false, false>(B0, B2, warp, lane, acc);
-        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) { S(SC_DQH)[i * 128 + j] = x; });
+        tm_put(TM_DQH, acc);
         // ---- B1 = X: dkh -= diag(beta) X kc ---------------------------------------------
         __syncthreads();
         stage(B1, S(SC_X), tid);
         __syncthreads();
         zero_acc(acc);
         mm128<false, false>(B1, B2, warp, lane, acc);
-        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) { S(SC_DKH)[i * 128 + j] -= vBeta[i] * x; });
+        {
+            float prev[2][4][4];
+            tm_get(TM_DKH, prev);
+            const int g = lane >> 2;
+#pragma unroll
+            for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+                for (int nj = 0; nj < 4; ++nj) {
+                    const float b0 = vBeta[ti0 + 16 * mi + g], b1 = vBeta[ti0 + 16 * mi + g + 8];
+                    prev[mi][nj][0] -= b0 * acc[mi][nj][0]; prev[mi][nj][1] -= b0 * acc[mi][nj][1];
+                    prev[mi][nj][2] -= b1 * acc[mi][nj][2]; prev[mi][nj][3] -= b1 * acc[mi][nj][3];
+                }
+            tm_put(TM_DKH, prev);
+        }
         // ---- B2 = qh: dkc += W^T qh ------------------------------------------------------
         __syncthreads();
         stage(B2, S(SC_QH), tid);
@@ -572,6 +656,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         mm128<true, false>(B0, B2, warp, lane, acc);
         __syncthreads();
         // ---- B0 = diag(beta) kh: dkc -= X^T (beta kh) ------------------------------------
+#pragma unroll
         for (int i = tid; i < BT * 32; i += TC_THREADS) {
             const int r = i >> 5, c4 = (i & 31) * 4;
             float4 x = *reinterpret_cast<const float4*>(S(SC_KH) + r * 128 + c4);
@@ -591,23 +676,58 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
 #pragma unroll
                     for (int u = 0; u < 4; ++u) acc[mi][nj][u] -= acc2[mi][nj][u];
         }
-        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) { S(SC_DKC)[i * 128 + j] += x; });
+        {
+            float prev[2][4][4];
+            tm_get(TM_DKC, prev);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) flat(prev)[u] += flat(acc)[u];
+            tm_put(TM_DKC, prev);
+        }
         __syncthreads();
 
         // ---- dG into B0; exit terms at the last row; reverse prefix sum; outputs -------------
-        if (tid < KD) {   // e^{G_last} rowsum(Z * S0) for row d = tid of the states
+        {   // e^{G_last} rowsum(Z * S0) for state row d = tid / 4 (four threads per row)
+            const int d = tid >> 2, q4 = (tid & 3) * 32;
             float s = 0.f;
-            for (int v4 = 0; v4 < VD; v4 += 4) {
-                const float4 a = *reinterpret_cast<const float4*>(Z + tid * VD + v4);
-                const float4 b = *reinterpret_cast<const float4*>(S0 + tid * VD + v4);
+#pragma unroll
+            for (int v4 = 0; v4 < 32; v4 += 4) {
+                const float4 a = *reinterpret_cast<const float4*>(Z + d * VD + q4 + v4);
+                const float4 b = *reinterpret_cast<const float4*>(S0 + d * VD + q4 + v4);
                 s = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, s))));
             }
-            vExit[tid] += __expf(vGl[tid]) * s;
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            if ((tid & 3) == 0) vExit[d] += __expf(vGl[d]) * s;
         }
-        for (int i = tid; i < BT * KD; i += TC_THREADS) {
-            const int r = i >> 7, d = i & 127;
-            const size_t e = (size_t)r * 128 + d;
-            B0[r * LD + d] = S(SC_QH)[e] * S(SC_DQH)[e] + S(SC_KH)[e] * S(SC_DKH)[e] - S(SC_KC)[e] * S(SC_DKC)[e];
+        // raw q, k rows (B1, B2), then per fragment element from TMEM: dq, dk and dG (into B0)
+        stage_rows_bf16(B1, p.q, row0, rs, n, tid);
+        stage_rows_bf16(B2, p.k, row0, rs, n, tid);
+        __syncthreads();
+        {   // one 16-row half of the warp's tile at a time (fragment elements 16 mi .. 16 mi + 15)
+            const int g = lane >> 2, t = lane & 3;
+#pragma unroll 1
+            for (int mi = 0; mi < 2; ++mi) {
+                float fg[16], fq[16], fh[16], fc[16];
+                tmem_ld16(tme + TM_G + 16u * mi, fg);
+                tmem_ld16(tme + TM_DQH + 16u * mi, fq);
+                tmem_ld16(tme + TM_DKH + 16u * mi, fh);
+                tmem_ld16(tme + TM_DKC + 16u * mi, fc);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int nj = e >> 2, u = e & 3;
+                    const int i = ti0 + 16 * mi + g + 8 * (u >> 1), j = tj0 + 8 * nj + 2 * t + (u & 1);
+                    const float x = fg[e] - vPiv[j];
+                    const float ep = __expf(x), em = __expf(-x);
+                    const float qq = scale * vNq[i] * B1[i * LD + j], kk = vNk[i] * B2[i * LD + j];
+                    // dG = qh dqh + kh dkh - kc dkc
+                    B0[i * LD + j] = qq * ep * fq[e] + kk * ep * fh[e] - kk * em * fc[e];
+                    if (i < n) {   // with the q/k norm: w.r.t. the normalised q, k
+                        p.dq[(row0 + i * rs) * KD + j] = scale * fq[e] * ep;
+                        p.dk[(row0 + i * rs) * KD + j] = fh[e] * ep + fc[e] * em;
+                    }
+                }
+            }
         }
         __syncthreads();
         if (tid < KD) {   // dg = reverse prefix sum over the valid rows, the exit terms at row n - 1
@@ -619,17 +739,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         }
         if (tid >= KD && tid < KD + BT && tid - KD < n) p.dbeta[row0 + (tid - KD) * rs] = vDb[tid - KD];
         __syncthreads();
-        for (int i = tid; i < n * KD; i += TC_THREADS) {
-            const int r = i >> 7, d = i & 127;
-            const size_t e = (size_t)r * 128 + d;
-            const float x = S(SC_G)[e] - vPiv[d];
-            const float ep = __expf(x), em = __expf(-x);
-            const size_t o = (row0 + r * rs) * KD + d;
-            p.dq[o] = scale * S(SC_DQH)[e] * ep;              // with the q/k norm: w.r.t. the normalised q, k
-            p.dk[o] = S(SC_DKH)[e] * ep + S(SC_DKC)[e] * em;
-            p.dg[o] = B0[r * LD + d];
+#pragma unroll 4
+        for (int i = tid; i < n * 32; i += TC_THREADS) {
+            const int r = i >> 5, c4 = (i & 31) * 4;
+            *reinterpret_cast<float4*>(p.dg + (row0 + r * rs) * KD + c4) = *reinterpret_cast<const float4*>(B0 + r * LD + c4);
         }
     }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
 cudaError_t launch_bwd_tc(const BwdParams& p, const FwdParams& fp, int ctas, cudaStream_t stream) {
