@@ -30,6 +30,7 @@
 #include "kda_bwd.cuh"
 #include "kda_common.cuh"
 #include "sm100_ptx.cuh"
+#include "kda_mma_tf32.cuh"
 
 namespace kda {
 
@@ -38,8 +39,8 @@ namespace {
 // ---------------------------------------------------------------------------
 // Transposed tiles
 // ---------------------------------------------------------------------------
-constexpr int BT_THREADS = 256;
-constexpr int QF_LD = KD + 4;                        // padded fp32 rows
+constexpr int BT_THREADS = 512;
+constexpr int QF_LD = MMA_LD;                        // padded fp32 rows
 constexpr uint32_t BT_SMEM = 2u * BT * QF_LD * 4u;   // Qe (fp32) and do (fp32)
 
 __device__ __forceinline__ float2 h2f(uint32_t u) {
@@ -117,33 +118,26 @@ __global__ void __launch_bounds__(BT_THREADS) kda_bwd_tiles_kernel(const FwdPara
     }
     __syncthreads();
 
-    // Bq[d][v] = sum_t Qe[t][d] do[t][v]: thread owns d0..d0+7 x v0..v0+7
-    const int d0 = (tid >> 4) * 8, v0 = (tid & 15) * 8;
-    float acc[8][8];
+    // Bq[d][v] = sum_t Qe[t][d] do[t][v] on the tensor cores (TF32, fp32 accumulation):
+    // warp w computes the 32 x 32 tile at d = 32 (w / 4), v = 32 (w % 4)
+    const int warp = tid >> 5, lane = tid & 31;
+    const int d0 = 32 * (warp >> 2), v0 = 32 * (warp & 3);
+    float acc[2][4][4];
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-        for (int u = 0; u < 8; ++u) acc[r][u] = 0.f;
-    const int rows = c.len;
-#pragma unroll 2
-    for (int t = 0; t < rows; ++t) {
-        const float4 a0 = *reinterpret_cast<const float4*>(qf + t * QF_LD + d0);
-        const float4 a1 = *reinterpret_cast<const float4*>(qf + t * QF_LD + d0 + 4);
-        const float4 b0 = *reinterpret_cast<const float4*>(df + t * QF_LD + v0);
-        const float4 b1 = *reinterpret_cast<const float4*>(df + t * QF_LD + v0 + 4);
-        const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        for (int nj = 0; nj < 4; ++nj) acc[mi][nj][0] = acc[mi][nj][1] = acc[mi][nj][2] = acc[mi][nj][3] = 0.f;
+    tile_mm<true, false>(qf, df, d0, v0, (c.len + 7) & ~7, lane, acc);
+    uint8_t* piece = dst + TILE_BC + (v0 / BV) * BC_PIECE;   // one 32-column piece per warp
+    const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+    for (int mi = 0; mi < 2; ++mi)
 #pragma unroll
-            for (int u = 0; u < 8; ++u) acc[r][u] = fmaf(a[r], b[u], acc[r][u]);
-    }
-    uint8_t* piece = dst + TILE_BC + (v0 / BV) * BC_PIECE;
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-        *reinterpret_cast<uint4*>(piece + sw64_off(d0 + r, v0 % BV)) =
-            make_uint4(f2h(acc[r][0], acc[r][1]), f2h(acc[r][2], acc[r][3]), f2h(acc[r][4], acc[r][5]),
-                       f2h(acc[r][6], acc[r][7]));
+        for (int nj = 0; nj < 4; ++nj) {
+            const int d = d0 + 16 * mi + g, col = 8 * nj + 2 * t;
+            *reinterpret_cast<uint32_t*>(piece + sw64_off(d, col)) = f2h(acc[mi][nj][0], acc[mi][nj][1]);
+            *reinterpret_cast<uint32_t*>(piece + sw64_off(d + 8, col)) = f2h(acc[mi][nj][2], acc[mi][nj][3]);
+        }
 }
 
 // ---------------------------------------------------------------------------

@@ -45,6 +45,7 @@
 #include "kda_bwd.cuh"
 #include "kda_common.cuh"
 #include "sm100_ptx.cuh"
+#include "kda_mma_tf32.cuh"
 
 namespace kda {
 
@@ -52,7 +53,7 @@ namespace {
 
 constexpr int TC_THREADS = 512;
 constexpr int TC_WARPS = TC_THREADS / 32;
-constexpr int LD = 132;                                 // padded row length of the shared buffers
+constexpr int LD = MMA_LD;                              // padded row length of the shared buffers
 constexpr int MAT = BT * LD;                            // floats per shared buffer
 constexpr int NVEC = 9;                                 // 128-float vectors in shared memory (+ the TMEM address)
 constexpr uint32_t TC_SMEM = (3u * MAT + NVEC * 128u) * 4u;
@@ -68,54 +69,6 @@ constexpr size_t SC_MAT = (size_t)BT * 128;
 
 // shared vectors
 enum : int { V_BETA = 0, V_PIV, V_GLAST, V_EXIT, V_DB, V_NQ, V_NK, V_TMP };
-
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
-
-// acc (a 32 x 32 tile at rows i0, cols j0) += opA(i0.., 0..kd) opB(0..kd, j0..) with
-// opA(i, l) = TA ? A[l][i] : A[i][l] and opB(l, j) = TB ? B[j][l] : B[l][j], shared
-// buffers of row length LD.  Fragment layouts of m16n8k8 (g = lane / 4, t = lane % 4):
-// A: (g, t) (g+8, t) (g, t+4) (g+8, t+4); B: (t, g) (t+4, g); D: (g, 2t) (g, 2t+1) (g+8, 2t) (g+8, 2t+1).
-template <bool TA, bool TB>
-__device__ __forceinline__ void tile_mm(const float* A, const float* B, int i0, int j0, int kd, int lane,
-                                        float (&acc)[2][4][4]) {
-    const int g = lane >> 2, t = lane & 3;
-    auto opA = [&](int i, int l) { return TA ? A[l * LD + i] : A[i * LD + l]; };
-    auto opB = [&](int l, int j) { return TB ? B[j * LD + l] : B[l * LD + j]; };
-#pragma unroll 2
-    for (int k0 = 0; k0 < kd; k0 += 8) {
-        uint32_t a[2][4], b[4][2];
-#pragma unroll
-        for (int mi = 0; mi < 2; ++mi) {
-            const int r = i0 + 16 * mi + g;
-            a[mi][0] = to_tf32(opA(r, k0 + t));
-            a[mi][1] = to_tf32(opA(r + 8, k0 + t));
-            a[mi][2] = to_tf32(opA(r, k0 + t + 4));
-            a[mi][3] = to_tf32(opA(r + 8, k0 + t + 4));
-        }
-#pragma unroll
-        for (int nj = 0; nj < 4; ++nj) {
-            const int c = j0 + 8 * nj + g;
-            b[nj][0] = to_tf32(opB(k0 + t, c));
-            b[nj][1] = to_tf32(opB(k0 + t + 4, c));
-        }
-#pragma unroll
-        for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-            for (int nj = 0; nj < 4; ++nj) mma_tf32(acc[mi][nj], a[mi], b[nj]);
-    }
-}
 
 __device__ __forceinline__ float (&flat(float (&acc)[2][4][4]))[32] {
     return *reinterpret_cast<float(*)[32]>(&acc[0][0][0]);
