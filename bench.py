@@ -370,12 +370,17 @@ def run_decode(args, rank, world, local):
 # ---------------------------------------------------------------------------
 
 BWD_METRIC = "KDA bwd (dq, dk, dv, dg, dbeta, dh0) token*heads/s at T=64K H=32 K=V=128"
-# The per-chunk chain-rule kernel's algorithmic work per token-head: one
-# forward replay (decay, k.a, delta update: 5 flop per state entry) and the
-# per-token chain rule (18 flop per state entry), over the K x V state.
-BWD_CHUNK_FLOP_PER_TH = 23 * N128 * N128
-# FP32 CUDA-core peak: 152 SMs x 128 lanes x 2 flop per FMA at the maximum SM clock.
-FP32_LANES = 152 * 128
+# The per-chunk kernel (chunked chain rule, kda_bwd_tc_kernel): algorithmic HBM
+# bytes per token-head = q, k, v, do bf16 (4 x 256) + g fp32 512 + beta 4 + the
+# chunk's entering state and exit state gradient (2 x 64 KiB per 128 tokens:
+# 1024) + dq, dk, dg fp32 (3 x 512) + dv fp32 512 + dbeta 4; algorithmic flop
+# per token-head = its sixteen 128 x 128 x 128 products at their triangular
+# sizes (5 dense + 11 triangular: 10.5 x 2 n^3 per chunk) plus the triangular
+# inverse (2/3 n^3), over n = 128 tokens.
+BWD_TC_BYTES_PER_TH = 4 * 256 + 512 + 4 + 1024 + 3 * 512 + 512 + 4
+BWD_TC_FLOP_PER_TH = (21.0 + 2.0 / 3.0) * N128 * N128
+# TF32 dense peak: the measured bf16 peak x the nominal TF32 / bf16 ratio (1.1 / 2.25).
+TF32_OVER_BF16 = 1.1 / 2.25
 
 
 def bwd_oracle_rate(w, target_s):
@@ -465,26 +470,37 @@ def run_bwd(args, rank, world, local, w):
     assert binding.get_status(ws) == 0
     ms = max_over_ranks(e0.elapsed_time(e1), dev, world) / args.steps
     stages = ["forward_replay", "transposed_tiles", "reverse_state_pass", "chunk_chain_rule", "rest"]
+    # chunk_chain_rule = the tensor-core per-chunk kernel and the per-token kernel for the chunks it left
     stage_ms = {nm: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j, nm in enumerate(stages)}
     th = B * T * H
     ck = clocks.summary(t_start, t_end)
-    sm_max = ck.get("sm_max_mhz") or 2070.0
-    peak = FP32_LANES * 2 * sm_max * 1e6 / 1e12
-    achieved = th * BWD_CHUNK_FLOP_PER_TH / (stage_ms["chunk_chain_rule"] * 1e-3) / 1e12
+    peaks = load_peaks()
+    k_ms = stage_ms["chunk_chain_rule"]
+    tf32_peak = peaks["bf16_tflops"] * TF32_OVER_BF16
+    t_hbm = th * BWD_TC_BYTES_PER_TH / (peaks["hbm_gbs"] * 1e9) * 1e3
+    t_tc = th * BWD_TC_FLOP_PER_TH / (tf32_peak * 1e12) * 1e3
+    gbs = th * BWD_TC_BYTES_PER_TH / (k_ms * 1e-3) / 1e9
+    tfl = th * BWD_TC_FLOP_PER_TH / (k_ms * 1e-3) / 1e12
+    tr = load_traffic().get("kda_bwd_tc_kernel")
+    if t_hbm >= t_tc:
+        roof = {"kernel": "kda_bwd_tc_kernel", "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}
+    else:
+        roof = {"kernel": "kda_bwd_tc_kernel", "bound": "tensor", "achieved": tfl, "peak": tf32_peak,
+                "unit": "TFLOP/s", "frac": tfl / tf32_peak}
+    roof.update({"traffic": (tr * th if tr is not None else None),
+                 "alg_bytes_per_launch": th * BWD_TC_BYTES_PER_TH, "alg_flop_per_launch": th * BWD_TC_FLOP_PER_TH,
+                 "ms_per_launch": k_ms, "tensor_tflops": tfl, "tensor_peak_tf32": tf32_peak,
+                 "peak_source": f"{peaks['source']} (HBM copy; TF32 = bf16 x 1.1/2.25)",
+                 "t_hbm_ms": t_hbm, "t_tensor_ms": t_tc})
     line = {"metric": BWD_METRIC, "value": job_rate(th, world, ms), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "B": B, "T": T, "H": H, "K": 128, "V": 128,
                        "l2_between_steps": "inputs and workspace (several GB) exceed L2; no flush"},
             "stage_ms": stage_ms,
-            "roofline": {"kernel": "kda_bwd_chunk_kernel", "bound": "alu", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak,
-                         "traffic": (tr * th if (tr := load_traffic().get("kda_bwd_chunk_kernel")) is not None
-                                     else None),
-                         "peak_basis": f"fp32 FMA: 152 SMs x 128 lanes x 2 flop x {sm_max:.0f} MHz",
-                         "alg_flop_per_launch": th * BWD_CHUNK_FLOP_PER_TH,
-                         "ms_per_launch": stage_ms["chunk_chain_rule"]},
-            "gpu_launches": 7 * args.steps}
+            "roofline": roof,
+            "gpu_launches": 8 * args.steps}
     if args.e2e_steps > 0:
         host_in = {n: t.cpu().pin_memory() for n, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta),
                                                         ("do", do), ("dht", dht))}

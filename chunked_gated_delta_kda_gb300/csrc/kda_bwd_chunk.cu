@@ -259,11 +259,11 @@ __global__ void __launch_bounds__(CB_THREADS, 1) kda_bwd_chunk_kernel(const BwdP
     float* scratch = p.scratch + (size_t)blockIdx.x * BT * VD * KD;
 
     for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+        if (p.tc_skip != nullptr && p.tc_skip[it] == 0u) continue;   // done by the tensor-core kernel
         const int slot = (int)(it / H), h = (int)(it % H);
         ChunkRef c;
         if (!slot_chunk(fp, slot, c)) continue;                    // uniform
         if (fp.exact_flags[(size_t)c.n * H + h] != 0u) continue;   // replayed by the token-by-token kernel
-        if (p.tc_skip != nullptr && p.tc_skip[it] == 0u) continue;   // done by the tensor-core kernel
         long long bos;
         int len;
         if (!seq_bounds(fp, c.n, bos, len)) continue;

@@ -107,3 +107,35 @@ def test_bwd_strong_decay(gate_div):
     ref = run_ref(x, gr)
     for path in PATHS:
         print(path, check(run_gpu(x, gr, path=path), ref, path))
+
+
+def _chunk_paths(x, T, H):
+    """Per (chunk, head) of a fixed-length input: (left by the tensor-core
+    kernel to the per-token kernel, flagged by the forward for the
+    token-by-token path), from the in-chunk gate prefix sums around the
+    pivot row min(n - 1, 64): the first when some factor exponent leaves
+    [-60, 60], the second when the decay from the pivot passes the forward's
+    e^80 factoring range."""
+    g = to_np(x["g"])[0].astype(np.float64)
+    out = []
+    for c0 in range(0, T, 128):
+        for h in range(H):
+            G = np.cumsum(g[c0:c0 + 128, h], axis=0)
+            P = G[min(G.shape[0] - 1, 64)]
+            d = np.abs(G - P).max()
+            out.append((bool(d > 60 or (P < -60).any() or (G[-1] - P < -60).any()), bool(d > 115 * np.log(2))))
+    return out
+
+
+@pytest.mark.parametrize("gate_div,expect_tc", [(1.5, True), (1.0, False)])
+def test_bwd_decay_paths(gate_div, expect_tc):
+    """Strong but in-range decay: at g/1.5 every chunk stays on the tensor-core
+    kernel (decays up to ~e^44 from the pivot); at g/1.0 every chunk leaves
+    its fp32 factor range (~e^65) without reaching the forward's, so the
+    per-token kernel takes the chunks (the forward's exact path does not)."""
+    w = custom("dp", B=1, T=256, H=2, with_h0=True, seed=17, gate_div=gate_div)
+    x = make_inputs(w)
+    paths = _chunk_paths(x, 256, 2)
+    assert all(skip != expect_tc and not exact for skip, exact in paths), paths
+    gr = make_grad_inputs(w)
+    print(gate_div, check(run_gpu(x, gr), run_ref(x, gr), "chunk"))
