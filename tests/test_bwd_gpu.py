@@ -164,3 +164,38 @@ def test_bwd_full_size_against_token_path():
         ratios[name] = ((a.double() - b.double()).abs() / (G_RTOL["chunk"] * (b.double().abs() + rms))).max().item()
     print(ratios)
     assert max(ratios.values()) <= 1.0, ratios
+
+
+@pytest.mark.parametrize("varlen", [False, True])
+def test_bwd_no_tokens(varlen):
+    """T = 0: no token gradients; dh0 = dht (the state passes through)."""
+    from chunked_gated_delta_kda_gb300 import binding
+    H, N = 2, (3 if varlen else 2)
+    B = 1 if varlen else N
+    z = lambda *s, dt=torch.bfloat16: torch.zeros(s, dtype=dt, device="cuda")
+    q, k, v, do = z(B, 0, H, 128), z(B, 0, H, 128), z(B, 0, H, 128), z(B, 0, H, 128)
+    g, beta = z(B, 0, H, 128, dt=torch.float32), z(B, 0, H, dt=torch.float32)
+    cu = torch.zeros(N + 1, dtype=torch.int32, device="cuda") if varlen else None
+    dht = torch.randn((N, H, 128, 128), generator=torch.Generator().manual_seed(3)).cuda()
+    out = binding.bwd(q, k, v, g, beta, do, dht=dht, cu_seqlens=cu)
+    torch.cuda.synchronize()
+    assert all(t.numel() == 0 for t in out[:5])
+    assert torch.equal(out[5], dht)
+
+
+def test_bwd_bad_cu_seqlens_reported():
+    """A decreasing cu_seqlens is found on the device and reported through the
+    workspace status word (BAD_CU_SEQLENS), not a fault."""
+    from chunked_gated_delta_kda_gb300 import binding
+    w = custom("bc", B=1, T=256, H=2, seqlens=(100, 156), seed=21)
+    x = {kk: (vv.cuda() if isinstance(vv, torch.Tensor) else vv) for kk, vv in make_inputs(w).items()}
+    gr = {kk: (vv.cuda() if isinstance(vv, torch.Tensor) else vv) for kk, vv in make_grad_inputs(w).items()}
+    cu = torch.tensor([0, 200, 150], dtype=torch.int32, device="cuda")   # not non-decreasing
+    ws = torch.empty(binding.bwd_workspace_bytes(1, 256, 2, 2), dtype=torch.uint8, device="cuda")
+    f32 = dict(dtype=torch.float32, device="cuda")
+    dq, dk, dv, dg = (torch.zeros((1, 256, 2, 128), **f32) for _ in range(4))
+    dbeta = torch.zeros((1, 256, 2), **f32)
+    dh0 = torch.zeros((2, 2, 128, 128), **f32)
+    binding.kda_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], None, None, cu, gr["do"], gr["dht"], dq, dk, dv, dg,
+                    dbeta, dh0, 2, 0, ws)
+    assert binding.get_status(ws) == 4
