@@ -97,6 +97,20 @@ __device__ __forceinline__ void tile_for(const float (&acc)[2][4][4], int i0, in
         }
 }
 
+// The warp tile's elements as 16 pairs of row-adjacent columns: pair q = (mi * 4 + nj) * 2 + hh
+// holds (i, j) and (i, j + 1) with i = i0 + 16 mi + g + 8 hh, j = j0 + 8 nj + 2 t, i.e.
+// acc[mi][nj][2 hh] and acc[mi][nj][2 hh + 1].
+template <class F>
+__device__ __forceinline__ void frag_pairs(int i0, int j0, int lane, F f) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int nj = 0; nj < 4; ++nj)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) f((mi * 4 + nj) * 2 + hh, mi, nj, hh, i0 + 16 * mi + g + 8 * hh, j0 + 8 * nj + 2 * t);
+}
+
 // Full 128 x 128 x 128 product: warp w owns the tile at rows 32 (w / 4), cols 32 (w % 4).
 template <bool TA, bool TB>
 __device__ __forceinline__ void mm128(const float* A, const float* B, int warp, int lane, float (&acc)[2][4][4]) {
@@ -443,16 +457,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         // ---- B2 = Sp = e^P S0 (rows) ---------------------------------------------------------
         stage_state_scaled(B2, S0, vPiv, tid);
         __syncthreads();
-        // ---- y0 = v - kh Sp; B1 = y = beta y0 ----------------------------------------------
-        zero_acc(acc);
-        mm128<false, false>(B1, B2, warp, lane, acc);
-        __syncthreads();
-        tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) {
-            const float vv = i < n ? bf16_at(p.v, (row0 + i * rs) * VD + j) : 0.f;
-            const float y0 = vv - x;
-            S(SC_Y0)[i * 128 + j] = y0;
-            B1[i * LD + j] = vBeta[i] * y0;
-        });
+        // ---- y0 = v - kh Sp; B1 = y = beta y0 (v fetched before the product) ---------------
+        {
+            uint32_t vpre[16];
+            frag_pairs(ti0, tj0, lane, [&](int q, int, int, int, int i, int j) {
+                vpre[q] = i < n ? *reinterpret_cast<const uint32_t*>(p.v + (row0 + i * rs) * VD + j) : 0u;
+            });
+            zero_acc(acc);
+            mm128<false, false>(B1, B2, warp, lane, acc);
+            __syncthreads();
+            frag_pairs(ti0, tj0, lane, [&](int q, int mi, int nj, int hh, int i, int j) {
+                const float y0a = __uint_as_float(vpre[q] << 16) - acc[mi][nj][2 * hh];
+                const float y0b = __uint_as_float(vpre[q] & 0xffff0000u) - acc[mi][nj][2 * hh + 1];
+                *reinterpret_cast<float2*>(S(SC_Y0) + i * 128 + j) = make_float2(y0a, y0b);
+                B1[i * LD + j] = vBeta[i] * y0a;
+                B1[i * LD + j + 1] = vBeta[i] * y0b;
+            });
+        }
         __syncthreads();
         // ---- rho = Li y; B1 = rho ------------------------------------------------------------
         zero_acc(acc);
@@ -476,7 +497,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         mm128<true, false>(B1, B0, warp, lane, acc);
         __syncthreads();
         stage(B1, S(SC_KC), tid);
-        stage_state_scaled(B2, Z, vTmp, tid);   // B2 = Ze = e^{G_last - P} Z (rows)
+        {   // B2 = Ze = e^{G_last - P} Z (rows); the exit term e^{G_last} rowsum(Z * S0) on the way
+            // step s of warp w covers state row w + 16 s (its 32 lanes x 4 columns)
+            float part[8];
+#pragma unroll
+            for (int st = 0; st < 8; ++st) {
+                const int r = warp + 16 * st, c4 = lane * 4;
+                float4 zv = *reinterpret_cast<const float4*>(Z + r * VD + c4);
+                const float4 sv = *reinterpret_cast<const float4*>(S0 + r * VD + c4);
+                part[st] = zv.x * sv.x + zv.y * sv.y + zv.z * sv.z + zv.w * sv.w;
+                const float f = __expf(vTmp[r]);
+                zv.x *= f; zv.y *= f; zv.z *= f; zv.w *= f;
+                *reinterpret_cast<float4*>(B2 + r * LD + c4) = zv;
+            }
+            warp_sum8(part, lane);
+            if (lane == 0) {
+#pragma unroll
+                for (int st = 0; st < 8; ++st) vExit[warp + 16 * st] += __expf(vGl[warp + 16 * st]) * part[st];
+            }
+        }
         __syncthreads();
         mm128<false, false>(B1, B2, warp, lane, acc);
         __syncthreads();
@@ -484,16 +523,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         stage(B0, S(SC_LI), tid);
         __syncthreads();
         // ---- dy = Li^T drho; dv = beta dy; dbeta += rowsum(dy y0) --------------------------
-        zero_acc(acc);
-        mm128<true, false>(B0, B1, warp, lane, acc);
-        __syncthreads();
         {
+            float2 ypre[16];
+            frag_pairs(ti0, tj0, lane, [&](int q, int, int, int, int i, int j) {
+                ypre[q] = *reinterpret_cast<const float2*>(S(SC_Y0) + i * 128 + j);
+            });
+            zero_acc(acc);
+            mm128<true, false>(B0, B1, warp, lane, acc);
+            __syncthreads();
             float rsum[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-            tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) {
-                B1[i * LD + j] = x;
-                if (i < n) p.dv[(row0 + i * rs) * VD + j] = vBeta[i] * x;
-                const int mi = (i - ti0) >> 4, hi = ((i - ti0) >> 3) & 1;
-                rsum[mi][hi] = fmaf(x, S(SC_Y0)[i * 128 + j], rsum[mi][hi]);
+            frag_pairs(ti0, tj0, lane, [&](int q, int mi, int nj, int hh, int i, int j) {
+                const float a = acc[mi][nj][2 * hh], b = acc[mi][nj][2 * hh + 1];
+                B1[i * LD + j] = a;
+                B1[i * LD + j + 1] = b;
+                if (i < n)
+                    *reinterpret_cast<float2*>(p.dv + (row0 + i * rs) * VD + j) = make_float2(vBeta[i] * a, vBeta[i] * b);
+                rsum[mi][hh] = fmaf(a, ypre[q].x, fmaf(b, ypre[q].y, rsum[mi][hh]));
             });
             // reduce over the 4 lanes sharing a row, then across the row band's warps
 #pragma unroll
@@ -509,15 +554,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         stage(B0, S(SC_RHO), tid);
         __syncthreads();
         // ---- X = strict_tril(dy rho^T); dbeta -= rowsum(X Pm) ------------------------------
-        zero_acc(acc);
-        mm128<false, true>(B1, B0, warp, lane, acc);
         {
+            float2 ppre[16];
+            frag_pairs(ti0, tj0, lane, [&](int q, int, int, int, int i, int j) {
+                ppre[q] = *reinterpret_cast<const float2*>(S(SC_PM) + i * 128 + j);
+            });
+            zero_acc(acc);
+            mm128<false, true>(B1, B0, warp, lane, acc);
             float rsum[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-            tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) {
-                const float xs = (j < i) ? x : 0.f;
-                S(SC_X)[i * 128 + j] = xs;
-                const int mi = (i - ti0) >> 4, hi = ((i - ti0) >> 3) & 1;
-                rsum[mi][hi] = fmaf(-xs, S(SC_PM)[i * 128 + j], rsum[mi][hi]);
+            frag_pairs(ti0, tj0, lane, [&](int q, int mi, int nj, int hh, int i, int j) {
+                const float a = (j < i) ? acc[mi][nj][2 * hh] : 0.f, b = (j + 1 < i) ? acc[mi][nj][2 * hh + 1] : 0.f;
+                *reinterpret_cast<float2*>(S(SC_X) + i * 128 + j) = make_float2(a, b);
+                rsum[mi][hh] = fmaf(-a, ppre[q].x, fmaf(-b, ppre[q].y, rsum[mi][hh]));
             });
 #pragma unroll
             for (int mi = 0; mi < 2; ++mi)
@@ -530,14 +578,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
                 }
         }
         // ---- dkc = rho Ze^T (+ later terms); exit term colsum(kc * rho Ze^T) ---------------
-        zero_acc(acc);
-        mm128<false, true>(B0, B2, warp, lane, acc);
         {
-            float csum[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+            float2 kpre[16];
+            frag_pairs(ti0, tj0, lane, [&](int q, int, int, int, int i, int j) {
+                kpre[q] = *reinterpret_cast<const float2*>(S(SC_KC) + i * 128 + j);
+            });
+            zero_acc(acc);
+            mm128<false, true>(B0, B2, warp, lane, acc);
             tm_put(TM_DKC, acc);
-            tile_for(acc, ti0, tj0, lane, [&](int i, int j, float x) {
-                const int nj = (j - tj0) >> 3, lo = (j - tj0) & 1;
-                csum[nj][lo] = fmaf(S(SC_KC)[i * 128 + j], x, csum[nj][lo]);
+            float csum[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+            frag_pairs(ti0, tj0, lane, [&](int q, int mi, int nj, int hh, int, int) {
+                csum[nj][0] = fmaf(kpre[q].x, acc[mi][nj][2 * hh], csum[nj][0]);
+                csum[nj][1] = fmaf(kpre[q].y, acc[mi][nj][2 * hh + 1], csum[nj][1]);
             });
             // reduce over the 8 lanes sharing a column (lane / 4), then across warps
 #pragma unroll
@@ -639,19 +691,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         __syncthreads();
 
         // ---- dG into B0; exit terms at the last row; reverse prefix sum; outputs -------------
-        {   // e^{G_last} rowsum(Z * S0) for state row d = tid / 4 (four threads per row)
-            const int d = tid >> 2, q4 = (tid & 3) * 32;
-            float s = 0.f;
-#pragma unroll
-            for (int v4 = 0; v4 < 32; v4 += 4) {
-                const float4 a = *reinterpret_cast<const float4*>(Z + d * VD + q4 + v4);
-                const float4 b = *reinterpret_cast<const float4*>(S0 + d * VD + q4 + v4);
-                s = fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, s))));
-            }
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if ((tid & 3) == 0) vExit[d] += __expf(vGl[d]) * s;
-        }
         // raw q, k rows (B1, B2), then per fragment element from TMEM: dq, dk and dG (into B0)
         stage_rows_bf16(B1, p.q, row0, rs, n, tid);
         stage_rows_bf16(B2, p.k, row0, rs, n, tid);
