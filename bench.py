@@ -472,6 +472,19 @@ def run_bwd(args, rank, world, local, w):
     stages = ["forward_replay", "transposed_tiles", "reverse_state_pass", "chunk_chain_rule", "rest"]
     # chunk_chain_rule = the tensor-core per-chunk kernel and the per-token kernel for the chunks it left
     stage_ms = {nm: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j, nm in enumerate(stages)}
+    # training path: one forward that saves its chunk states, then backwards that reuse them
+    o_tmp = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device=dev)
+    binding.kda_fwd(q, k, v, g, beta, None, h0, cu, o_tmp, None, N, binding.KDA_FLAG_SAVE_FOR_BWD, ws)
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    for i in range(args.steps):
+        binding.kda_bwd(q, k, v, g, beta, None, h0, cu, do, dht, dq, dk, dv, dg, dbeta, dh0, N,
+                        binding.KDA_FLAG_BWD_REUSE_FWD, ws)
+    r1.record(stream)
+    torch.cuda.synchronize(dev)
+    assert binding.get_status(ws) == 0
+    ms_reuse = max_over_ranks(r0.elapsed_time(r1), dev, world) / args.steps
+    del o_tmp
     th = B * T * H
     ck = clocks.summary(t_start, t_end)
     peaks = load_peaks()
@@ -499,6 +512,7 @@ def run_bwd(args, rank, world, local, w):
             "config": {"workload": w.name, "B": B, "T": T, "H": H, "K": 128, "V": 128,
                        "l2_between_steps": "inputs and workspace (several GB) exceed L2; no flush"},
             "stage_ms": stage_ms,
+            "ms_per_step_reusing_saved_forward": ms_reuse,
             "roofline": roof,
             "gpu_launches": 8 * args.steps}
     if args.e2e_steps > 0:

@@ -25,6 +25,8 @@ from . import build as _build
 KDA_FLAG_QK_L2NORM = 1
 KDA_FLAG_BWD_TOKEN_EXACT = 2
 KDA_FLAG_BWD_CHUNK_FP32 = 4
+KDA_FLAG_SAVE_FOR_BWD = 8
+KDA_FLAG_BWD_REUSE_FWD = 16
 
 _STATUS = {
     0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
@@ -160,9 +162,12 @@ def _check(name, t, dtype, ndim):
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
         scale: Optional[float] = None, initial_state: Optional[torch.Tensor] = None,
         output_final_state: bool = False, use_qk_l2norm_in_kernel: bool = False,
-        cu_seqlens: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None
-        ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """Chunked KDA forward.  q, k: bf16 [B,T,H,K]; v: bf16 [B,T,H,V]; g: fp32
+        cu_seqlens: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+        save_for_backward: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunked KDA forward.  ``save_for_backward`` (training) also stores the
+    chunk states in ``workspace`` (which must then be a caller tensor of at
+    least ``bwd_workspace_bytes`` bytes) for ``bwd(..., reuse_forward=True,
+    workspace=<the same tensor>)``.  q, k: bf16 [B,T,H,K]; v: bf16 [B,T,H,V]; g: fp32
     [B,T,H,K]; beta: fp32 [B,T,H]; initial_state: fp32 [N,H,V,K] or None;
     cu_seqlens: int32 [N+1] on the device (varlen, B == 1) or None (fixed
     length, T % 128 == 0).  Returns (o bf16 [B,T,H,V], final state fp32
@@ -193,10 +198,12 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
     h0 = initial_state.contiguous() if initial_state is not None else None
     o = torch.empty((B, T, H, V), dtype=torch.bfloat16, device=dev)
     ht = torch.empty((N, H, V, K), dtype=torch.float32, device=dev) if output_final_state else None
-    need = workspace_bytes(B, T, H, N, K, V)
+    need = bwd_workspace_bytes(B, T, H, N, K, V) if save_for_backward else workspace_bytes(B, T, H, N, K, V)
     if workspace is None or workspace.numel() * workspace.element_size() < need:
+        if save_for_backward:
+            raise ValueError("save_for_backward needs a workspace of at least bwd_workspace_bytes(...) bytes")
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
-    flags = KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0
+    flags = (KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0) | (KDA_FLAG_SAVE_FOR_BWD if save_for_backward else 0)
     with torch.cuda.device(dev):
         kda_fwd(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, N, flags, workspace)
     return o, ht
@@ -351,12 +358,14 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
         do: torch.Tensor, scale: Optional[float] = None, initial_state: Optional[torch.Tensor] = None,
         dht: Optional[torch.Tensor] = None, use_qk_l2norm_in_kernel: bool = False,
         cu_seqlens: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-        token_exact: bool = False, chunk_fp32: bool = False):
+        token_exact: bool = False, chunk_fp32: bool = False, reuse_forward: bool = False):
     """KDA backward of ``fwd`` with the same arguments: the gradients of
     <do, o> + <dht, ht>.  do: bf16 [B,T,H,V]; dht: fp32 [N,H,V,K] or None.
     ``token_exact`` selects the token-by-token backward for every unit;
     ``chunk_fp32`` the per-token fp32 chain rule inside every chunk (instead
-    of the chunked form on the tensor cores).
+    of the chunked form on the tensor cores); ``reuse_forward`` skips the
+    forward replay, using what ``fwd(..., save_for_backward=True)`` left in
+    ``workspace`` for the same inputs.
     Returns fp32 (dq, dk, dv, dg, dbeta, dh0) with the shapes of q, k, v, g,
     beta and the state [N,H,V,K]."""
     for name, t, dt, nd in (("q", q, torch.bfloat16, 4), ("k", k, torch.bfloat16, 4), ("v", v, torch.bfloat16, 4),
@@ -389,9 +398,11 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
     dh0 = torch.empty((N, H, V, K), **f32)
     need = bwd_workspace_bytes(B, T, H, N, K, V)
     if workspace is None or workspace.numel() * workspace.element_size() < need:
+        if reuse_forward:
+            raise ValueError("reuse_forward needs the workspace the saving forward used")
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     flags = ((KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0) | (KDA_FLAG_BWD_TOKEN_EXACT if token_exact else 0)
-             | (KDA_FLAG_BWD_CHUNK_FP32 if chunk_fp32 else 0))
+             | (KDA_FLAG_BWD_CHUNK_FP32 if chunk_fp32 else 0) | (KDA_FLAG_BWD_REUSE_FWD if reuse_forward else 0))
     with torch.cuda.device(dev):
         kda_bwd(q, k, v, g, beta, scale, h0, cu_seqlens, do, dht, dq, dk, dv, dg, dbeta, dh0, N, flags, workspace)
     return dq, dk, dv, dg, dbeta, dh0

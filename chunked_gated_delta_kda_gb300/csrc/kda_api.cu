@@ -8,6 +8,7 @@
 #include "kda_common.cuh"
 
 namespace kda {
+unsigned long long bwd_chunk_state_offset(int B, int T, int H, int N);
 cudaError_t launch_prep(const FwdParams& p, bool l2norm, cudaStream_t stream);
 cudaError_t launch_scan(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_exact(const FwdParams& p, const uint32_t* flags, bool l2norm, cudaStream_t stream);
@@ -50,7 +51,8 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const fl
     if (!workspace) return KDA_ERR_INVALID_ARG;
     if (T > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
     if (B < 1 || T < 0 || H < 1 || N < 1 || H > 65535 || N > 65535) return KDA_ERR_INVALID_ARG;
-    if ((flags & ~KDA_FLAG_QK_L2NORM) != 0u) return KDA_ERR_INVALID_ARG;
+    if ((flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_SAVE_FOR_BWD)) != 0u) return KDA_ERR_INVALID_ARG;
+    const bool save = (flags & KDA_FLAG_SAVE_FOR_BWD) != 0u;
     if (cu_seqlens == nullptr) {
         if (N != B || T % kda::BT != 0) return KDA_ERR_INVALID_ARG;
     } else {
@@ -61,6 +63,7 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const fl
         (h0 && !aligned16(h0)) || (ht && !aligned16(ht)) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return KDA_ERR_INVALID_ARG;
     if (workspace_bytes < kda_fwd_workspace_bytes(B, T, H, K, V, N)) return KDA_ERR_INVALID_ARG;
+    if (save && workspace_bytes < kda_bwd_workspace_bytes(B, T, H, K, V, N)) return KDA_ERR_INVALID_ARG;
     const long long total_rows = (long long)B * T * H;
     if (total_rows * kda::KD >= (1ll << 62)) return KDA_ERR_INVALID_ARG;
     if (!(scale > 0.f) || std::isnan(scale)) scale = 1.0f / std::sqrt((float)K);
@@ -82,6 +85,11 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const fl
     p.tiles = static_cast<uint8_t*>(workspace) + kda::ws_tiles_offset(items);
     p.exact_flags =
         reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + kda::ws_tiles_offset(items) + items * kda::TILE_BYTES);
+    // with KDA_FLAG_SAVE_FOR_BWD the scan also stores the state entering every
+    // chunk where kda_bwd's workspace layout keeps it (the tiles and flags are
+    // already where kda_bwd reads them: its layout starts with this one)
+    p.ckpt = save ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kda::bwd_chunk_state_offset(B, T, H, N))
+                  : nullptr;
     p.scale = scale;
     p.T = T;
     p.H = H;

@@ -70,6 +70,12 @@ bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
+namespace kda {
+// Byte offset of the chunk states in kda_bwd's workspace (kda_fwd stores them
+// there under KDA_FLAG_SAVE_FOR_BWD).
+unsigned long long bwd_chunk_state_offset(int B, int T, int H, int N) { return layout(B, T, H, N).ckpt_s; }
+}  // namespace kda
+
 extern "C" {
 
 size_t kda_bwd_workspace_bytes(int B, int T, int H, int K, int V, int N) {
@@ -85,8 +91,11 @@ static kda_status bwd_impl(const void* q, const void* k, const void* v, const fl
     if (K != kda::KD || V != kda::VD) return KDA_ERR_UNSUPPORTED;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return KDA_ERR_INVALID_ARG;
     if (B < 1 || T < 0 || H < 1 || N < 1 || H > 65535 || N > 65535) return KDA_ERR_INVALID_ARG;
-    if ((flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_BWD_TOKEN_EXACT | KDA_FLAG_BWD_CHUNK_FP32)) != 0u)
+    if ((flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_BWD_TOKEN_EXACT | KDA_FLAG_BWD_CHUNK_FP32 |
+                   KDA_FLAG_BWD_REUSE_FWD)) != 0u)
         return KDA_ERR_INVALID_ARG;
+    const bool reuse = (flags & KDA_FLAG_BWD_REUSE_FWD) != 0u;
+    if (reuse && (flags & KDA_FLAG_BWD_TOKEN_EXACT)) return KDA_ERR_INVALID_ARG;
     if (cu_seqlens == nullptr) {
         if (N != B || T % kda::BT != 0) return KDA_ERR_INVALID_ARG;
     } else if (B != 1) {
@@ -169,9 +178,11 @@ static kda_status bwd_impl(const void* q, const void* k, const void* v, const fl
     if (flags & KDA_FLAG_BWD_TOKEN_EXACT) {
         if (kda::launch_bwd_exact(p, nullptr, ctas < N * H ? ctas : N * H, stream) != cudaSuccess) return KDA_ERR_CUDA;
     } else {
-        if (cudaMemsetAsync(fp.exact_flags, 0, (size_t)N * H * 4, stream) != cudaSuccess) return KDA_ERR_CUDA;
-        if (fp.nslots > 0 && kda::launch_prep(fp, l2norm, stream) != cudaSuccess) return KDA_ERR_CUDA;
-        if (kda::launch_scan(fp, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        if (!reuse) {   // else: the tiles, flags and chunk states of the saving forward are in place
+            if (cudaMemsetAsync(fp.exact_flags, 0, (size_t)N * H * 4, stream) != cudaSuccess) return KDA_ERR_CUDA;
+            if (fp.nslots > 0 && kda::launch_prep(fp, l2norm, stream) != cudaSuccess) return KDA_ERR_CUDA;
+            if (kda::launch_scan(fp, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        }
         if (!mark(1)) return KDA_ERR_CUDA;
         if (kda::launch_bwd_tiles(fp, ws + L.btiles, p.dout, stream) != cudaSuccess) return KDA_ERR_CUDA;
         if (!mark(2)) return KDA_ERR_CUDA;

@@ -55,7 +55,7 @@ constexpr int TC_THREADS = 512;
 constexpr int TC_WARPS = TC_THREADS / 32;
 constexpr int LD = MMA_LD;                              // padded row length of the shared buffers
 constexpr int MAT = BT * LD;                            // floats per shared buffer
-constexpr int NVEC = 9;                                 // 128-float vectors in shared memory (+ the TMEM address)
+constexpr int NVEC = 17;                                // 128-float vectors in shared memory (+ the TMEM address)
 constexpr uint32_t TC_SMEM = (3u * MAT + NVEC * 128u) * 4u;
 constexpr float TC_RANGE = 60.f;                        // |exponent| bound of the factored operands
 
@@ -68,7 +68,9 @@ constexpr uint32_t TM_G = 0, TM_DQH = 128, TM_DKH = 256, TM_DKC = 384, TM_COLS =
 constexpr size_t SC_MAT = (size_t)BT * 128;
 
 // shared vectors
-enum : int { V_BETA = 0, V_PIV, V_GLAST, V_EXIT, V_DB, V_NQ, V_NK, V_TMP };
+enum : int { V_BETA = 0, V_PIV, V_GLAST, V_EXIT, V_UNUSED, V_NQ, V_NK, V_TMP, V_TSLOT,
+             V_DBP = 9,     // 4 vectors: dbeta partials of the four column-band warps (summed in a fixed order)
+             V_EXP = 13 };  // 4 vectors: exit-term column partials of the four row-band warps
 
 __device__ __forceinline__ float (&flat(float (&acc)[2][4][4]))[32] {
     return *reinterpret_cast<float(*)[32]>(&acc[0][0][0]);
@@ -240,8 +242,6 @@ __device__ void invert_unit_lower(float* L, int warp, int lane, int tid) {
     (void)tid;
 }
 
-__device__ __forceinline__ float bf16_at(const uint16_t* p, size_t i) { return __uint_as_float((uint32_t)p[i] << 16); }
-
 __device__ __forceinline__ void bf16x8(const uint4 u, float (&x)[8]) {
     x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
     x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xffff0000u);
@@ -288,7 +288,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
     float* vPiv = vec + V_PIV * 128;
     float* vGl = vec + V_GLAST * 128;
     float* vExit = vec + V_EXIT * 128;
-    float* vDb = vec + V_DB * 128;
     float* vNq = vec + V_NQ * 128;
     float* vNk = vec + V_NK * 128;
     float* vTmp = vec + V_TMP * 128;
@@ -299,7 +298,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
     auto S = [&](int m) { return sc + (size_t)m * SC_MAT; };
     const int ti0 = 32 * (warp >> 2), tj0 = 32 * (warp & 3);   // this warp's output tile
     const float scale = p.scale;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(vec + 8 * 128);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(vec + V_TSLOT * 128);
+    float* vDbP = vec + V_DBP * 128;   // [4][128]: [column band][row]
+    float* vExP = vec + V_EXP * 128;   // [4][128]: [row band][column]
     if (warp == 0) {
         tmem_alloc(smem_u32(tslot), TM_COLS);
         tmem_relinquish();
@@ -378,7 +379,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
             vTmp[tid] = acc - vPiv[tid];
             vExit[tid] = 0.f;
         }
-        if (tid >= KD && tid < 2 * KD) vDb[tid - KD] = 0.f;
         __syncthreads();
         // Range guard: the factors e^{+-(G-P)}, e^{P} and e^{G_last-P} must stay well
         // inside fp32; a chunk beyond that is left to the per-token kernel.
@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
                     float v = rsum[mi][hi];
                     v += __shfl_xor_sync(0xffffffffu, v, 1);
                     v += __shfl_xor_sync(0xffffffffu, v, 2);
-                    if ((lane & 3) == 0) atomicAdd(&vDb[ti0 + 16 * mi + 8 * hi + (lane >> 2)], v);
+                    if ((lane & 3) == 0) vDbP[(warp & 3) * 128 + ti0 + 16 * mi + 8 * hi + (lane >> 2)] = v;
                 }
         }
         stage(B0, S(SC_RHO), tid);
@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
                     float v = rsum[mi][hi];
                     v += __shfl_xor_sync(0xffffffffu, v, 1);
                     v += __shfl_xor_sync(0xffffffffu, v, 2);
-                    if ((lane & 3) == 0) atomicAdd(&vDb[ti0 + 16 * mi + 8 * hi + (lane >> 2)], v);
+                    if ((lane & 3) == 0) vDbP[(warp & 3) * 128 + ti0 + 16 * mi + 8 * hi + (lane >> 2)] += v;
                 }
         }
         // ---- dkc = rho Ze^T (+ later terms); exit term colsum(kc * rho Ze^T) ---------------
@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
                     v += __shfl_xor_sync(0xffffffffu, v, 4);
                     v += __shfl_xor_sync(0xffffffffu, v, 8);
                     v += __shfl_xor_sync(0xffffffffu, v, 16);
-                    if (lane < 4) atomicAdd(&vExit[tj0 + 8 * nj + 2 * lane + lo], v);
+                    if (lane < 4) vExP[(warp >> 2) * 128 + tj0 + 8 * nj + 2 * lane + lo] = v;
                 }
         }
         __syncthreads();
@@ -723,13 +723,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         }
         __syncthreads();
         if (tid < KD) {   // dg = reverse prefix sum over the valid rows, the exit terms at row n - 1
-            float acc1 = vExit[tid];
+            float acc1 = vExit[tid] + ((vExP[tid] + vExP[128 + tid]) + (vExP[256 + tid] + vExP[384 + tid]));
             for (int r = n - 1; r >= 0; --r) {
                 acc1 += B0[r * LD + tid];
                 B0[r * LD + tid] = acc1;
             }
         }
-        if (tid >= KD && tid < KD + BT && tid - KD < n) p.dbeta[row0 + (tid - KD) * rs] = vDb[tid - KD];
+        if (tid >= KD && tid < KD + BT && tid - KD < n) {
+            const int r = tid - KD;
+            p.dbeta[row0 + r * rs] = (vDbP[r] + vDbP[128 + r]) + (vDbP[256 + r] + vDbP[384 + r]);
+        }
         __syncthreads();
 #pragma unroll 4
         for (int i = tid; i < n * 32; i += TC_THREADS) {

@@ -26,6 +26,7 @@ extern "C" kda_status kda_fwd_noalloc(const void* q, const void* k, const void* 
                                       const float* beta, float scale, const float* h0,
                                       const int32_t* cu_seqlens, void* o, float* ht, int B, int T, int H, int K,
                                       int V, int N, unsigned flags, cudaStream_t stream) {
+    if (flags & KDA_FLAG_SAVE_FOR_BWD) return KDA_ERR_INVALID_ARG;   // the saved states need a caller workspace
     const size_t need = kda_fwd_workspace_bytes(B, T, H, K, V, N);
     if (need == 0) return (K != 128 || V != 128) ? KDA_ERR_UNSUPPORTED : KDA_ERR_INVALID_ARG;
     if (need > (size_t)KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_TOO_LARGE;

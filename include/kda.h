@@ -64,6 +64,21 @@ typedef enum {
  * the CUDA cores instead of in chunked form on the tensor cores. */
 #define KDA_FLAG_BWD_CHUNK_FP32 4u
 
+/* kda_fwd only (training): also store the fp32 state entering every chunk, so
+ * that a following kda_bwd on the same workspace with KDA_FLAG_BWD_REUSE_FWD
+ * can skip its forward replay.  Needs a workspace of at least
+ * kda_bwd_workspace_bytes(...) bytes; costs one extra write of the chunk
+ * states (64 KiB per 128 tokens and head). */
+#define KDA_FLAG_SAVE_FOR_BWD 8u
+
+/* kda_bwd only: the workspace holds what the last kda_fwd with
+ * KDA_FLAG_SAVE_FOR_BWD left in it (its tiles, flags and chunk states) for the
+ * very same inputs (q, k, v, g, beta, scale, h0, cu_seqlens, sizes, q/k norm
+ * flag), unchanged since: the backward skips its own forward replay.  The
+ * caller guarantees that; nothing is checked.  Not with
+ * KDA_FLAG_BWD_TOKEN_EXACT. */
+#define KDA_FLAG_BWD_REUSE_FWD 16u
+
 /*
  * Bytes of device workspace kda_fwd needs for these sizes (an upper bound
  * that covers both fixed-length and varlen packing).  0 on invalid sizes.
@@ -88,7 +103,7 @@ size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int N);
  *   o           bf16 [B, T, H, V]   output (written for every valid token)
  *   ht          fp32 [N, H, V, K] final state, or NULL to skip it
  *   B, T, H, K, V, N  sizes (K == V == 128)
- *   flags       0 or KDA_FLAG_QK_L2NORM
+ *   flags       0, KDA_FLAG_QK_L2NORM, KDA_FLAG_SAVE_FOR_BWD (or both)
  *   workspace   device scratch of at least kda_fwd_workspace_bytes(...)
  *               bytes, 256-byte aligned; its contents need not be
  *               initialised.  Two calls that share a workspace must not

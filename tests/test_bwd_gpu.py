@@ -199,3 +199,40 @@ def test_bwd_bad_cu_seqlens_reported():
     binding.kda_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], None, None, cu, gr["do"], gr["dht"], dq, dk, dv, dg,
                     dbeta, dh0, 2, 0, ws)
     assert binding.get_status(ws) == 4
+
+
+@pytest.mark.parametrize("varlen", [False, True])
+def test_bwd_reusing_saved_forward(varlen):
+    """Training path: a forward with save_for_backward leaves its tiles, flags
+    and chunk states in the workspace; the backward that reuses them skips its
+    forward replay and gives bit-identical gradients (the same kernels produce
+    the same chunk states), and the saving forward's output is unchanged."""
+    from chunked_gated_delta_kda_gb300 import binding
+    w = (custom("rv", B=1, T=640, H=2, seqlens=(300, 1, 339), with_h0=True, seed=23) if varlen
+         else custom("rf", B=2, T=384, H=2, with_h0=True, seed=24))
+    x = {kk: (vv.cuda() if isinstance(vv, torch.Tensor) else vv) for kk, vv in make_inputs(w).items()}
+    gr = {kk: (vv.cuda() if isinstance(vv, torch.Tensor) else vv) for kk, vv in make_grad_inputs(w).items()}
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"])
+    ws = torch.empty(binding.bwd_workspace_bytes(w.B, w.T, w.H, w.N), dtype=torch.uint8, device="cuda")
+    o_plain, ht_plain = binding.fwd(*args, initial_state=x["h0"], output_final_state=True, cu_seqlens=x["cu_seqlens"])
+    o, ht = binding.fwd(*args, initial_state=x["h0"], output_final_state=True, cu_seqlens=x["cu_seqlens"],
+                        workspace=ws, save_for_backward=True)
+    kw = dict(initial_state=x["h0"], dht=gr["dht"], cu_seqlens=x["cu_seqlens"])
+    reused = binding.bwd(*args, gr["do"], **kw, workspace=ws, reuse_forward=True)
+    fresh = binding.bwd(*args, gr["do"], **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_plain) and torch.equal(ht, ht_plain)
+    for a, b in zip(reused, fresh):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bwd_deterministic(path):
+    """Two runs give bit-identical gradients (fixed-order reductions, no float
+    atomics) on every path."""
+    w = custom("det", B=1, T=300, H=2, seqlens=(170, 130), with_h0=True, seed=25)
+    x = make_inputs(w)
+    gr = make_grad_inputs(w)
+    a, b = run_gpu(x, gr, path=path), run_gpu(x, gr, path=path)
+    for name, u, v in zip(NAMES, a, b):
+        assert np.array_equal(u, v), name

@@ -73,7 +73,9 @@ def test_host_validation_rejects_before_any_cuda_call():
     assert call(N=2) == 1                   # fixed length needs N == B
     assert call(B=2, N=2, cu=p) == 1        # varlen needs B == 1
     assert call(wsb=ws - 1) == 1            # workspace too small
-    assert call(flags=4) == 1               # unknown flag
+    assert call(flags=4) == 1               # unknown flag (a backward-only flag)
+    assert call(flags=8) == 1               # save for the backward: workspace below kda_bwd_workspace_bytes
+    assert lib.kda_fwd_noalloc(p, p, p, p, p, 0.0, None, None, p, None, 1, 256, 1, 128, 128, 1, 8, None) == 1
     assert call(H=0) == 1
     misaligned = ctypes.c_void_p(p.value + 8)
     assert call(o=misaligned) == 1          # 16-byte alignment
@@ -181,8 +183,9 @@ def test_bwd_workspace_and_host_checks():
     assert call(N=2) == 1
     assert call(B=2, N=2, cu=p) == 1
     assert call(wsb=ws - 1) == 1
-    assert call(flags=8) == 1
-    assert call(flags=16) == 1
+    assert call(flags=8) == 1                # the forward's save flag
+    assert call(flags=32) == 1
+    assert call(flags=16 | 2) == 1           # reusing a saved forward is not for the token path
     misaligned = ctypes.c_void_p(p.value + 8)
     assert call(dq=misaligned) == 1
     assert call(dh0=misaligned) == 1
