@@ -23,21 +23,22 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// acc (a 32 x 32 tile at rows i0, cols j0) += opA(i0.., 0..kd) opB(0..kd, j0..) with
-// opA(i, l) = TA ? A[l][i] : A[i][l] and opB(l, j) = TB ? B[j][l] : B[l][j], shared
-// buffers of row length MMA_LD.  Fragment layouts of m16n8k8 (g = lane / 4, t = lane % 4):
-// A: (g, t) (g+8, t) (g, t+4) (g+8, t+4); B: (t, g) (t+4, g); D: (g, 2t) (g, 2t+1) (g+8, 2t) (g+8, 2t+1).
-template <bool TA, bool TB>
+// acc (a (16 MI) x 32 tile at rows i0, cols j0) += opA(i0.., 0..kd) opB(0..kd, j0..)
+// with opA(i, l) = TA ? A[l][i] : A[i][l] and opB(l, j) = TB ? B[j][l] : B[l][j],
+// shared buffers of row length MMA_LD.  Fragment layouts of m16n8k8
+// (g = lane / 4, t = lane % 4): A: (g, t) (g+8, t) (g, t+4) (g+8, t+4);
+// B: (t, g) (t+4, g); D: (g, 2t) (g, 2t+1) (g+8, 2t) (g+8, 2t+1).
+template <bool TA, bool TB, int MI>
 __device__ __forceinline__ void tile_mm(const float* A, const float* B, int i0, int j0, int kd, int lane,
-                                        float (&acc)[2][4][4]) {
+                                        float (&acc)[MI][4][4]) {
     const int g = lane >> 2, t = lane & 3;
     auto opA = [&](int i, int l) { return TA ? A[l * MMA_LD + i] : A[i * MMA_LD + l]; };
     auto opB = [&](int l, int j) { return TB ? B[j * MMA_LD + l] : B[l * MMA_LD + j]; };
 #pragma unroll 2
     for (int k0 = 0; k0 < kd; k0 += 8) {
-        uint32_t a[2][4], b[4][2];
+        uint32_t a[MI][4], b[4][2];
 #pragma unroll
-        for (int mi = 0; mi < 2; ++mi) {
+        for (int mi = 0; mi < MI; ++mi) {
             const int r = i0 + 16 * mi + g;
             a[mi][0] = to_tf32(opA(r, k0 + t));
             a[mi][1] = to_tf32(opA(r + 8, k0 + t));
@@ -51,7 +52,7 @@ __device__ __forceinline__ void tile_mm(const float* A, const float* B, int i0, 
             b[nj][1] = to_tf32(opB(k0 + t + 4, c));
         }
 #pragma unroll
-        for (int mi = 0; mi < 2; ++mi)
+        for (int mi = 0; mi < MI; ++mi)
 #pragma unroll
             for (int nj = 0; nj < 4; ++nj) mma_tf32(acc[mi][nj], a[mi], b[nj]);
     }
