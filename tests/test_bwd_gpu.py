@@ -236,3 +236,26 @@ def test_bwd_deterministic(path):
     a, b = run_gpu(x, gr, path=path), run_gpu(x, gr, path=path)
     for name, u, v in zip(NAMES, a, b):
         assert np.array_equal(u, v), name
+
+
+@pytest.mark.parametrize("case", ["scale_0.3_b3", "l2norm_fixed_h4", "h8_dht_only"])
+def test_bwd_more_configurations(case):
+    """A non-default scale with three fixed-length sequences; the q/k
+    normalisation with fixed-length packing; eight heads with dht and no h0."""
+    if case == "scale_0.3_b3":
+        w, l2 = custom("s3", B=3, T=256, H=2, with_h0=True, seed=26), False
+    elif case == "l2norm_fixed_h4":
+        w, l2 = custom("l4", B=1, T=256, H=4, with_h0=True, seed=27), True
+    else:
+        w, l2 = custom("h8", B=1, T=256, H=8, seed=28), False
+    x = make_inputs(w)
+    if case == "scale_0.3_b3":
+        x["scale"] = 0.3
+    if l2:
+        gen = torch.Generator().manual_seed(9)
+        for n in ("q", "k"):
+            x[n] = (x[n].float() * (0.5 + 2 * torch.rand(x[n].shape[:3] + (1,), generator=gen))).bfloat16()
+    gr = make_grad_inputs(w)
+    ref = run_ref(x, gr, l2norm=l2)
+    for path in PATHS:
+        print(case, path, check(run_gpu(x, gr, l2norm=l2, path=path), ref, path))
