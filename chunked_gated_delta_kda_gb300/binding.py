@@ -27,6 +27,7 @@ KDA_FLAG_BWD_TOKEN_EXACT = 2
 KDA_FLAG_BWD_CHUNK_FP32 = 4
 KDA_FLAG_SAVE_FOR_BWD = 8
 KDA_FLAG_BWD_REUSE_FWD = 16
+KDA_FLAG_BWD_UMMA = 32
 
 _STATUS = {
     0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
@@ -358,14 +359,15 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
         do: torch.Tensor, scale: Optional[float] = None, initial_state: Optional[torch.Tensor] = None,
         dht: Optional[torch.Tensor] = None, use_qk_l2norm_in_kernel: bool = False,
         cu_seqlens: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-        token_exact: bool = False, chunk_fp32: bool = False, reuse_forward: bool = False):
+        token_exact: bool = False, chunk_fp32: bool = False, reuse_forward: bool = False, umma: bool = False):
     """KDA backward of ``fwd`` with the same arguments: the gradients of
     <do, o> + <dht, ht>.  do: bf16 [B,T,H,V]; dht: fp32 [N,H,V,K] or None.
     ``token_exact`` selects the token-by-token backward for every unit;
     ``chunk_fp32`` the per-token fp32 chain rule inside every chunk (instead
     of the chunked form on the tensor cores); ``reuse_forward`` skips the
     forward replay, using what ``fwd(..., save_for_backward=True)`` left in
-    ``workspace`` for the same inputs.
+    ``workspace`` for the same inputs; ``umma`` the per-chunk chain rule on
+    tcgen05 products instead of the warp-level TF32 ones.
     Returns fp32 (dq, dk, dv, dg, dbeta, dh0) with the shapes of q, k, v, g,
     beta and the state [N,H,V,K]."""
     for name, t, dt, nd in (("q", q, torch.bfloat16, 4), ("k", k, torch.bfloat16, 4), ("v", v, torch.bfloat16, 4),
@@ -402,7 +404,8 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
             raise ValueError("reuse_forward needs the workspace the saving forward used")
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     flags = ((KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0) | (KDA_FLAG_BWD_TOKEN_EXACT if token_exact else 0)
-             | (KDA_FLAG_BWD_CHUNK_FP32 if chunk_fp32 else 0) | (KDA_FLAG_BWD_REUSE_FWD if reuse_forward else 0))
+             | (KDA_FLAG_BWD_CHUNK_FP32 if chunk_fp32 else 0) | (KDA_FLAG_BWD_REUSE_FWD if reuse_forward else 0)
+             | (KDA_FLAG_BWD_UMMA if umma else 0))
     with torch.cuda.device(dev):
         kda_bwd(q, k, v, g, beta, scale, h0, cu_seqlens, do, dht, dq, dk, dv, dg, dbeta, dh0, N, flags, workspace)
     return dq, dk, dv, dg, dbeta, dh0

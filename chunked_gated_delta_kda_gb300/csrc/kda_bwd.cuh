@@ -39,6 +39,7 @@ struct FwdParams;
 cudaError_t launch_bwd_tiles(const FwdParams& fp, uint8_t* btiles, const uint16_t* dout, cudaStream_t stream);
 cudaError_t launch_bwd_chunk(const BwdParams& p, const FwdParams& fp, int ctas, cudaStream_t stream);
 cudaError_t launch_bwd_tc(const BwdParams& p, const FwdParams& fp, int ctas, cudaStream_t stream);
+cudaError_t launch_bwd_umma(const BwdParams& p, const FwdParams& fp, int ctas, cudaStream_t stream);
 cudaError_t launch_bwd_exact(const BwdParams& p, const uint32_t* only, int ctas, cudaStream_t stream);
 cudaError_t launch_l2norm_bwd(const BwdParams& p, long long rows, cudaStream_t stream);
 

@@ -92,7 +92,7 @@ static kda_status bwd_impl(const void* q, const void* k, const void* v, const fl
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return KDA_ERR_INVALID_ARG;
     if (B < 1 || T < 0 || H < 1 || N < 1 || H > 65535 || N > 65535) return KDA_ERR_INVALID_ARG;
     if ((flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_BWD_TOKEN_EXACT | KDA_FLAG_BWD_CHUNK_FP32 |
-                   KDA_FLAG_BWD_REUSE_FWD)) != 0u)
+                   KDA_FLAG_BWD_REUSE_FWD | KDA_FLAG_BWD_UMMA)) != 0u)
         return KDA_ERR_INVALID_ARG;
     const bool reuse = (flags & KDA_FLAG_BWD_REUSE_FWD) != 0u;
     if (reuse && (flags & KDA_FLAG_BWD_TOKEN_EXACT)) return KDA_ERR_INVALID_ARG;
@@ -200,7 +200,9 @@ static kda_status bwd_impl(const void* q, const void* k, const void* v, const fl
             kda::BwdParams tp = p;
             tp.tc_skip = reinterpret_cast<uint32_t*>(ws + L.skip);
             if (cudaMemsetAsync(tp.tc_skip, 0, (size_t)items * 4, stream) != cudaSuccess) return KDA_ERR_CUDA;
-            if (kda::launch_bwd_tc(tp, fp, ctas, stream) != cudaSuccess) return KDA_ERR_CUDA;
+            const cudaError_t e = (flags & KDA_FLAG_BWD_UMMA) ? kda::launch_bwd_umma(tp, fp, ctas, stream)
+                                                               : kda::launch_bwd_tc(tp, fp, ctas, stream);
+            if (e != cudaSuccess) return KDA_ERR_CUDA;
             if (kda::launch_bwd_chunk(tp, fp, ctas, stream) != cudaSuccess) return KDA_ERR_CUDA;
         }
         if (!mark(4)) return KDA_ERR_CUDA;

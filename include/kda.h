@@ -79,6 +79,13 @@ typedef enum {
  * KDA_FLAG_BWD_TOKEN_EXACT. */
 #define KDA_FLAG_BWD_REUSE_FWD 16u
 
+/* kda_bwd only: evaluate the per-chunk chain rule with tcgen05 kind::tf32
+ * products (operands staged K-major in shared memory, accumulators in TMEM)
+ * instead of the default warp-level TF32 products.  Same results within the
+ * backward's tolerance; slower on GB300 (its operand staging and transposes
+ * are serialised with the products), kept as an alternative. */
+#define KDA_FLAG_BWD_UMMA 32u
+
 /*
  * Bytes of device workspace kda_fwd needs for these sizes (an upper bound
  * that covers both fixed-length and varlen packing).  0 on invalid sizes.

@@ -2,7 +2,7 @@
 against the fp64 gradient oracle (``oracle.backward``: torch autograd through
 the per-token recurrence, pinned in ``test_oracle_backward.py``).
 
-Three paths are checked.  The token-by-token path evaluates the chain rule in
+Four paths are checked.  The token-by-token path evaluates the chain rule in
 fp32 from the same bf16 inputs, so its error is fp32 rounding accumulated
 along the sequence (the state recurrence is contracting for g <= 0,
 0 <= beta <= 1 and unit k): bound |d - d_ref| <= 1e-3 (|d_ref| + rms(d_ref))
@@ -12,8 +12,8 @@ carries (fp16 operands, fp32 accumulation: ~1e-3 relative, the forward's own
 state tolerance) and carries the state gradient with the same products, so
 its bound is ten times wider, 1e-2 (|d_ref| + rms(d_ref)), the forward's
 tolerance on o.  That holds both for the chunked form of the per-chunk chain
-rule (TF32 tensor-core products) and for its per-token fp32 evaluation
-(``chunk_fp32``).  Inputs: ``inputs.make_inputs`` and ``inputs.make_grad_inputs``.
+rule (TF32 tensor-core products: warp-level by default, tcgen05 with
+``umma``) and for its per-token fp32 evaluation (``chunk_fp32``).  Inputs: ``inputs.make_inputs`` and ``inputs.make_grad_inputs``.
 """
 
 import numpy as np
@@ -26,7 +26,7 @@ from oracle import backward as obw
 
 pytestmark = pytest.mark.gpu
 
-G_RTOL = {"token": 1e-3, "chunk": 1e-2, "chunk_fp32": 1e-2}
+G_RTOL = {"token": 1e-3, "chunk": 1e-2, "chunk_umma": 1e-2, "chunk_fp32": 1e-2}
 NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
 
 
@@ -35,7 +35,8 @@ def run_gpu(x, gr, l2norm=False, path="chunk"):
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in {**x, **gr}.items()}
     out = binding.bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["do"], scale=d.get("scale"),
                       initial_state=d["h0"], dht=d["dht"], use_qk_l2norm_in_kernel=l2norm,
-                      cu_seqlens=d["cu_seqlens"], token_exact=(path == "token"), chunk_fp32=(path == "chunk_fp32"))
+                      cu_seqlens=d["cu_seqlens"], token_exact=(path == "token"), chunk_fp32=(path == "chunk_fp32"),
+                      umma=(path == "chunk_umma"))
     torch.cuda.synchronize()
     return [to_np(t).astype(np.float64) for t in out]
 
@@ -71,7 +72,7 @@ CASES = {
 }
 
 
-PATHS = ["chunk", "chunk_fp32", "token"]
+PATHS = ["chunk", "chunk_umma", "chunk_fp32", "token"]
 
 
 @pytest.mark.parametrize("case", list(CASES))
@@ -138,7 +139,9 @@ def test_bwd_decay_paths(gate_div, expect_tc):
     paths = _chunk_paths(x, 256, 2)
     assert all(skip != expect_tc and not exact for skip, exact in paths), paths
     gr = make_grad_inputs(w)
-    print(gate_div, check(run_gpu(x, gr), run_ref(x, gr), "chunk"))
+    ref = run_ref(x, gr)
+    for path in ("chunk", "chunk_umma"):
+        print(gate_div, path, check(run_gpu(x, gr, path=path), ref, path))
 
 
 def test_bwd_full_size_against_token_path():

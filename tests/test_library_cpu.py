@@ -184,7 +184,7 @@ def test_bwd_workspace_and_host_checks():
     assert call(B=2, N=2, cu=p) == 1
     assert call(wsb=ws - 1) == 1
     assert call(flags=8) == 1                # the forward's save flag
-    assert call(flags=32) == 1
+    assert call(flags=64) == 1
     assert call(flags=16 | 2) == 1           # reusing a saved forward is not for the token path
     misaligned = ctypes.c_void_p(p.value + 8)
     assert call(dq=misaligned) == 1
