@@ -260,9 +260,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
         }
     } else if (warp == 8) {
         // ------------------------------------------------------------------
-        // MMA issue (one thread): Nm S(j), then Qe S(j - 1).
+        // MMA issue (the whole warp computes the operands, one elected lane
+        // issues): Nm S(j), then Qe S(j - 1).
         // ------------------------------------------------------------------
-        if (lane == 0) {
+        {
             const uint32_t id = idesc_f16(T_F16, 128, BV, false, true);
             // per k-step only the start-address field of these advances
             const uint64_t a_nm0 = smem_desc(sbase + ST_NM, 16u, 1024u, SW_128B);
@@ -274,27 +275,29 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
                     const int s = j & 1;
                     wait(full(s), (uint32_t)(j >> 1) & 1u);
                     if (j >= 1) wait(s16rdy, (uint32_t)(j - 1) & 1u);
+                    __syncwarp();   // reconverge (the waits are bounded) before elect.sync
                     tc_fence_after();
                     const uint64_t a_nm = s ? a_nm1 : a_nm0;
                     const uint64_t b_s = smem_desc(sbase + s16buf(j), 512u, 512u, SW_64B);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)   // critical chain: Nm S -> cols [0,32)
-                        mma_f16(tmem, a_nm + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), b_s + (uint64_t)(ks * 64),
+                        mma_f16_warp(tmem, a_nm + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2), b_s + (uint64_t)(ks * 64),
                                 id, ks > 0);
-                    mma_commit(mmas);
+                    mma_commit_warp(mmas);
                 }
                 if (j >= 1 && p.o != nullptr) {
                     const int c = j - 1, b = c & 1;
                     wait(qfull(b), (uint32_t)(c >> 1) & 1u);
                     if (c >= 2) wait(ofree(b), (uint32_t)((c - 2) >> 1) & 1u);
+                    __syncwarp();
                     tc_fence_after();
                     const uint64_t a_qe = b ? a_qe1 : a_qe0;
                     const uint64_t b_s = smem_desc(sbase + s16buf(c), 512u, 512u, SW_64B);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)   // output product Qe S(c) -> buffer b
-                        mma_f16(tmem + 32u + 32u * (uint32_t)b, a_qe + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
+                        mma_f16_warp(tmem + 32u + 32u * (uint32_t)b, a_qe + (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2),
                                 b_s + (uint64_t)(ks * 64), id, ks > 0);
-                    mma_commit(mmao(b));
+                    mma_commit_warp(mmao(b));
                 }
             }
         }

@@ -174,6 +174,28 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
+// The same two operations executed by a whole converged warp: the operands
+// are computed warp-uniformly and one lane, picked by elect.sync (the same
+// lane for the same full mask), issues the instruction.  Measured on GB300:
+// ~30% less issue time per M=128, N=32 MMA than a single-thread branch.
+__device__ __forceinline__ void mma_f16_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05: TMEM -> registers.  Warp w of a warpgroup reads lanes 32*(w%4)..+31;
 // thread i of the warp gets lane 32*(w%4)+i, columns col..col+N-1.
