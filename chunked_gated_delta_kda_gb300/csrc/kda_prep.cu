@@ -72,6 +72,7 @@ constexpr uint32_t M_EP = RM + 2560;       // f32[128]  exp(P)          (fast)
 constexpr uint32_t M_CL = RM + 3072;       // f32[128]  exp(G_last - P) (fast)
 constexpr uint32_t M_TOT = RM + 3584;      // f32[8][128] row-block sums (wide)
 constexpr uint32_t M_BAR = RM + 7680;      // mbarrier
+constexpr uint32_t M_BAR2 = RM + 7688;     // mbarrier of the second transition product
 constexpr uint32_t M_TMEM = RM + 7744;     // TMEM base address
 constexpr uint32_t M_FLAG = RM + 7748;     // failure flag
 constexpr uint32_t SMEM_USED = RM + 7808;
@@ -357,6 +358,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     float* Wd = reinterpret_cast<float*>(sm + W_DIAG);
     float* Wt = reinterpret_cast<float*>(sm + W_TMP);
     const uint32_t bar = sbase + M_BAR;
+    const uint32_t bar2 = sbase + M_BAR2;
+    uint32_t phase2 = 0;
     volatile uint32_t* sFlag = reinterpret_cast<volatile uint32_t*>(sm + M_FLAG);
     uint32_t phase = 0;
 
@@ -372,6 +375,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     }
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(bar2, 1);
         fence_mbar_init();
         *sFlag = 0;
     }
@@ -941,15 +945,17 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             sync_for_mma();
 
             // --------------------------------------------------------------
-            // Phase 6: [X^T w | X^T u] -> [0,256) with X = R (fast) or kg
-            // (wide);  [A2 w | A2 u] -> [256,512)
+            // Phase 6: [A2 w | A2 u] -> [256,512), then [X^T w | X^T u] ->
+            // [0,256) with X = R (fast) or kg (wide).  Separate commits: the
+            // epilogue of the first runs while the second computes.
             // --------------------------------------------------------------
             if (tid == 0) {
                 const Operand KgT{sbase + MP::KGT, true, 128}, A2h{sbase + RW, false, 128},
                     WU{sbase + MP::WU, true, 128};
-                mma_128(tmem + 0, KgT, WU, idesc_f16(T_F16, 128, 256, true, true), 8);
                 mma_128(tmem + 256, A2h, WU, idesc_f16(T_F16, 128, 256, false, true), 8);
                 mma_commit(bar);
+                mma_128(tmem + 0, KgT, WU, idesc_f16(T_F16, 128, 256, true, true), 8);
+                mma_commit(bar2);
             }
             wait_mma();
 
@@ -970,6 +976,11 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 const float rs = FAST ? sCL[trow] : 1.f;   // rows d of Nm / Bc
 #pragma unroll 1
                 for (int part = 0; part < 4; ++part) {
+                    if (part == 2) {   // Nm | Bc: the second product
+                        if (!mbar_wait(bar2, phase2, WAIT_LIMIT)) *sFlag = 1;
+                        phase2 ^= 1;
+                        tc_fence_after();
+                    }
                     float x[32];
                     int kind, vt;
                     if (part < 2) {
