@@ -392,6 +392,40 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     };
 
 
+    // fast variant: a chunk's beta, gate rows and first k / q / v row are
+    // loaded at the end of the previous chunk, before its tile stores are
+    // queued, so that the read requests leave the SM ahead of 128 KB of
+    // store data
+    float4 gpre[4][2];
+    uint4 kpre = make_uint4(0u, 0u, 0u, 0u), qpre = kpre, vpre = kpre;
+    float bpre = 0.f;
+    auto load_rows = [&](const ChunkRef& cc, int hh) {
+        const int d8 = (tid & 15) * 8;
+        const int tg0 = (tid >> 4) * 4;
+        const size_t r0 = (size_t)cc.tok0 * H + hh;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int t = tg0 + r;
+            gpre[r][0] = gpre[r][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < cc.len) {
+                const size_t off = (r0 + (size_t)t * H) * KD + d8;
+                gpre[r][0] = __ldg(reinterpret_cast<const float4*>(p.g + off));
+                gpre[r][1] = __ldg(reinterpret_cast<const float4*>(p.g + off + 4));
+            }
+        }
+        kpre = qpre = vpre = make_uint4(0u, 0u, 0u, 0u);
+        if (tg0 < cc.len) {
+            const size_t off = (r0 + (size_t)tg0 * H) * KD + d8;
+            kpre = __ldg(reinterpret_cast<const uint4*>(p.k + off));
+            qpre = __ldg(reinterpret_cast<const uint4*>(p.q + off));
+            vpre = __ldg(reinterpret_cast<const uint4*>(p.v + off));
+        }
+        bpre = (tid < BT && tid < cc.len) ? __ldg(p.beta + r0 + (size_t)tid * H) : 0.f;
+    };
+    ChunkRef none{};   // zero rows: loads nothing, defines the registers
+    none.len = 0;
+    if (FAST) load_rows(c, h);
+
     while (have && *sFlag == 0) {
         long long nidx = idx + gridDim.x, nitem = 0;
         ChunkRef cn;
@@ -405,7 +439,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
         // L2 normalisation x / sqrt(sum x^2 + 1e-6)).
         // ------------------------------------------------------------------
         if (tid < BT) {
-            sBeta[tid] = tid < len ? __ldg(p.beta + row0 + (size_t)tid * H) : 0.f;
+            sBeta[tid] = FAST ? bpre : (tid < len ? __ldg(p.beta + row0 + (size_t)tid * H) : 0.f);
             if (!L2NORM) {
                 sInvQ[tid] = p.scale;
                 sInvK[tid] = 1.f;
@@ -451,21 +485,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             // k, q, v rows are loaded one row ahead of their use (row 0 with
             // the gate), so each row's loads are in flight before the
             // previous row's shared-memory stores.
-            uint4 kn = make_uint4(0u, 0u, 0u, 0u), qn = kn, vn = kn;
+            uint4 kn = kpre, qn = qpre, vn = vpre;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-                const int t = tg0 + r;
-                float4 ga = make_float4(0.f, 0.f, 0.f, 0.f), gb = ga;
-                if (t < len) {
-                    const size_t off = (row0 + (size_t)t * H) * KD + d8;
-                    ga = __ldg(reinterpret_cast<const float4*>(p.g + off));
-                    gb = __ldg(reinterpret_cast<const float4*>(p.g + off + 4));
-                    if (r == 0) {
-                        kn = __ldg(reinterpret_cast<const uint4*>(p.k + off));
-                        qn = __ldg(reinterpret_cast<const uint4*>(p.q + off));
-                        vn = __ldg(reinterpret_cast<const uint4*>(p.v + off));
-                    }
-                }
+                const float4 ga = gpre[r][0], gb = gpre[r][1];
                 G[r][0] = ga.x; G[r][1] = ga.y; G[r][2] = ga.z; G[r][3] = ga.w;
                 G[r][4] = gb.x; G[r][5] = gb.y; G[r][6] = gb.z; G[r][7] = gb.w;
             }
@@ -690,6 +713,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 p.wide_list[slot_i] = (int32_t)item;
             }
             if (have_n) prefetch_chunk(p, cn, hn, tid);
+            if (FAST) load_rows(have_n ? cn : none, hn);
             __syncthreads();
         } else {
             if (tid == 0) {
@@ -1042,6 +1066,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                     dg.w = ex2(sGL[tid * 4 + 3]);
                     *reinterpret_cast<float4*>(dst + TILE_DG + tid * 16) = dg;
                 }
+                if (FAST) load_rows(have_n ? cn : none, hn);   // ahead of the tile stores
                 fence_async_smem();
                 tc_fence_before();
                 __syncthreads();
