@@ -39,14 +39,15 @@ namespace {
 // ---------------------------------------------------------------------------
 // Transposed tiles
 // ---------------------------------------------------------------------------
-constexpr int BT_THREADS = 512;
-constexpr int QF_LD = MMA_LD;                        // padded fp32 rows
-constexpr uint32_t BT_SMEM = 2u * BT * QF_LD * 4u;   // Qe (fp32) and do (fp32)
+constexpr int BT_THREADS = 256;
+// Shared memory (1024-aligned): the forward's Qe tile as stored (fp16, 128-byte
+// swizzled [t][d]: the MN-major A operand of Qe^T), the raw Nm tile, do as fp16
+// in the same layout (the MN-major B operand), then barriers and scratch.
+constexpr uint32_t BTS_QE = 0, BTS_NM = 32768, BTS_DO = 65536, BTS_MISC = 98304;
+constexpr uint32_t BTS_BAR_TX = BTS_MISC, BTS_BAR_MMA = BTS_MISC + 8, BTS_TMEM = BTS_MISC + 16,
+                   BTS_MAX = BTS_MISC + 32;   // f32[8]: per-warp max |do|
+constexpr uint32_t BT_SMEM = BTS_MISC + 64 + 1024;
 
-__device__ __forceinline__ float2 h2f(uint32_t u) {
-    __half2 h = *reinterpret_cast<__half2*>(&u);
-    return __half22float2(h);
-}
 __device__ __forceinline__ uint32_t f2h(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -54,90 +55,144 @@ __device__ __forceinline__ uint32_t f2h(float a, float b) {
 
 }  // namespace
 
-// One CTA per (chunk slot, head): writes, at the mirrored chunk position of
-// the same sequence, the tile the reverse state pass reads: Nm^T (same fp16
-// 128-byte-swizzled layout as Nm), Qe^T do as the four fp16 Bc pieces, Dg.
-__global__ void __launch_bounds__(BT_THREADS) kda_bwd_tiles_kernel(const FwdParams fp, uint8_t* btiles,
-                                                                   const uint16_t* __restrict__ dout) {
-    extern __shared__ __align__(16) float bsm[];
-    float* qf = bsm;                   // Qe[t][d], fp32
-    float* df = bsm + BT * QF_LD;      // do[t][v], fp32 (first: raw Nm bytes)
+// One CTA per (chunk slot, head), two CTAs per SM: writes, at the mirrored
+// chunk position of the same sequence, the tile the reverse state pass reads:
+// Nm^T (same fp16 128-byte-swizzled layout as Nm), Qe^T do as the four fp16
+// Bc pieces, Dg.  Qe^T do is one M=128 N=128 K=128 tcgen05 product (fp16
+// operands, fp32 accumulation in TMEM).  do enters as fp16 scaled by a power
+// of two, 2^s with s from the chunk's largest |do|, so that the bf16 -> fp16
+// conversion is exact in range; the accumulator is multiplied by 2^-s.
+__global__ void __launch_bounds__(BT_THREADS, 2) kda_bwd_tiles_kernel(const FwdParams fp, uint8_t* btiles,
+                                                                      const uint16_t* __restrict__ dout) {
+    extern __shared__ uint8_t bsm_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(bsm_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(sm);
     const int slot = (int)blockIdx.x, h = (int)blockIdx.y;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = fp.H;
     ChunkRef c;
-    if (!slot_chunk(fp, slot, c)) return;
+    if (!slot_chunk(fp, slot, c)) return;   // uniform
     long long bos;
     int len;
     if (!seq_bounds(fp, c.n, bos, len)) return;
     const int nch = (len + BT - 1) / BT;
     const uint8_t* src = tile_ptr(fp, slot, h);
     uint8_t* dst = btiles + ((size_t)chunk_slot(fp, c.n, nch - 1 - c.j) * H + h) * TILE_BYTES;
+    const uint32_t bar_tx = sbase + BTS_BAR_TX, bar_mma = sbase + BTS_BAR_MMA;
+    float* wmax = reinterpret_cast<float*>(sm + BTS_MAX);
 
-    // Nm^T: stage the raw tile, then write (d, e) <- Nm(e, d) in 16-byte runs
-    uint8_t* raw = reinterpret_cast<uint8_t*>(df);
-    for (int i = tid; i < KD * KD * 2 / 16; i += BT_THREADS)
-        reinterpret_cast<uint4*>(raw)[i] = reinterpret_cast<const uint4*>(src + TILE_NM)[i];
+    if (tid == 0) {
+        mbar_init(bar_tx, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(sbase + BTS_TMEM, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + BTS_TMEM);
+    if (tid == 0) {   // the forward's Nm and Qe tiles, as stored
+        mbar_arrive_expect_tx(bar_tx, 65536u);
+        bulk_g2s(sbase + BTS_NM, src + TILE_NM, 32768u, bar_tx);
+        bulk_g2s(sbase + BTS_QE, src + TILE_QE, 32768u, bar_tx);
+    }
     if (tid < KD / 4)
         reinterpret_cast<float4*>(dst + TILE_DG)[tid] = reinterpret_cast<const float4*>(src + TILE_DG)[tid];
-    __syncthreads();
-    for (int i = tid; i < KD * KD / 8; i += BT_THREADS) {
-        const int d = i >> 4, e0 = (i & 15) * 8;
-        uint16_t x[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = *reinterpret_cast<const uint16_t*>(raw + sw128_off(e0 + u, d, 128));
-        *reinterpret_cast<uint4*>(dst + TILE_NM + sw128_off(d, e0, 128)) =
-            make_uint4(x[0] | ((uint32_t)x[1] << 16), x[2] | ((uint32_t)x[3] << 16), x[4] | ((uint32_t)x[5] << 16),
-                       x[6] | ((uint32_t)x[7] << 16));
-    }
-    __syncthreads();
 
-    // Qe and do of the chunk's valid rows, fp32
-    for (int i = tid; i < BT * KD / 8; i += BT_THREADS) {
-        const int t = i >> 4, c8 = (i & 15) * 8;
-        float qv[8], dv[8];
-        if (t < c.len) {
-            const uint4 a = *reinterpret_cast<const uint4*>(src + TILE_QE + sw128_off(t, c8, 128));
-            const float2 a0 = h2f(a.x), a1 = h2f(a.y), a2 = h2f(a.z), a3 = h2f(a.w);
-            qv[0] = a0.x; qv[1] = a0.y; qv[2] = a1.x; qv[3] = a1.y; qv[4] = a2.x; qv[5] = a2.y; qv[6] = a3.x; qv[7] = a3.y;
-            const uint4 b = *reinterpret_cast<const uint4*>(dout + ((size_t)(c.tok0 + t) * H + h) * VD + c8);
-            dv[0] = __uint_as_float(b.x << 16); dv[1] = __uint_as_float(b.x & 0xffff0000u);
-            dv[2] = __uint_as_float(b.y << 16); dv[3] = __uint_as_float(b.y & 0xffff0000u);
-            dv[4] = __uint_as_float(b.z << 16); dv[5] = __uint_as_float(b.z & 0xffff0000u);
-            dv[6] = __uint_as_float(b.w << 16); dv[7] = __uint_as_float(b.w & 0xffff0000u);
-        } else {
+    // do of the chunk's rows: 8 pieces of 8 values per thread (rows past the
+    // chunk's length are zero), and the chunk's largest |do|
+    uint4 dr[8];
+    float m = 0.f;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) qv[u] = dv[u] = 0.f;
-        }
-        float4* qd = reinterpret_cast<float4*>(qf + t * QF_LD + c8);
-        float4* dd = reinterpret_cast<float4*>(df + t * QF_LD + c8);
-        qd[0] = make_float4(qv[0], qv[1], qv[2], qv[3]);
-        qd[1] = make_float4(qv[4], qv[5], qv[6], qv[7]);
-        dd[0] = make_float4(dv[0], dv[1], dv[2], dv[3]);
-        dd[1] = make_float4(dv[4], dv[5], dv[6], dv[7]);
+    for (int u = 0; u < 8; ++u) {
+        const int i = tid + u * BT_THREADS, t = i >> 4, c8 = (i & 15) * 8;
+        dr[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (t < c.len) dr[u] = *reinterpret_cast<const uint4*>(dout + ((size_t)(c.tok0 + t) * H + h) * VD + c8);
+        const uint32_t w4[4] = {dr[u].x, dr[u].y, dr[u].z, dr[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)   // |x| of the two bf16 halves as fp32 bit patterns
+            m = fmaxf(m, fmaxf(__uint_as_float((w4[e] << 16) & 0x7fff0000u), __uint_as_float(w4[e] & 0x7fff0000u)));
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) wmax[warp] = m;
     __syncthreads();
+    m = wmax[0];
+#pragma unroll
+    for (int w = 1; w < BT_THREADS / 32; ++w) m = fmaxf(m, wmax[w]);
+    // 2^s brings the largest |do| into [2^13, 2^14); |s| <= 126 keeps 2^s and 2^-s normal
+    int s = 0;
+    if (m > 0.f && m <= 3.0e38f) s = 13 - (int)((__float_as_uint(m) >> 23) & 0xffu) + 127;
+    s = s < -126 ? -126 : (s > 126 ? 126 : s);
+    const float up = __uint_as_float((uint32_t)(s + 127) << 23), down = __uint_as_float((uint32_t)(127 - s) << 23);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int i = tid + u * BT_THREADS, t = i >> 4, c8 = (i & 15) * 8;
+        const uint32_t w4[4] = {dr[u].x, dr[u].y, dr[u].z, dr[u].w};
+        uint32_t o4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            o4[e] = f2h(__uint_as_float(w4[e] << 16) * up, __uint_as_float(w4[e] & 0xffff0000u) * up);
+        *reinterpret_cast<uint4*>(sm + BTS_DO + sw128_off(t, c8, 128)) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+    }
+    fence_async_smem();
+    const bool tx_done = __syncthreads_and(mbar_wait(bar_tx, 0, WAIT_LIMIT)) != 0;
+    tc_fence_after();
+    bool ok = tx_done;
+    if (ok && warp == 0) {   // Bq[d][v] = sum_t Qe[t][d] do[t][v]: both operands MN-major, K = t
+        const uint64_t da = smem_desc(sbase + BTS_QE, 16384u, 1024u, SW_128B);
+        const uint64_t db = smem_desc(sbase + BTS_DO, 16384u, 1024u, SW_128B);
+        const uint32_t id = idesc_f16(T_F16, 128, 128, true, true);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_f16_warp(tmem, da + (uint64_t)ks * 128u, db + (uint64_t)ks * 128u, id, ks > 0);
+        mma_commit_warp(bar_mma);
+    }
 
-    // Bq[d][v] = sum_t Qe[t][d] do[t][v] on the tensor cores (TF32, fp32 accumulation):
-    // warp w computes the 32 x 32 tile at d = 32 (w / 4), v = 32 (w % 4)
-    const int warp = tid >> 5, lane = tid & 31;
-    const int d0 = 32 * (warp >> 2), v0 = 32 * (warp & 3);
-    float acc[2][4][4];
+    // Nm^T while the product runs: write (d, e) <- Nm(e, d) in 16-byte runs
+    if (ok) {
+        const uint8_t* raw = sm + BTS_NM;
+        for (int i = tid; i < KD * KD / 8; i += BT_THREADS) {
+            const int d = i >> 4, e0 = (i & 15) * 8;
+            uint16_t x[8];
 #pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-        for (int nj = 0; nj < 4; ++nj) acc[mi][nj][0] = acc[mi][nj][1] = acc[mi][nj][2] = acc[mi][nj][3] = 0.f;
-    tile_mm<true, false>(qf, df, d0, v0, (c.len + 7) & ~7, lane, acc);
-    uint8_t* piece = dst + TILE_BC + (v0 / BV) * BC_PIECE;   // one 32-column piece per warp
-    const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-        for (int nj = 0; nj < 4; ++nj) {
-            const int d = d0 + 16 * mi + g, col = 8 * nj + 2 * t;
-            *reinterpret_cast<uint32_t*>(piece + sw64_off(d, col)) = f2h(acc[mi][nj][0], acc[mi][nj][1]);
-            *reinterpret_cast<uint32_t*>(piece + sw64_off(d + 8, col)) = f2h(acc[mi][nj][2], acc[mi][nj][3]);
+            for (int u = 0; u < 8; ++u) x[u] = *reinterpret_cast<const uint16_t*>(raw + sw128_off(e0 + u, d, 128));
+            *reinterpret_cast<uint4*>(dst + TILE_NM + sw128_off(d, e0, 128)) =
+                make_uint4(x[0] | ((uint32_t)x[1] << 16), x[2] | ((uint32_t)x[3] << 16), x[4] | ((uint32_t)x[5] << 16),
+                           x[6] | ((uint32_t)x[7] << 16));
         }
+    }
+
+    // Bq rows d = TMEM lanes; warp w reads lane quarter w % 4, columns 64 (w / 4) ..
+    // +64, i.e. two of the four 32-column Bc pieces
+    bool mma_done = false;
+    if (ok) ok = mma_done = __syncthreads_and(mbar_wait(bar_mma, 0, WAIT_LIMIT)) != 0;
+    tc_fence_after();
+    if (ok) {
+        const int d = 32 * (warp & 3) + lane;
+#pragma unroll 1
+        for (int q = 0; q < 2; ++q) {
+            const int vt = 2 * (warp >> 2) + q;
+            float x[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(vt * BV), x);
+            tmem_ld_wait();
+            uint8_t* piece = dst + TILE_BC + vt * BC_PIECE;
+#pragma unroll
+            for (int j = 0; j < BV; j += 8)
+                *reinterpret_cast<uint4*>(piece + sw64_off(d, j)) =
+                    make_uint4(f2h(x[j] * down, x[j + 1] * down), f2h(x[j + 2] * down, x[j + 3] * down),
+                               f2h(x[j + 4] * down, x[j + 5] * down), f2h(x[j + 6] * down, x[j + 7] * down));
+        }
+    } else {   // a bounded wait ran out: flag it, let the copies and the product finish (bounded), free TMEM
+        if (tid == 0) atomicOr(fp.status, STATUS_TIMEOUT);
+        if (!tx_done) mbar_wait(bar_tx, 0, WAIT_LIMIT);
+        else if (!mma_done) mbar_wait(bar_mma, 0, WAIT_LIMIT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 // ---------------------------------------------------------------------------
