@@ -399,20 +399,20 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     float4 gpre[4][2];
     uint4 kpre = make_uint4(0u, 0u, 0u, 0u), qpre = kpre, vpre = kpre;
     float bpre = 0.f;
-    auto load_rows = [&](const ChunkRef& cc, int hh) {
+    auto load_g = [&](const ChunkRef& cc, int hh, int r) {
+        const int d8 = (tid & 15) * 8;
+        const int t = (tid >> 4) * 4 + r;
+        gpre[r][0] = gpre[r][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < cc.len) {
+            const size_t off = ((size_t)cc.tok0 * H + hh + (size_t)t * H) * KD + d8;
+            gpre[r][0] = __ldg(reinterpret_cast<const float4*>(p.g + off));
+            gpre[r][1] = __ldg(reinterpret_cast<const float4*>(p.g + off + 4));
+        }
+    };
+    auto load_first = [&](const ChunkRef& cc, int hh) {   // row 0 of k / q / v, and beta
         const int d8 = (tid & 15) * 8;
         const int tg0 = (tid >> 4) * 4;
         const size_t r0 = (size_t)cc.tok0 * H + hh;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int t = tg0 + r;
-            gpre[r][0] = gpre[r][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < cc.len) {
-                const size_t off = (r0 + (size_t)t * H) * KD + d8;
-                gpre[r][0] = __ldg(reinterpret_cast<const float4*>(p.g + off));
-                gpre[r][1] = __ldg(reinterpret_cast<const float4*>(p.g + off + 4));
-            }
-        }
         kpre = qpre = vpre = make_uint4(0u, 0u, 0u, 0u);
         if (tg0 < cc.len) {
             const size_t off = (r0 + (size_t)tg0 * H) * KD + d8;
@@ -421,6 +421,11 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             vpre = __ldg(reinterpret_cast<const uint4*>(p.v + off));
         }
         bpre = (tid < BT && tid < cc.len) ? __ldg(p.beta + r0 + (size_t)tid * H) : 0.f;
+    };
+    auto load_rows = [&](const ChunkRef& cc, int hh) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) load_g(cc, hh, r);
+        load_first(cc, hh);
     };
     ChunkRef none{};   // zero rows: loads nothing, defines the registers
     none.len = 0;
@@ -998,8 +1003,16 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 // or two Bc blocks: Qe costs about twice the others.
                 const int role = warp >> 2;
                 const float rs = FAST ? sCL[trow] : 1.f;   // rows d of Nm / Bc
-#pragma unroll 1
+                const ChunkRef& cx = have_n ? cn : none;
+#pragma unroll
                 for (int part = 0; part < 4; ++part) {
+                    // the next chunk's first loads, spread over the parts so
+                    // that their requests do not queue up behind each other
+                    if (FAST) {
+                        if (part == 0) { load_g(cx, hn, 0); load_g(cx, hn, 1); }
+                        if (part == 1) { load_g(cx, hn, 2); load_g(cx, hn, 3); }
+                        if (part == 2) load_first(cx, hn);
+                    }
                     if (part == 2) {   // Nm | Bc: the second product
                         if (!mbar_wait(bar2, phase2, WAIT_LIMIT)) *sFlag = 1;
                         phase2 ^= 1;
@@ -1066,7 +1079,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                     dg.w = ex2(sGL[tid * 4 + 3]);
                     *reinterpret_cast<float4*>(dst + TILE_DG + tid * 16) = dg;
                 }
-                if (FAST) load_rows(have_n ? cn : none, hn);   // ahead of the tile stores
                 fence_async_smem();
                 tc_fence_before();
                 __syncthreads();
