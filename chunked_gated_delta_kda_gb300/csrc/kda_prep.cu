@@ -263,6 +263,10 @@ __device__ __forceinline__ void sync_for_mma() {
     tc_fence_after();
 }
 
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_line(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
@@ -490,6 +494,16 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             // k, q, v rows are loaded one row ahead of their use (row 0 with
             // the gate), so each row's loads are in flight before the
             // previous row's shared-memory stores.
+            // rows 1 of k, q, v into L1 while the prefix scan runs
+#pragma unroll
+            for (int r = 1; r <= 1; ++r) {
+                if (tg0 + r < len) {
+                    const size_t off = (row0 + (size_t)(tg0 + r) * H) * KD + d8;
+                    prefetch_l1(p.k + off);
+                    prefetch_l1(p.q + off);
+                    prefetch_l1(p.v + off);
+                }
+            }
             uint4 kn = kpre, qn = qpre, vn = vpre;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
