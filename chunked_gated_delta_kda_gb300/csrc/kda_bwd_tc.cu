@@ -128,6 +128,25 @@ __device__ __forceinline__ void stage(float* dst, const float* __restrict__ src,
         *reinterpret_cast<float4*>(dst + r * LD + c4) = *reinterpret_cast<const float4*>(src + r * 128 + c4);
     }
 }
+// Stores of the gradients with an L2 evict-first policy: streamed once, they
+// should not push the per-CTA scratch out of L2.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void st_ef(float* p, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_ef2(float* p, float a, float b, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(p), "f"(a), "f"(b), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_ef4(float* p, float4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w), "l"(pol)
+                 : "memory");
+}
+
 __device__ __forceinline__ void spill(float* dst, const float* src, int tid) {
 #pragma unroll
     for (int i = tid; i < BT * 32; i += TC_THREADS) {
@@ -155,6 +174,53 @@ __device__ __forceinline__ void stage_rows_bf16(float* dst, const uint16_t* __re
         bf16x8(u, x);
         *reinterpret_cast<float4*>(dst + r * LD + c8) = make_float4(x[0], x[1], x[2], x[3]);
         *reinterpret_cast<float4*>(dst + r * LD + c8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
+    }
+}
+
+// Last reads of the streamed inputs, with the same policy.
+__device__ __forceinline__ uint4 ld_ef_u4(const void* p, uint64_t pol) {
+    uint4 r;
+    asm("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p), "l"(pol));
+    return r;
+}
+__device__ __forceinline__ float4 ld_ef_f4(const void* p, uint64_t pol) {
+    float4 r;
+    asm("ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+        : "l"(p), "l"(pol));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_ef_u32(const void* p, uint64_t pol) {
+    uint32_t r;
+    asm("ld.global.nc.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(r) : "l"(p), "l"(pol));
+    return r;
+}
+__device__ __forceinline__ void stage_rows_bf16_ef(float* dst, const uint16_t* __restrict__ src, size_t row0, size_t rs,
+                                                   int n, int tid, uint64_t pol) {
+#pragma unroll
+    for (int i = tid; i < BT * 16; i += TC_THREADS) {
+        const int r = i >> 4, c8 = (i & 15) * 8;
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (r < n) u = ld_ef_u4(src + (row0 + r * rs) * 128 + c8, pol);
+        float x[8];
+        bf16x8(u, x);
+        *reinterpret_cast<float4*>(dst + r * LD + c8) = make_float4(x[0], x[1], x[2], x[3]);
+        *reinterpret_cast<float4*>(dst + r * LD + c8 + 4) = make_float4(x[4], x[5], x[6], x[7]);
+    }
+}
+
+// stage_state_scaled with the evict-first policy (the state's last read)
+__device__ __forceinline__ void stage_state_scaled_ef(float* dst, const float* __restrict__ src, const float* e, int tid,
+                                                      uint64_t pol) {
+#pragma unroll
+    for (int i = tid; i < KD * 32; i += TC_THREADS) {
+        const int r = i >> 5, c4 = (i & 31) * 4;
+        float4 x = ld_ef_f4(src + r * VD + c4, pol);
+        const float f = __expf(e[r]);
+        x.x *= f; x.y *= f; x.z *= f; x.w *= f;
+        *reinterpret_cast<float4*>(dst + r * LD + c4) = x;
     }
 }
 
@@ -214,6 +280,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         tmem_ld_wait();
     };
 
+    const uint64_t efp = evict_first_policy();
     for (long long it = blockIdx.x; it < items; it += gridDim.x) {
         const int slot = (int)(it / H), h = (int)(it % H);
         ChunkRef c;
@@ -236,7 +303,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         for (int i = tid; i < BT * 32; i += TC_THREADS) {
             const int r = i >> 5, c4 = (i & 31) * 4;
             float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < n) x = *reinterpret_cast<const float4*>(p.g + (row0 + r * rs) * KD + c4);
+            if (r < n) x = ld_ef_f4(p.g + (row0 + r * rs) * KD + c4, efp);
             *reinterpret_cast<float4*>(B0 + r * LD + c4) = x;
         }
         if (tid < BT) vBeta[tid] = tid < n ? p.beta[row0 + tid * rs] : 0.f;
@@ -355,7 +422,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         {
             uint32_t vpre[16];
             frag_pairs(ti0, tj0, lane, [&](int q, int, int, int, int i, int j) {
-                vpre[q] = i < n ? *reinterpret_cast<const uint32_t*>(p.v + (row0 + i * rs) * VD + j) : 0u;
+                vpre[q] = i < n ? ld_ef_u32(p.v + (row0 + i * rs) * VD + j, efp) : 0u;
             });
             zero_acc(acc);
             mm128<false, false>(B1, B2, warp, lane, acc);
@@ -397,7 +464,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
 #pragma unroll
             for (int st = 0; st < 8; ++st) {
                 const int r = warp + 16 * st, c4 = lane * 4;
-                float4 zv = *reinterpret_cast<const float4*>(Z + r * VD + c4);
+                float4 zv = ld_ef_f4(Z + r * VD + c4, efp);
                 const float4 sv = *reinterpret_cast<const float4*>(S0 + r * VD + c4);
                 part[st] = zv.x * sv.x + zv.y * sv.y + zv.z * sv.z + zv.w * sv.w;
                 const float f = __expf(vTmp[r]);
@@ -431,7 +498,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
                 B1[i * LD + j] = a;
                 B1[i * LD + j + 1] = b;
                 if (i < n)
-                    *reinterpret_cast<float2*>(p.dv + (row0 + i * rs) * VD + j) = make_float2(vBeta[i] * a, vBeta[i] * b);
+                    st_ef2(p.dv + (row0 + i * rs) * VD + j, vBeta[i] * a, vBeta[i] * b, efp);
                 rsum[mi][hh] = fmaf(a, ypre[q].x, fmaf(b, ypre[q].y, rsum[mi][hh]));
             });
             // reduce over the 4 lanes sharing a row, then across the row band's warps
@@ -499,7 +566,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         }
         __syncthreads();
         // ---- B0 = Sp; dkh = -diag(beta) dy Sp^T -------------------------------------------
-        stage_state_scaled(B0, S0, vPiv, tid);
+        stage_state_scaled_ef(B0, S0, vPiv, tid, efp);
         __syncthreads();
         zero_acc(acc);
         mm128<false, true>(B1, B0, warp, lane, acc);
@@ -516,7 +583,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
         }
         __syncthreads();
         // ---- B1 = do; dqh = do Sp^T ----------------------------------------------------------
-        stage_rows_bf16(B1, p.dout, row0, rs, n, tid);
+        stage_rows_bf16_ef(B1, p.dout, row0, rs, n, tid, efp);
         __syncthreads();
         zero_acc(acc);
         mm128<false, true>(B1, B0, warp, lane, acc);
@@ -586,8 +653,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
 
         // ---- dG into B0; exit terms at the last row; reverse prefix sum; outputs -------------
         // raw q, k rows (B1, B2), then per fragment element from TMEM: dq, dk and dG (into B0)
-        stage_rows_bf16(B1, p.q, row0, rs, n, tid);
-        stage_rows_bf16(B2, p.k, row0, rs, n, tid);
+        stage_rows_bf16_ef(B1, p.q, row0, rs, n, tid, efp);
+        stage_rows_bf16_ef(B2, p.k, row0, rs, n, tid, efp);
         __syncthreads();
         {   // one 16-row half of the warp's tile at a time (fragment elements 16 mi .. 16 mi + 15)
             const int g = lane >> 2, t = lane & 3;
@@ -609,8 +676,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
                     // dG = qh dqh + kh dkh - kc dkc
                     B0[i * LD + j] = qq * ep * fq[e] + kk * ep * fh[e] - kk * em * fc[e];
                     if (i < n) {   // with the q/k norm: w.r.t. the normalised q, k
-                        p.dq[(row0 + i * rs) * KD + j] = scale * fq[e] * ep;
-                        p.dk[(row0 + i * rs) * KD + j] = fh[e] * ep + fc[e] * em;
+                        st_ef(p.dq + (row0 + i * rs) * KD + j, scale * fq[e] * ep, efp);
+                        st_ef(p.dk + (row0 + i * rs) * KD + j, fh[e] * ep + fc[e] * em, efp);
                     }
                 }
             }
@@ -631,7 +698,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) kda_bwd_tc_kernel(const BwdPara
 #pragma unroll 4
         for (int i = tid; i < n * 32; i += TC_THREADS) {
             const int r = i >> 5, c4 = (i & 31) * 4;
-            *reinterpret_cast<float4*>(p.dg + (row0 + r * rs) * KD + c4) = *reinterpret_cast<const float4*>(B0 + r * LD + c4);
+            st_ef4(p.dg + (row0 + r * rs) * KD + c4, *reinterpret_cast<const float4*>(B0 + r * LD + c4), efp);
         }
     }
     tc_fence_before();
