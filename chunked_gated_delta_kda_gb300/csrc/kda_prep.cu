@@ -152,6 +152,29 @@ __device__ __forceinline__ uint32_t ldg_u32(const uint16_t* p) {
 }
 __device__ __forceinline__ float2 ldg_f2(const float* p) { return __ldg(reinterpret_cast<const float2*>(p)); }
 
+// Read-once input rows (one head's rows of one chunk): loaded with an L2
+// evict-first policy so that they leave L2 ahead of the prefetched rows of
+// the next chunk.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint4 ldg_ef_u4(const void* p, uint64_t pol) {
+    uint4 r;
+    asm("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p), "l"(pol));
+    return r;
+}
+__device__ __forceinline__ float4 ldg_ef_f4(const void* p, uint64_t pol) {
+    float4 r;
+    asm("ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+        : "l"(p), "l"(pol));
+    return r;
+}
+
 __device__ __forceinline__ void unpack8_bf16(const uint4 u, float (&x)[8]) {
     float2 a = unpack_bf16(u.x), b = unpack_bf16(u.y), c = unpack_bf16(u.z), d = unpack_bf16(u.w);
     x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y; x[4] = c.x; x[5] = c.y; x[6] = d.x; x[7] = d.y;
@@ -400,6 +423,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     // loaded at the end of the previous chunk, before its tile stores are
     // queued, so that the read requests leave the SM ahead of 128 KB of
     // store data
+    const uint64_t efp = evict_first_policy();
     float4 gpre[4][2];
     uint4 kpre = make_uint4(0u, 0u, 0u, 0u), qpre = kpre, vpre = kpre;
     float bpre = 0.f;
@@ -409,8 +433,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
         gpre[r][0] = gpre[r][1] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (t < cc.len) {
             const size_t off = ((size_t)cc.tok0 * H + hh + (size_t)t * H) * KD + d8;
-            gpre[r][0] = __ldg(reinterpret_cast<const float4*>(p.g + off));
-            gpre[r][1] = __ldg(reinterpret_cast<const float4*>(p.g + off + 4));
+            gpre[r][0] = ldg_ef_f4(p.g + off, efp);
+            gpre[r][1] = ldg_ef_f4(p.g + off + 4, efp);
         }
     };
     auto load_first = [&](const ChunkRef& cc, int hh) {   // row 0 of k / q / v, and beta
@@ -420,9 +444,9 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
         kpre = qpre = vpre = make_uint4(0u, 0u, 0u, 0u);
         if (tg0 < cc.len) {
             const size_t off = (r0 + (size_t)tg0 * H) * KD + d8;
-            kpre = __ldg(reinterpret_cast<const uint4*>(p.k + off));
-            qpre = __ldg(reinterpret_cast<const uint4*>(p.q + off));
-            vpre = __ldg(reinterpret_cast<const uint4*>(p.v + off));
+            kpre = ldg_ef_u4(p.k + off, efp);
+            qpre = ldg_ef_u4(p.q + off, efp);
+            vpre = ldg_ef_u4(p.v + off, efp);
         }
         bpre = (tid < BT && tid < cc.len) ? __ldg(p.beta + r0 + (size_t)tid * H) : 0.f;
     };
@@ -585,9 +609,9 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                     kn = qn = vn = make_uint4(0u, 0u, 0u, 0u);
                     if (t + 1 < len) {
                         const size_t off = (row0 + (size_t)(t + 1) * H) * KD + d8;
-                        kn = __ldg(reinterpret_cast<const uint4*>(p.k + off));
-                        qn = __ldg(reinterpret_cast<const uint4*>(p.q + off));
-                        vn = __ldg(reinterpret_cast<const uint4*>(p.v + off));
+                        kn = ldg_ef_u4(p.k + off, efp);
+                        qn = ldg_ef_u4(p.q + off, efp);
+                        vn = ldg_ef_u4(p.v + off, efp);
                     }
                 }
                 float kf[8], qf[8], vf[8];
