@@ -23,6 +23,12 @@
 // per-thread work.  Matrices needed again later live in a per-CTA global
 // scratch; the unit lower-triangular inverse is the blocked one shared with
 // the mma.sync kernel (on a padded fp32 copy).
+//
+// Selected by KDA_FLAG_BWD_UMMA.  On GB300 it is slower than the mma.sync
+// kernel (20.9 against 16.5 ms for the per-chunk stage at T=65536, H=32):
+// the products take ~15% of a chunk's cycles, the operand staging between
+// them (gating, transposes, scratch round trips) the rest, with one chunk in
+// flight per SM and nothing overlapping it.
 #include <cuda_bf16.h>
 
 #include "kda.h"
