@@ -262,3 +262,27 @@ def test_bwd_more_configurations(case):
     ref = run_ref(x, gr, l2norm=l2)
     for path in PATHS:
         print(case, path, check(run_gpu(x, gr, l2norm=l2, path=path), ref, path))
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("c", [2.0 ** -10, 2.0 ** 8])
+def test_bwd_gradient_scale(path, c):
+    """Every gradient is linear in (do, dht) jointly: with do and dht scaled
+    by c = 2^-10 or 2^8 (exact in bf16 / fp32) each gradient must match the
+    oracle's times c under the path's bound.  This exercises the power-of-two
+    normalisation of do in the transposed-tiles kernel (its fp16 Qe^T do
+    product) away from unit magnitudes.  The token-by-token path runs in fp32
+    only, where a power-of-two factor commutes with every rounding step, so
+    there it must also reproduce c times the unscaled run bit for bit."""
+    w = custom("eq", B=1, T=300, H=2, seqlens=(170, 130), with_h0=True, seed=29)
+    x = make_inputs(w)
+    gr = make_grad_inputs(w)
+    grs = {"do": (gr["do"].float() * c).bfloat16(), "dht": gr["dht"] * c}
+    assert torch.equal(grs["do"].float(), gr["do"].float() * c)   # exact in bf16
+    ref = run_ref(x, gr)
+    scaled = run_gpu(x, grs, path=path)
+    print(path, c, check(scaled, [r * c for r in ref], path))
+    if path == "token":
+        base = run_gpu(x, gr, path=path)
+        for name, a_, b_ in zip(NAMES, base, scaled):
+            assert np.array_equal(a_ * c, b_), name
