@@ -518,15 +518,14 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             // k, q, v rows are loaded one row ahead of their use (row 0 with
             // the gate), so each row's loads are in flight before the
             // previous row's shared-memory stores.
-            // rows 1 of k, q, v into L1 while the prefix scan runs
-#pragma unroll
-            for (int r = 1; r <= 1; ++r) {
-                if (tg0 + r < len) {
-                    const size_t off = (row0 + (size_t)(tg0 + r) * H) * KD + d8;
-                    prefetch_l1(p.k + off);
-                    prefetch_l1(p.q + off);
-                    prefetch_l1(p.v + off);
-                }
+            // the thread's second row of k, q, v into L1 while the prefix scan
+            // runs (the third and fourth as well would overflow the L1 left
+            // beside this kernel's shared memory)
+            if (tg0 + 1 < len) {
+                const size_t off = (row0 + (size_t)(tg0 + 1) * H) * KD + d8;
+                prefetch_l1(p.k + off);
+                prefetch_l1(p.q + off);
+                prefetch_l1(p.v + off);
             }
             uint4 kn = kpre, qn = qpre, vn = vpre;
 #pragma unroll
