@@ -227,7 +227,8 @@ def run_reference(args, w, rank, world):
     dt = (time.perf_counter() - t0) / args.steps
     value = Ts * w.H / dt
     th, _, _, _ = algorithmic(w, w.N)
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "runs_on": "host cores (the fp64 oracle; no GPU work)",
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V,
@@ -263,7 +264,7 @@ def decode_oracle_rate(x, target_s):
         if dt > target_s / 4 or n >= DECODE_N:
             break
         n = min(DECODE_N, n * 4)
-    return {"value": n * DECODE_H / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": n * DECODE_H / dt, "unit": UNIT, "cores": 1, "kind": "oracle", "seconds": dt,
             "sample": f"fp64 numpy decode oracle, {n} sequences x {DECODE_H} heads x 1 token ({dt:.1f} s)"}
 
 
@@ -276,8 +277,10 @@ def run_decode(args, rank, world, local):
             return 0
         x = make_decode_inputs(DECODE_N, DECODE_H, 1, pool_slots=DECODE_POOL, seed=5)
         cb = decode_oracle_rate(x, target_s=max(1.0, 60.0 / max(1, args.steps + args.warmup)))
-        line = {"impl": "reference", "metric": DECODE_METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": 0,
-                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        line = {"impl": "reference", "metric": DECODE_METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": world,
+                "runs_on": "host cores (the fp64 oracle; no GPU work)",
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": cb["seconds"] * 1e3,
+                "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": name},
                 "cpu_baseline": cb,
                 "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -401,7 +404,7 @@ def bwd_oracle_rate(w, target_s):
         if dt * 4 > target_s or Ts >= w.T:
             break
         Ts = min(w.T, Ts * 2)
-    return {"value": Ts * w.H / dt, "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle",
+    return {"value": Ts * w.H / dt, "unit": UNIT, "cores": torch.get_num_threads(), "kind": "oracle", "seconds": dt,
             "sample": f"fp64 torch autograd through the per-token recurrence on the first {Ts} tokens x {w.H} heads "
                       f"of the {w.name} workload ({dt:.1f} s)"}
 
@@ -413,8 +416,10 @@ def run_bwd(args, rank, world, local, w):
         if rank != 0:
             return 0
         cb = bwd_oracle_rate(w, target_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)))
-        line = {"impl": "reference", "metric": BWD_METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": 0,
-                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        line = {"impl": "reference", "metric": BWD_METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": world,
+                "runs_on": "host cores (the fp64 oracle; no GPU work)",
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": cb["seconds"] * 1e3,
+                "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": w.name},
                 "cpu_baseline": cb,
                 "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
