@@ -151,17 +151,31 @@ __global__ void __launch_bounds__(BT_THREADS, 2) kda_bwd_tiles_kernel(const FwdP
         mma_commit_warp(bar_mma);
     }
 
-    // Nm^T while the product runs: write (d, e) <- Nm(e, d) in 16-byte runs
+    // Nm^T while the product runs: write (d, e) <- Nm(e, d) in 16-byte runs.
+    // The lanes sharing d read rows e0 + u with e0 a multiple of 8, which
+    // all fall on one swizzled 16-byte position; each lane therefore starts
+    // at its own u (k = e0 / 8 % 8: 2-way instead of 16-way bank conflicts)
+    // and rotates its eight values back into place.
     if (ok) {
         const uint8_t* raw = sm + BTS_NM;
         for (int i = tid; i < KD * KD / 8; i += BT_THREADS) {
-            const int d = i >> 4, e0 = (i & 15) * 8;
-            uint16_t x[8];
+            const int d = i >> 4, e0 = (i & 15) * 8, k = i & 7;
+            uint32_t x[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) x[u] = *reinterpret_cast<const uint16_t*>(raw + sw128_off(e0 + u, d, 128));
+            for (int u = 0; u < 8; ++u)   // x[u] = Nm(e0 + (u + k) % 8, d)
+                x[u] = *reinterpret_cast<const uint16_t*>(raw + sw128_off(e0 + ((u + k) & 7), d, 128));
+#pragma unroll
+            for (int b = 1; b < 8; b <<= 1) {   // rotate by k: x[j] <- x[(j - k) % 8]
+                if (k & b) {
+                    uint32_t y[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) y[j] = x[(j - b) & 7];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) x[j] = y[j];
+                }
+            }
             *reinterpret_cast<uint4*>(dst + TILE_NM + sw128_off(d, e0, 128)) =
-                make_uint4(x[0] | ((uint32_t)x[1] << 16), x[2] | ((uint32_t)x[3] << 16), x[4] | ((uint32_t)x[5] << 16),
-                           x[6] | ((uint32_t)x[7] << 16));
+                make_uint4(x[0] | (x[1] << 16), x[2] | (x[3] << 16), x[4] | (x[5] << 16), x[6] | (x[7] << 16));
         }
     }
 
