@@ -83,7 +83,8 @@ constexpr uint32_t RW = 163840;
 // inverse, row stride 68 floats (conflict-free column walks).
 constexpr int DS = 68;
 constexpr uint32_t W_DIAG = RW;                          // 2 x 64 x 68 floats = 34816 B
-constexpr uint32_t W_TMP = RW + 2 * 64 * DS * 4;         // merge temps, up to 8 KB
+constexpr uint32_t W_TMP = RW + 2 * 64 * DS * 4;         // merge temps, up to 10 KB
+static_assert(W_TMP + 2 * 1280 * 4 <= RM, "merge temps overlap the misc block");
 
 template <bool FAST>
 struct Map {
@@ -861,13 +862,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 const int db = warp >> 1;
                 const int C0 = (warp & 1) * 32, R0 = C0 + 16;
                 float* Db = Wd + db * 64 * DS;
-                float* T1 = Wt + warp * 256;
+                float* T1 = Wt + warp * 384;   // 16 x 16, row stride 24 (conflict-free fragment loads)
                 float acc[2][4];
                 tile16_load(acc, Db + R0 * DS + C0, DS, lane);                           // Y
                 mma_tile16<16>(acc, Db + R0 * DS + C0, DS, Db + C0 * DS + C0, DS, lane);  // + Y Xs
-                tile16_store(acc, T1, 16, lane, 1.f);
+                tile16_store(acc, T1, 24, lane, 1.f);
                 __syncwarp();
-                mma_tile16<16>(acc, Db + R0 * DS + R0, DS, T1, 16, lane);               // T + Zs T
+                mma_tile16<16>(acc, Db + R0 * DS + R0, DS, T1, 24, lane);               // T + Zs T
                 tile16_store(acc, Db + R0 * DS + C0, DS, lane, -1.f);
             }
             __syncthreads();
@@ -877,13 +878,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 const int db = warp >> 2;
                 const int mr = ((warp >> 1) & 1) * 16, nc = (warp & 1) * 16;
                 float* Db = Wd + db * 64 * DS;
-                float* T2 = Wt + db * 1024;     // 32 x 32
+                float* T2 = Wt + db * 1280;     // 32 x 32, row stride 40 (conflict-free fragment loads)
                 float acc[2][4];
                 tile16_load(acc, Db + (32 + mr) * DS + nc, DS, lane);                        // Y
                 mma_tile16<32>(acc, Db + (32 + mr) * DS, DS, Db + nc, DS, lane);             // + Y Xs
-                tile16_store(acc, T2 + mr * 32 + nc, 32, lane, 1.f);
+                tile16_store(acc, T2 + mr * 40 + nc, 40, lane, 1.f);
                 bar_sync_named(1, 256);
-                mma_tile16<32>(acc, Db + (32 + mr) * DS + 32, DS, T2 + nc, 32, lane);        // T + Zs T
+                mma_tile16<32>(acc, Db + (32 + mr) * DS + 32, DS, T2 + nc, 40, lane);        // T + Zs T
                 tile16_store(acc, Db + (32 + mr) * DS + nc, DS, lane, -1.f);
             }
             __syncthreads();
