@@ -27,6 +27,19 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(lib, n), f"libkda.so does not export {n}"
 
 
+def test_flag_constants_match_the_header():
+    """Every KDA_FLAG_* of include/kda.h has the same value in the Python
+    binding, and the flags are distinct single bits."""
+    from chunked_gated_delta_kda_gb300 import binding
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    flags = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+(KDA_FLAG_[A-Z0-9_]+)\s+(\d+)u", text)}
+    assert len(flags) >= 6, flags
+    for name, value in flags.items():
+        assert getattr(binding, name) == value, name
+        assert value > 0 and value & (value - 1) == 0, name
+    assert len(set(flags.values())) == len(flags)
+
+
 def test_workspace_bytes():
     from chunked_gated_delta_kda_gb300 import binding
     lib = binding.load_library()
