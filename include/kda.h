@@ -319,10 +319,16 @@ size_t kda_bwd_workspace_bytes(int B, int T, int H, int K, int V, int N);
  * chunk; the state gradient obeys the same recurrence with the transposed
  * transition, dS_c = Dg_c dS_{c+1} + Nm_c^T dS_{c+1} + Qe_c^T do_c, which the
  * same scan evaluates on transposed tiles in reverse chunk order; then every
- * chunk replays its tokens in fp32 from its entering state and applies the
- * per-token chain rule backwards from its exit state gradient.  Precision:
- * the chunk states and state gradients carry the forward's product
- * precision (fp16 operands, fp32 accumulation), the per-token part is fp32.
+ * chunk applies the chain rule in chunked form from its entering state and
+ * its exit state gradient, on TF32 tensor-core products (with
+ * KDA_FLAG_BWD_CHUNK_FP32: token by token in fp32; chunks outside the
+ * chunked form's factor range take that path anyway).  Precision: the chunk
+ * states and state gradients carry the forward's product precision (fp16
+ * operands, fp32 accumulation), the per-chunk part TF32 products with fp32
+ * accumulation.  Range: the reverse pass takes Qe_c^T do_c as fp16, so its
+ * entries must stay below 65504 and lose relative precision below about
+ * 6e-5 (fp16's normal range); dout of the magnitudes loss scaling produces
+ * keeps them inside it.
  * (sequence, head) units the forward flags as beyond its factoring range go
  * to the token-by-token path, which replays the forward in fp32 one token at
  * a time (exact for any decay, one unit per CTA: slow); with
