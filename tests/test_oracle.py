@@ -416,3 +416,106 @@ def _passes(pin, run):
 def test_pins_catch_mutants(kind):
     failed = [p.__name__ for p in PINS if not _passes(p, _mutant(kind))]
     assert failed, f"no pin catches mutant {kind}"
+
+
+# ---------------------------------------------------------------------------
+# The two operands of M4's subtraction (u and w S) and the cancellation ratio
+# built on them (section "测试与验证体系": the cancellation_stress search).
+#
+# Unrolling the per-token rule inside one chunk gives the meaning of
+# v_new = u - w S without any chunked algebra: with the decayed state
+# S'_t = diag(exp(g_t)) S_{t-1}, the per-token rule adds k_t d_t^T where
+#   d_t = beta_t (v_t - S'_t^T k_t),
+# so S_T = diag(exp(G_T)) S_0 + sum_t diag(exp(G_T - G_t)) k_t d_t^T, which is
+# M4's state update with v_new[t] = d_t.  Hence, recorded from a plain
+# token loop: u - w S = d (any S_0), u = d at S_0 = 0 (u does not depend on
+# S_0), and w S = u - d.  With beta = 0 both operands vanish.
+# ---------------------------------------------------------------------------
+
+def _token_deltas(S0, k, v, g, beta):
+    """d_t of the per-token rule over one chunk (plain loop, fp64)."""
+    S = np.array(S0, dtype=np.float64)
+    d = np.zeros((k.shape[0], v.shape[1]))
+    for t in range(k.shape[0]):
+        S = np.exp(g[t])[:, None] * S
+        d[t] = beta[t] * (v[t] - S.T @ k[t])
+        S = S + np.outer(k[t], d[t])
+    return d
+
+
+def _terms_problem(seed, L=23, K=6, V=6):
+    rng = np.random.default_rng(seed)
+    k = rng.standard_normal((L, K))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    v = rng.standard_normal((L, V))
+    g = -0.3 * np.abs(rng.standard_normal((L, K)))
+    beta = rng.uniform(0.1, 0.9, L)
+    S = rng.standard_normal((K, V))
+    return S, k, v, g, beta
+
+
+def pin_terms(step):
+    """u and w S returned by ``step`` (a chunk_step-like callable) against the
+    token deltas; also the ratio helper built from them."""
+    S, k, v, g, beta = _terms_problem(5)
+    qs = np.zeros_like(k)
+    BT = 32
+    _, _, (u0, wS0) = step(np.zeros_like(S), qs, k, v, g, beta, BT, return_terms=True)
+    _, _, (u, wS) = step(S, qs, k, v, g, beta, BT, return_terms=True)
+    d0 = _token_deltas(np.zeros_like(S), k, v, g, beta)
+    d = _token_deltas(S, k, v, g, beta)
+    ok = np.allclose(u0, d0, rtol=0, atol=1e-12) and np.allclose(wS0, 0.0, atol=1e-12)
+    ok = ok and np.allclose(u, d0, rtol=0, atol=1e-12)
+    ok = ok and np.allclose(wS, d0 - d, rtol=0, atol=1e-12)
+    ok = ok and np.allclose(u - wS, d, rtol=0, atol=1e-12)
+    _, _, (ub, wSb) = step(S, qs, k, v, g, np.zeros_like(beta), BT, return_terms=True)
+    ok = ok and np.array_equal(ub, np.zeros_like(ub)) and np.array_equal(wSb, np.zeros_like(wSb))
+    return bool(ok)
+
+
+def test_cancellation_terms_equal_token_deltas():
+    assert pin_terms(chunk_step)
+
+
+def test_cancellation_terms_with_tail_and_full_chunk():
+    """The same identity on a ragged tail (L < BT) and on a full 128-row chunk."""
+    for L, BT in ((37, 128), (128, 128)):
+        S, k, v, g, beta = _terms_problem(6 + L, L=L, K=8, V=5)
+        _, _, (u, wS) = chunk_step(S, np.zeros_like(k), k, v, g, beta, BT, return_terms=True)
+        np.testing.assert_allclose(u - wS, _token_deltas(S, k, v, g, beta), rtol=0, atol=1e-11)
+
+
+def test_cancellation_ratio_value():
+    """cancellation_ratio = ||d|| / max(||u||, ||u - d||) with u the deltas
+    from a zero state and d those from S; 0 when v is chosen so that every
+    token's prediction is exact (d = 0 with S = 0, v = 0)."""
+    from oracle.chunked import cancellation_ratio
+    S, k, v, g, beta = _terms_problem(8)
+    d0 = _token_deltas(np.zeros_like(S), k, v, g, beta)
+    d = _token_deltas(S, k, v, g, beta)
+    want = np.linalg.norm(d) / max(np.linalg.norm(d0), np.linalg.norm(d0 - d))
+    assert abs(cancellation_ratio(S, k, v, g, beta, BT=32) - want) < 1e-12
+    assert cancellation_ratio(np.zeros_like(S), k, np.zeros_like(v), g, beta, BT=32) == 0.0
+
+
+def _terms_mutant(kind):
+    """chunk_step with a plausible mistake planted in its returned terms."""
+    def step(S, qs, k, v, g, beta, BT, return_terms=False):
+        o, S1, (u, wS) = chunk_step(S, qs, k, v, g, beta, BT, return_terms=True)
+        if kind == "w_not_times_S":
+            # w itself instead of w S (K == V here, so the shapes agree)
+            _, _, (_, w) = chunk_step(np.eye(S.shape[0]), qs, k, v, g, beta, BT, return_terms=True)
+            wS = w
+        elif kind == "wS_sign":
+            wS = -wS
+        elif kind == "u_without_inverse":
+            u = beta[:, None] * v
+        elif kind == "terms_swapped":
+            u, wS = wS, u
+        return o, S1, (u, wS)
+    return step
+
+
+@pytest.mark.parametrize("kind", ["w_not_times_S", "wS_sign", "u_without_inverse", "terms_swapped"])
+def test_terms_pin_catches_mutants(kind):
+    assert not pin_terms(_terms_mutant(kind))
