@@ -689,7 +689,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "bf16 in/out; fp16 MMA operands, fp32 accumulate, fp32 state", "data": "synthetic",
         "config": {"workload": w.name, "B": B, "T": T, "H": H, "K": w.K, "V": w.V, "chunk": 128,
                    "h0": h0 is not None, "output_final_state": True,
                    "l2_between_steps": "inputs (2.7 GB per step) larger than L2 (129 MB); no flush",

@@ -29,6 +29,9 @@ KDA_FLAG_SAVE_FOR_BWD = 8
 KDA_FLAG_BWD_REUSE_FWD = 16
 KDA_FLAG_BWD_UMMA = 32
 
+KDA_DEBUG_WAIT_LIMIT = 1
+KDA_DEBUG_DROP_SCAN_LOAD = 2
+
 _STATUS = {
     0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
     4: "invalid cu_seqlens", 5: "device wait timed out", 6: "too large for the no-alloc scratch",
@@ -79,6 +82,8 @@ def load_library(path: Optional[str] = None):
                             i, i, i, i, i, i, u, vp, sz, vp]
     lib.kda_bwd_timed.restype = ctypes.c_int
     lib.kda_bwd_timed.argtypes = lib.kda_bwd.argtypes + [vp]
+    lib.kda_debug_set.restype = ctypes.c_int
+    lib.kda_debug_set.argtypes = [i, u]
     lib.kda_status_str.restype = ctypes.c_char_p
     lib.kda_status_str.argtypes = [i]
     _lib = lib
@@ -141,6 +146,15 @@ def kda_fwd_noalloc(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, N: int, flag
                              _ptr(o), _ptr(ht), B, T, H, K, V, N, flags, _stream_handle(q.device))
     if rc != 0:
         raise KdaError(rc, "kda_fwd_noalloc")
+
+
+def debug_set(what: int, value: int) -> None:
+    """Test hook of the bounded device waits (``kda_debug_set``): the poll
+    limit (``KDA_DEBUG_WAIT_LIMIT``, 0 = default) or a one-shot dropped scan
+    load (``KDA_DEBUG_DROP_SCAN_LOAD``) for the next forward."""
+    rc = load_library().kda_debug_set(int(what), int(value))
+    if rc != 0:
+        raise KdaError(rc, "kda_debug_set")
 
 
 def get_status(workspace: torch.Tensor) -> int:

@@ -8,6 +8,11 @@
 #include "kda_common.cuh"
 
 namespace kda {
+// Test hooks (kda_debug_set): poll limit of the bounded waits (0: the
+// kernels' default) and one-shot debug bits for the next forward.
+static uint32_t g_wait_limit = 0;
+static uint32_t g_debug_once = 0;
+uint32_t debug_wait_limit() { return g_wait_limit; }
 unsigned long long bwd_chunk_state_offset(int B, int T, int H, int N);
 cudaError_t launch_prep(const FwdParams& p, bool l2norm, cudaStream_t stream);
 cudaError_t launch_scan(const FwdParams& p, cudaStream_t stream);
@@ -94,6 +99,9 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const fl
     p.T = T;
     p.H = H;
     p.N = N;
+    p.wait_limit = kda::g_wait_limit;
+    p.debug = kda::g_debug_once;
+    kda::g_debug_once = 0;
     if (cu_seqlens == nullptr) {
         p.NT = T / kda::BT;
         p.nslots = N * p.NT;
@@ -141,6 +149,17 @@ kda_status kda_get_status(const void* workspace, cudaStream_t stream) {
     if (word & kda::STATUS_TIMEOUT) return KDA_ERR_TIMEOUT;
     if (word & kda::STATUS_BAD_INDEX) return KDA_ERR_BAD_STATE_INDEX;
     return KDA_OK;
+}
+
+kda_status kda_debug_set(int what, unsigned value) {
+    switch (what) {
+        case KDA_DEBUG_WAIT_LIMIT: kda::g_wait_limit = value; return KDA_OK;
+        case KDA_DEBUG_DROP_SCAN_LOAD:
+            kda::g_debug_once = value ? (kda::g_debug_once | kda::DEBUG_DROP_SCAN_LOAD)
+                                      : (kda::g_debug_once & ~kda::DEBUG_DROP_SCAN_LOAD);
+            return KDA_OK;
+    }
+    return KDA_ERR_INVALID_ARG;
 }
 
 const char* kda_status_str(kda_status status) {

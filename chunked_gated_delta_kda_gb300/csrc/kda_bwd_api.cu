@@ -24,6 +24,7 @@
 namespace kda {
 cudaError_t launch_prep(const FwdParams& p, bool l2norm, cudaStream_t stream);
 cudaError_t launch_scan(const FwdParams& p, cudaStream_t stream);
+uint32_t debug_wait_limit();
 }  // namespace kda
 
 namespace {
@@ -136,6 +137,7 @@ static kda_status bwd_impl(const void* q, const void* k, const void* v, const fl
     fp.exact_flags = reinterpret_cast<uint32_t*>(ws + L.flags);
     fp.ckpt = reinterpret_cast<float*>(ws + L.ckpt_s);
     fp.scale = scale;
+    fp.wait_limit = kda::debug_wait_limit();
     fp.T = T;
     fp.H = H;
     fp.N = N;

@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(BT_THREADS, 2) kda_bwd_tiles_kernel(const FwdP
         *reinterpret_cast<uint4*>(sm + BTS_DO + sw128_off(t, c8, 128)) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
     }
     fence_async_smem();
-    const bool tx_done = __syncthreads_and(mbar_wait(bar_tx, 0, WAIT_LIMIT)) != 0;
+    const bool tx_done = __syncthreads_and(mbar_wait(bar_tx, 0, wait_limit_of(fp))) != 0;
     tc_fence_after();
     bool ok = tx_done;
     if (ok && warp == 0) {   // Bq[d][v] = sum_t Qe[t][d] do[t][v]: both operands MN-major, K = t
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(BT_THREADS, 2) kda_bwd_tiles_kernel(const FwdP
     // Bq rows d = TMEM lanes; warp w reads lane quarter w % 4, columns 64 (w / 4) ..
     // +64, i.e. two of the four 32-column Bc pieces
     bool mma_done = false;
-    if (ok) ok = mma_done = __syncthreads_and(mbar_wait(bar_mma, 0, WAIT_LIMIT)) != 0;
+    if (ok) ok = mma_done = __syncthreads_and(mbar_wait(bar_mma, 0, wait_limit_of(fp))) != 0;
     tc_fence_after();
     if (ok) {
         const int d = 32 * (warp & 3) + lane;
@@ -201,8 +201,8 @@ __global__ void __launch_bounds__(BT_THREADS, 2) kda_bwd_tiles_kernel(const FwdP
         }
     } else {   // a bounded wait ran out: flag it, let the copies and the product finish (bounded), free TMEM
         if (tid == 0) atomicOr(fp.status, STATUS_TIMEOUT);
-        if (!tx_done) mbar_wait(bar_tx, 0, WAIT_LIMIT);
-        else if (!mma_done) mbar_wait(bar_mma, 0, WAIT_LIMIT);
+        if (!tx_done) mbar_wait(bar_tx, 0, DRAIN_LIMIT);
+        else if (!mma_done) mbar_wait(bar_mma, 0, DRAIN_LIMIT);
     }
     tc_fence_before();
     __syncthreads();

@@ -263,9 +263,13 @@ __global__ void __launch_bounds__(UM_THREADS, 1) kda_bwd_umma_kernel(const BwdPa
         __syncthreads();
         tc_fence_after();
     };
+    // bounded: once a wait of this CTA has run out, later ones return at once
+    // and the item loop ends at its next iteration (tested right after a CTA
+    // barrier, so every thread takes the same decision)
+    const uint32_t wlim = wait_limit_of(fp);
     auto commit_wait = [&]() {
         if (tid == 0) mma_commit(bar);
-        if (!mbar_wait(bar, phase, WAIT_LIMIT)) *sFlag = 1;
+        if (*sFlag == 0 && !mbar_wait(bar, phase, wlim)) *sFlag = 1;
         phase ^= 1u;
         tc_fence_after();
     };
@@ -292,6 +296,7 @@ __global__ void __launch_bounds__(UM_THREADS, 1) kda_bwd_umma_kernel(const BwdPa
         float* G0 = reinterpret_cast<float*>(S0);   // padded fp32 view (row length MMA_LD)
         tc_fence_before();
         __syncthreads();
+        if (*sFlag != 0) break;
 
         // ---- gate prefix sums G (S0 padded), beta, q/k row norms --------------------------
 #pragma unroll 4
@@ -703,8 +708,15 @@ __global__ void __launch_bounds__(UM_THREADS, 1) kda_bwd_umma_kernel(const BwdPa
         }
     }
     __syncwarp();
-    if (*sFlag != 0 && tid == 0) atomicOr(p.status, STATUS_TIMEOUT);
     tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        if (*sFlag != 0) atomicOr(p.status, STATUS_TIMEOUT);
+        // every product issued has completed before TMEM is freed (after the
+        // last commit_wait the barrier's pending phase has parity `phase`)
+        mma_commit(bar);
+        mbar_wait(bar, phase, DRAIN_LIMIT);
+    }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, T_COLS);
 }

@@ -112,8 +112,18 @@ __host__ __device__ constexpr unsigned long long ws_tiles_offset(unsigned long l
     return WS_HEADER + ((items * 4ull + 255ull) / 256ull) * 256ull;
 }
 
-// Poll limit for mbarrier waits (MMA / bulk-copy completion inside one CTA).
+// Poll limit for mbarrier waits (MMA / bulk-copy completion inside one CTA),
+// used when FwdParams::wait_limit is 0.  A wait on another role of the same
+// CTA gives up after the limit, sets the CTA's failure flag and returns;
+// every later wait of that CTA then returns at once, so a stalled CTA leaves
+// within one limit.  Before it frees its TMEM or shared memory a CTA waits
+// (with DRAIN_LIMIT, never skipped) for the copies and products it issued
+// itself: those complete on their own.
 constexpr uint32_t WAIT_LIMIT = 1u << 24;
+constexpr uint32_t DRAIN_LIMIT = 1u << 24;
+
+// FwdParams::debug bits (failure-detection tests only; see kda_debug_set)
+constexpr uint32_t DEBUG_DROP_SCAN_LOAD = 1u;   // scan: unit (0, 0), V tile 0 never loads chunk 1's stage
 
 struct FwdParams {
     const uint16_t* q;      // bf16 [B*T, H, K]
@@ -137,7 +147,13 @@ struct FwdParams {
     int N;
     int NT;                 // chunks per sequence (fixed length), else 0
     int nslots;             // number of chunk slots the workspace holds
+    uint32_t wait_limit;    // poll limit of the bounded waits (0: WAIT_LIMIT)
+    uint32_t debug;         // DEBUG_* bits (0 in normal use)
 };
+
+__device__ __forceinline__ uint32_t wait_limit_of(const FwdParams& p) {
+    return p.wait_limit != 0u ? p.wait_limit : WAIT_LIMIT;
+}
 
 // A chunk: sequence n, chunk j inside it, first token (packed index), rows.
 struct ChunkRef {

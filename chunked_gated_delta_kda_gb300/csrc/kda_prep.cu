@@ -34,10 +34,13 @@
 //
 // GB300 mapping.  Persistent kernels: one 512-thread CTA per SM walks the
 // work items.  The 128-wide contractions run on tcgen05 tensor cores with
-// fp32 accumulators in TMEM; the prefix sum, the gated operands and the
-// 16x16 / 32x32 / 64x64 levels of the inverse run on CUDA cores in fp32; the
-// 64 -> 128 level of the inverse runs on the tensor cores.  While one chunk
-// computes, its successor's input rows are prefetched into L2.
+// fp16 operands (bf16 for the wide variant's gated operands) and fp32
+// accumulators in TMEM.  The prefix sum, the gated operands and the 16x16
+// diagonal blocks of the inverse run on CUDA cores in fp32; the 16 -> 32 and
+// 32 -> 64 merges of the inverse on warp-level TF32 tensor-core products
+// (mma.sync, fp32 accumulation); the 64 -> 128 merge on tcgen05 with fp16
+// operands.  While one chunk computes, its successor's input rows are
+// prefetched into L2.
 #include "kda_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -73,6 +76,7 @@ constexpr uint32_t M_CL = RM + 3072;       // f32[128]  exp(G_last - P) (fast)
 constexpr uint32_t M_TOT = RM + 3584;      // f32[8][128] row-block sums (wide)
 constexpr uint32_t M_BAR = RM + 7680;      // mbarrier
 constexpr uint32_t M_BAR2 = RM + 7688;     // mbarrier of the second transition product
+constexpr uint32_t M_BARD = RM + 7696;     // mbarrier: every issued product done (before TMEM is freed)
 constexpr uint32_t M_TMEM = RM + 7744;     // TMEM base address
 constexpr uint32_t M_FLAG = RM + 7748;     // failure flag
 constexpr uint32_t SMEM_USED = RM + 7808;
@@ -404,6 +408,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(bar2, 1);
+        mbar_init(sbase + M_BARD, 1);
         fence_mbar_init();
         *sFlag = 0;
     }
@@ -413,8 +418,17 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + M_TMEM);
 
+    // Bounded waits: once one has run out (flag set), later ones of this CTA
+    // return at once, the item finishes on whatever the tensor memory holds
+    // (its tiles are garbage; the status word reports the failure) and the
+    // loop ends after it.  The flag is only set before the item's last CTA
+    // barrier, so every thread sees the same value at the loop test.
+    const uint32_t wlim = wait_limit_of(p);
+    auto bounded_wait = [&](uint32_t b, uint32_t parity) {
+        if (*sFlag == 0 && !mbar_wait(b, parity, wlim)) *sFlag = 1;
+    };
     auto wait_mma = [&]() {
-        if (!mbar_wait(bar, phase, WAIT_LIMIT)) *sFlag = 1;
+        bounded_wait(bar, phase);
         phase ^= 1;
         tc_fence_after();
     };
@@ -1052,7 +1066,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                         if (part == 2) load_first(cx, hn);
                     }
                     if (part == 2) {   // Nm | Bc: the second product
-                        if (!mbar_wait(bar2, phase2, WAIT_LIMIT)) *sFlag = 1;
+                        bounded_wait(bar2, phase2);
                         phase2 ^= 1;
                         tc_fence_after();
                     }
@@ -1140,7 +1154,12 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
         have = have_n;
     }
     if (bulk_thread) bulk_wait0();
-    if (tid == 0 && *sFlag != 0) atomicOr(p.status, STATUS_TIMEOUT);
+    if (tid == 0) {
+        if (*sFlag != 0) atomicOr(p.status, STATUS_TIMEOUT);
+        // every product this thread issued has completed before TMEM is freed
+        mma_commit(sbase + M_BARD);
+        mbar_wait(sbase + M_BARD, 0, DRAIN_LIMIT);
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);

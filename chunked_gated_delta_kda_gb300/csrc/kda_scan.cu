@@ -47,7 +47,7 @@ constexpr uint32_t S_S16 = S_OI + 4 * OI_PIECE;   // fp16 state copies: 3 x [K][
 constexpr uint32_t S_BAR = S_S16 + 3 * 8192;
 // barrier offsets (8 bytes each)
 constexpr uint32_t B_FULL = 0, B_QFULL = 16, B_OIFULL = 32, B_OIFREE = 64, B_MMAS = 96, B_MMAO = 104,
-                   B_OFREE = 120, B_S16 = 136, B_SFREE = 144;
+                   B_OFREE = 120, B_S16 = 136, B_SFREE = 144, B_DRAIN = 160;
 constexpr uint32_t S_TMEM = S_BAR + 192;
 constexpr uint32_t S_FLAG = S_TMEM + 4;
 constexpr uint32_t SCAN_SMEM = S_BAR + 256 + 1024;
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
     auto ofree = [&](int b) { return bars + B_OFREE + 8u * (uint32_t)b; };
     auto sfree = [&](int s) { return bars + B_SFREE + 8u * (uint32_t)s; };
     auto s16buf = [&](int j) { return S_S16 + (uint32_t)(j % 3) * 8192u; };
-    const uint32_t mmas = bars + B_MMAS, s16rdy = bars + B_S16;
+    const uint32_t mmas = bars + B_MMAS, s16rdy = bars + B_S16, drain = bars + B_DRAIN;
     volatile uint32_t* sFlag = reinterpret_cast<volatile uint32_t*>(sm + S_FLAG);
     if (warp == 0) {
         tmem_alloc(sbase + S_TMEM, 128);
@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
         }
         mbar_init(mmas, 1);
         mbar_init(s16rdy, 1);
+        mbar_init(drain, 1);
         fence_mbar_init();
         *sFlag = 0;
     }
@@ -159,14 +160,23 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + S_TMEM);
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
 
-    auto wait = [&](uint32_t bar, uint32_t parity) {
-        if (!mbar_wait(bar, parity, WAIT_LIMIT)) *sFlag = 1;
+    // A wait on another role.  When one runs out the CTA's flag is set and
+    // the role leaves its loop at once (one decision per role, taken by vote
+    // so that the role's barriers still match); a role waiting on a role that
+    // has left runs out in its turn, so the CTA is done within about two
+    // limits.  (Checking the flag before every wait instead cost ~10% here.)
+    const uint32_t wlim = wait_limit_of(p);
+    auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        if (mbar_wait(bar, parity, wlim)) return true;
+        *sFlag = 1;
+        return false;
     };
 
     if (warp < 4) {
         // ------------------------------------------------------------------
         // State: S' = Dg S + Nm S + Bc, row d = tid.
         // ------------------------------------------------------------------
+        bool alive = true;
         for (int j = 0; j < nch; ++j) {
             const int s = j & 1;
             if (p.ckpt != nullptr) {   // the state entering chunk j, row d, [K][V] layout
@@ -176,9 +186,11 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
                 for (int c4 = 0; c4 < BV / 4; ++c4)
                     ck[c4] = make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]);
             }
-            wait(full(s), (uint32_t)(j >> 1) & 1u);   // Bc / Dg of this chunk have landed
-            wait(mmas, (uint32_t)j & 1u);
+            bool ok = wait(full(s), (uint32_t)(j >> 1) & 1u);   // Bc / Dg of this chunk have landed
+            ok = ok && wait(mmas, (uint32_t)j & 1u);
+            ok = __all_sync(0xffffffffu, ok);               // warp-uniform before tcgen05.ld
             tc_fence_after();
+            if (ok) {
             const uint8_t* st = sm + (size_t)s * ST_STRIDE;
             float x[BV];
             tmem_ld32(tmem + lane_off, x);
@@ -207,15 +219,19 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
                 *reinterpret_cast<uint4*>(s16 + sw64_off(row, c8)) =
                     make_uint4(pack_f16x2(S[c8], S[c8 + 1]), pack_f16x2(S[c8 + 2], S[c8 + 3]),
                                pack_f16x2(S[c8 + 4], S[c8 + 5]), pack_f16x2(S[c8 + 6], S[c8 + 7]));
+            }
             fence_async_smem();
             tc_fence_before();
-            bar_sync_named(1, 128);
+            if (!bar_and_named(1, 128, ok)) {
+                alive = false;
+                break;
+            }
             if (tid == 0) {
                 mbar_arrive(s16rdy);      // next chunk's MMAs may start
                 mbar_arrive(sfree(s));    // Nm / Bc / Dg of stage s are consumed
             }
         }
-        if (p.ht != nullptr) {
+        if (alive && p.ht != nullptr) {
 #pragma unroll
             for (int j = 0; j < BV; ++j) p.ht[sbase_state + (size_t)(vt * BV + j) * KD + row] = S[j];
         }
@@ -226,17 +242,20 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
         // ------------------------------------------------------------------
         for (int j = 0; j < (p.o != nullptr ? nch : 0); ++j) {
             const int b = j & 1, r = j & 3;
-            wait(mmao(b), (uint32_t)(j >> 1) & 1u);
+            bool ok = wait(mmao(b), (uint32_t)(j >> 1) & 1u);
+            ok = __all_sync(0xffffffffu, ok);
             tc_fence_after();
             float y[BV];
-            tmem_ld32(tmem + lane_off + 32u + 32u * (uint32_t)b, y);
-            tmem_ld_wait();
+            if (ok) {
+                tmem_ld32(tmem + lane_off + 32u + 32u * (uint32_t)b, y);
+                tmem_ld_wait();
+            }
             tc_fence_before();
-            bar_sync_named(2, 128);
+            if (!bar_and_named(2, 128, ok)) break;
             if (tid == 128) mbar_arrive(ofree(b));
-            wait(oifull(r), (uint32_t)(j >> 2) & 1u);
+            ok = wait(oifull(r), (uint32_t)(j >> 2) & 1u);
             const int rows = len - j * BT < BT ? len - j * BT : BT;
-            if (row < rows) {
+            if (ok && row < rows) {
                 const uint8_t* oi_s = sm + S_OI + (uint32_t)r * OI_PIECE;
                 uint32_t w[BV / 2];
 #pragma unroll
@@ -255,7 +274,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
                 for (int q4 = 0; q4 < BV / 8; ++q4)
                     dst[q4] = make_uint4(w[q4 * 4 + 0], w[q4 * 4 + 1], w[q4 * 4 + 2], w[q4 * 4 + 3]);
             }
-            bar_sync_named(2, 128);
+            if (!bar_and_named(2, 128, ok)) break;
             if (tid == 128) mbar_arrive(oifree(r));
         }
     } else if (warp == 8) {
@@ -273,9 +292,10 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
             for (int j = 0; j <= nch; ++j) {
                 if (j < nch) {
                     const int s = j & 1;
-                    wait(full(s), (uint32_t)(j >> 1) & 1u);
-                    if (j >= 1) wait(s16rdy, (uint32_t)(j - 1) & 1u);
-                    __syncwarp();   // reconverge (the waits are bounded) before elect.sync
+                    bool ok = wait(full(s), (uint32_t)(j >> 1) & 1u);
+                    if (j >= 1) ok = ok && wait(s16rdy, (uint32_t)(j - 1) & 1u);
+                    // reconverged and warp-uniform before elect.sync
+                    if (!__all_sync(0xffffffffu, ok)) break;
                     tc_fence_after();
                     const uint64_t a_nm = s ? a_nm1 : a_nm0;
                     const uint64_t b_s = smem_desc(sbase + s16buf(j), 512u, 512u, SW_64B);
@@ -287,9 +307,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
                 }
                 if (j >= 1 && p.o != nullptr) {
                     const int c = j - 1, b = c & 1;
-                    wait(qfull(b), (uint32_t)(c >> 1) & 1u);
-                    if (c >= 2) wait(ofree(b), (uint32_t)((c - 2) >> 1) & 1u);
-                    __syncwarp();
+                    bool ok = wait(qfull(b), (uint32_t)(c >> 1) & 1u);
+                    if (c >= 2) ok = ok && wait(ofree(b), (uint32_t)((c - 2) >> 1) & 1u);
+                    if (!__all_sync(0xffffffffu, ok)) break;
                     tc_fence_after();
                     const uint64_t a_qe = b ? a_qe1 : a_qe0;
                     const uint64_t b_s = smem_desc(sbase + s16buf(c), 512u, 512u, SW_64B);
@@ -300,6 +320,9 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
                     mma_commit_warp(mmao(b));
                 }
             }
+            // every product issued above has completed before TMEM is freed
+            mma_commit_warp(drain);
+            mbar_wait(drain, 0, DRAIN_LIMIT);
         }
     } else {
         // ------------------------------------------------------------------
@@ -311,28 +334,47 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
         //   warp 10: Qe once its product of two chunks back has completed,
         //            Oi once its slot has been read.
         // ------------------------------------------------------------------
+        // Before the CTA exits each loader waits for the last copy it issued
+        // into every buffer slot (copies complete on their own); chunk c's
+        // copy completes phase c / (ring size) of its slot's barrier.  The
+        // last chunk per slot is kept in scalars (an indexed array here goes
+        // to local memory and slowed the scan by ~15%).
         if (warp == 9 && lane == 0) {
+            int last0 = -1, last1 = -1;   // last chunk loaded into stage 0 / 1
+            const bool drop = (p.debug & DEBUG_DROP_SCAN_LOAD) != 0u && n == 0 && h == 0 && vt == 0;
             for (int c = 0; c < nch; ++c) {
                 const int s = c & 1;
-                if (c >= 2) wait(sfree(s), (uint32_t)((c - 2) >> 1) & 1u);
+                if (c >= 2 && !wait(sfree(s), (uint32_t)((c - 2) >> 1) & 1u)) break;
+                if (drop && c == 1) continue;   // failure-detection test: this stage never arrives
                 load_stage(p, chunk_slot(p, n, c), h, vt, sbase + (uint32_t)s * ST_STRIDE, full(s));
+                if (s) last1 = c;
+                else last0 = c;
             }
+            if (last0 >= 0) mbar_wait(full(0), (uint32_t)(last0 >> 1) & 1u, DRAIN_LIMIT);
+            if (last1 >= 0) mbar_wait(full(1), (uint32_t)(last1 >> 1) & 1u, DRAIN_LIMIT);
         } else if (warp == 10 && lane == 0 && p.o != nullptr) {
+            int nq = 0, no = 0;           // chunks whose Qe / Oi copies were issued (in order)
             for (int c = 0; c < nch; ++c) {
                 const int s = c & 1, r = c & 3;
                 const uint8_t* src = tile_ptr(p, chunk_slot(p, n, c), h);
-                if (c >= 2) wait(mmao(s), (uint32_t)((c - 2) >> 1) & 1u);
+                if (c >= 2 && !wait(mmao(s), (uint32_t)((c - 2) >> 1) & 1u)) break;
                 load_piece(src + TILE_QE, BT * KD * 2, sbase + S_QE + (uint32_t)s * 32768u, qfull(s));
-                if (c >= 4) wait(oifree(r), (uint32_t)((c - 4) >> 2) & 1u);
+                nq = c + 1;
+                if (c >= 4 && !wait(oifree(r), (uint32_t)((c - 4) >> 2) & 1u)) break;
                 load_piece(src + TILE_OI + vt * OI_PIECE, OI_PIECE, sbase + S_OI + (uint32_t)r * OI_PIECE, oifull(r));
+                no = c + 1;
             }
+            for (int c = nq - 2 < 0 ? 0 : nq - 2; c < nq; ++c)
+                mbar_wait(qfull(c & 1), (uint32_t)(c >> 1) & 1u, DRAIN_LIMIT);
+            for (int c = no - 4 < 0 ? 0 : no - 4; c < no; ++c)
+                mbar_wait(oifull(c & 3), (uint32_t)(c >> 2) & 1u, DRAIN_LIMIT);
         }
     }
 
     __syncwarp();
-    if (*sFlag != 0 && tid == 0) atomicOr(p.status, STATUS_TIMEOUT);
     tc_fence_before();
     __syncthreads();
+    if (*sFlag != 0 && tid == 0) atomicOr(p.status, STATUS_TIMEOUT);
     if (warp == 0) tmem_dealloc(tmem, 128);
 }
 

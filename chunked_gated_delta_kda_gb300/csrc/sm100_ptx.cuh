@@ -64,6 +64,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
     return false;
 }
 
+// Named-barrier AND-reduction over `nthreads` threads: every thread gets
+// true iff every participant passed true.  Used to turn per-thread wait
+// results into one decision for a role before it leaves a loop together.
+__device__ __forceinline__ bool bar_and_named(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // ---------------------------------------------------------------------------
 // Bulk (non-tensor) async copies, global <-> shared, completion on mbarrier
 // (loads) or bulk groups (stores).  Addresses 16-byte aligned, size a

@@ -360,6 +360,28 @@ kda_status kda_bwd_timed(const void* q, const void* k, const void* v, const floa
 /* Static English description of a status code. */
 const char* kda_status_str(kda_status status);
 
+/*
+ * Test hooks for the failure detection of the bounded device waits (no
+ * counterpart on the pages; the pages' kernels have no such waits).  Every
+ * wait of one CTA role on another (tensor-core product done, bulk copy
+ * landed, a stage freed) polls at most a fixed number of times; when one
+ * runs out the CTA records KDA_ERR_TIMEOUT in the workspace status word,
+ * every later wait of that CTA returns at once, the CTA waits for the copies
+ * and products it issued itself, frees its tensor memory and exits.
+ *   KDA_DEBUG_WAIT_LIMIT: poll limit of those waits for the following calls
+ *     (value 0 restores the default, 2^24 polls).
+ *   KDA_DEBUG_DROP_SCAN_LOAD: the next kda_fwd only (the hook resets itself
+ *     when that call is enqueued): in the sequential scan, unit (sequence 0,
+ *     head 0), value tile 0 never issues the load of chunk 1's stage, so the
+ *     waits on it run out.  Needs a sequence of at least two chunks.
+ * The settings are process-wide and not synchronised: set them only while no
+ * other thread calls the library.  Returns KDA_ERR_INVALID_ARG for an
+ * unknown `what`.
+ */
+#define KDA_DEBUG_WAIT_LIMIT 1
+#define KDA_DEBUG_DROP_SCAN_LOAD 2
+kda_status kda_debug_set(int what, unsigned value);
+
 #ifdef __cplusplus
 }
 #endif

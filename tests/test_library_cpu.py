@@ -40,6 +40,21 @@ def test_flag_constants_match_the_header():
     assert len(set(flags.values())) == len(flags)
 
 
+def test_debug_constants_match_the_header():
+    """The KDA_DEBUG_* selectors of include/kda.h have the binding's values,
+    and kda_debug_set rejects an unknown selector without touching a GPU."""
+    import re
+    from chunked_gated_delta_kda_gb300 import binding
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    sel = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+(KDA_DEBUG_[A-Z0-9_]+)\s+(\d+)\b", text)}
+    assert sel == {"KDA_DEBUG_WAIT_LIMIT": 1, "KDA_DEBUG_DROP_SCAN_LOAD": 2}
+    for name, value in sel.items():
+        assert getattr(binding, name) == value
+    lib = binding.load_library()
+    assert lib.kda_debug_set(99, 0) == 1
+    assert lib.kda_debug_set(binding.KDA_DEBUG_WAIT_LIMIT, 0) == 0
+
+
 def test_workspace_bytes():
     from chunked_gated_delta_kda_gb300 import binding
     lib = binding.load_library()

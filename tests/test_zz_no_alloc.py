@@ -1,14 +1,13 @@
 """GPU test of kda_fwd_noalloc, the entry point for callers that cannot
 allocate device memory (stream capture, allocator callbacks, hosts that own
-every allocation).  It must give the same result as kda_fwd with a
-caller-provided workspace, call after call, and refuse problems that do not
+every allocation).  It must give bit for bit the result of kda_fwd
+with a caller-provided workspace (it runs the same kernels), call after call, and refuse problems that do not
 fit its static scratch.  This file is collected last on purpose."""
 
 import pytest
 import torch
 
 from chunked_gated_delta_kda_gb300.inputs import custom, make_inputs
-from kda_cases import O_ATOL, O_RTOL, S_ATOL, S_RTOL
 
 pytestmark = pytest.mark.gpu
 
@@ -41,8 +40,23 @@ def test_noalloc_matches_kda_fwd_on_consecutive_calls(w):
                                   seed=w.seed + 100 * call))
         o, ht, o_ref, ht_ref = _run_both(x)
         assert torch.isfinite(o.float()).all() and torch.isfinite(ht).all()
-        torch.testing.assert_close(o.float(), o_ref.float(), atol=O_ATOL, rtol=O_RTOL)
-        torch.testing.assert_close(ht, ht_ref, atol=S_ATOL, rtol=S_RTOL)
+        # the same kernels on the same inputs: bit-identical, not just close
+        assert torch.equal(o, o_ref)
+        assert torch.equal(ht, ht_ref)
+
+
+def test_noalloc_guarded_outputs():
+    """Outputs inside canary guards: the no-alloc call writes nothing outside
+    o and ht and gives kda_fwd's bits (two calls in a row: the second finds
+    the first one's leftovers in the shared scratch)."""
+    from kda_cases import run_gpu_guarded
+    for call in range(2):
+        w = custom("noalloc_guard", B=1, T=700, H=2, seqlens=[1, 128, 0, 571], with_h0=True, seed=64 + call)
+        x = make_inputs(w)
+        o, ht, ok = run_gpu_guarded(x, noalloc=True)
+        assert ok
+        o_ref, ht_ref, _ = run_gpu_guarded(x)
+        assert torch.equal(o, o_ref) and torch.equal(ht, ht_ref)
 
 
 def test_noalloc_rejects_problem_larger_than_scratch():
