@@ -41,6 +41,10 @@
 // (mma.sync, fp32 accumulation); the 64 -> 128 merge on tcgen05 with fp16
 // operands.  While one chunk computes, its successor's input rows are
 // prefetched into L2.
+#include <cuda.h>            // CUtensorMap (types only; the encoder comes through the runtime)
+#include <cudaTypedefs.h>
+#include <mutex>
+
 #include "kda_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -58,14 +62,18 @@ constexpr float EXP2_CAP = 115.0f;
 constexpr float FP16_SAFE = 16384.0f;
 
 // Shared-memory regions (bytes from the 1024-aligned base).
-//                      fast variant                      wide variant
-//   0      .. 64K :    Lk | v16   -> w | u               Lk | Lq -> qg | kg
-//   64K    .. 96K :    Lq                                R -> merge tiles -> Ainv
-//   96K    .. 128K:    R                                 RHS (k part) -> w
-//   128K   .. 160K:    merge tiles -> Ainv               RHS (v part) -> u
-//   160K   .. 208K:    scan sums -> fp32 diag blocks     qg stash -> fp32 diag
-//                      -> A2                             blocks -> A2
-constexpr uint32_t RM = 212992;            // misc
+//                  fast variant (layout 0 | layout 1)          wide variant
+//   0    .. 64K :  raw k | raw v -> Lk | v16 -> w | u          Lk | Lq -> qg | kg
+//   64K  .. 96K :  raw q -> Lq    | R                          R -> merge tiles -> Ainv
+//   96K  .. 128K:  R              | merge tiles -> Ainv        RHS (k part) -> w
+//   128K .. 160K:  merge tiles -> Ainv | raw q -> Lq           RHS (v part) -> u
+//   160K .. 208K:  fp32 diag blocks -> A2 (160K .. 192K)       qg stash -> fp32
+//                  -> output staging 1; prefix totals at 192K  diag blocks -> A2
+// Fast variant: chunks alternate between the two layouts, so that the next
+// chunk's raw q (in place of this chunk's inverse, or of its R) and raw k, v
+// (in place of w | u) can be loaded while this chunk's output tiles are
+// staged in 96K .. 128K and 160K .. 192K.
+constexpr uint32_t RM = 213248;            // misc
 constexpr uint32_t M_G64 = RM;             // f32[128]  G at the pivot row (log2 units)
 constexpr uint32_t M_GL = RM + 512;        // f32[128]  G at the last row (log2 units)
 constexpr uint32_t M_BETA = RM + 1024;     // f32[128]
@@ -77,6 +85,7 @@ constexpr uint32_t M_TOT = RM + 3584;      // f32[8][128] row-block sums (wide)
 constexpr uint32_t M_BAR = RM + 7680;      // mbarrier
 constexpr uint32_t M_BAR2 = RM + 7688;     // mbarrier of the second transition product
 constexpr uint32_t M_BARD = RM + 7696;     // mbarrier: every issued product done (before TMEM is freed)
+constexpr uint32_t M_RAWB = RM + 7704;     // mbarrier: a chunk's raw q / k / v tiles landed (fast variant)
 constexpr uint32_t M_TMEM = RM + 7744;     // TMEM base address
 constexpr uint32_t M_FLAG = RM + 7748;     // failure flag
 constexpr uint32_t SMEM_USED = RM + 7808;
@@ -89,7 +98,17 @@ constexpr int DS = 68;
 constexpr uint32_t W_DIAG = RW;                          // 2 x 64 x 68 floats = 34816 B
 constexpr uint32_t W_TMP = RW + 2 * 64 * DS * 4;         // merge temps, up to 10 KB
 static_assert(W_TMP + 2 * 1280 * 4 <= RM, "merge temps overlap the misc block");
+// fast variant: the gate prefix-scan totals ([32 row groups][129] fp32), clear
+// of the output staging buffers that may still be draining when they are written
+constexpr uint32_t W_TOT = 196608;
+static_assert(W_TOT + 32 * 129 * 4 <= RM, "prefix totals overlap the misc block");
+// fast variant: the two 32 KB staging buffers of the output tiles
+constexpr uint32_t ST0 = 98304;
+constexpr uint32_t ST1 = RW;
+static_assert(PREP_SMEM <= 232448, "shared memory above the 227 KB limit");
 
+// Fixed region map of the wide variant (the fast variant uses LK, B2 and WU
+// from it and takes Lq, R and the inverse's region from its chunk's layout).
 template <bool FAST>
 struct Map {
     static constexpr uint32_t LK = 0;
@@ -131,10 +150,6 @@ __device__ __forceinline__ void sts_v4(uint8_t* s, uint32_t off, uint32_t a, uin
                                        uint32_t d) {
     *reinterpret_cast<uint4*>(s + off) = make_uint4(a, b, c, d);
 }
-__device__ __forceinline__ void stg_v4(uint8_t* g, uint32_t off, uint32_t a, uint32_t b, uint32_t c,
-                                       uint32_t d) {
-    *reinterpret_cast<uint4*>(g + off) = make_uint4(a, b, c, d);
-}
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -164,13 +179,6 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
-}
-__device__ __forceinline__ uint4 ldg_ef_u4(const void* p, uint64_t pol) {
-    uint4 r;
-    asm("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p), "l"(pol));
-    return r;
 }
 __device__ __forceinline__ float4 ldg_ef_f4(const void* p, uint64_t pol) {
     float4 r;
@@ -291,9 +299,6 @@ __device__ __forceinline__ void sync_for_mma() {
     tc_fence_after();
 }
 
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p) : "memory");
-}
 
 __device__ __forceinline__ void prefetch_line(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
@@ -336,11 +341,13 @@ template <bool FAST>
 __device__ __forceinline__ bool fetch_item(const FwdParams& p, long long& idx, long long& item, ChunkRef& c,
                                            int& h) {
     if (FAST) {
-        const long long nitems = (long long)p.nslots * p.H;
-        while (idx < nitems) {
-            if (slot_chunk(p, (int)(idx / p.H), c)) {
+        // 32-bit index arithmetic (nslots * H < 2^31, checked on the host)
+        const uint32_t nitems = (uint32_t)p.nslots * (uint32_t)p.H;
+        while (idx < (long long)nitems) {
+            const uint32_t ui = (uint32_t)idx, slot = ui / (uint32_t)p.H;
+            if (slot_chunk(p, (int)slot, c)) {
                 item = idx;
-                h = (int)(idx % p.H);
+                h = (int)(ui - slot * (uint32_t)p.H);
                 return true;
             }
             idx += gridDim.x;
@@ -363,7 +370,9 @@ __device__ __forceinline__ bool fetch_item(const FwdParams& p, long long& idx, l
 }  // namespace
 
 template <bool L2NORM, bool FAST>
-__global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(PREP_THREADS, 1)
+    kda_prep_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v) {
     using MP = Map<FAST>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -376,9 +385,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     const int cg = warp >> 2;             // column group (0..3) for TMEM read-backs
     const uint32_t lane_off = (uint32_t)(lq * 32) << 16;
     const int trow = lq * 32 + lane;      // TMEM lane = matrix row of this thread
-    // one thread in each 128-thread group issues (and later waits for) one of
-    // the four bulk tile stores
-    const bool bulk_thread = (tid & 127) == 0;
+    // fast: thread 0 issues (and waits for) every bulk tile store and tensor
+    // load; wide: one thread in each 128-thread group issues one of the four
+    // bulk tile stores
+    const bool bulk_thread = FAST ? tid == 0 : (tid & 127) == 0;
 
     float* sG64 = reinterpret_cast<float*>(sm + M_G64);
     float* sGL = reinterpret_cast<float*>(sm + M_GL);
@@ -409,6 +419,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
         mbar_init(bar, 1);
         mbar_init(bar2, 1);
         mbar_init(sbase + M_BARD, 1);
+        mbar_init(sbase + M_RAWB, 1);
         fence_mbar_init();
         *sFlag = 0;
     }
@@ -417,6 +428,32 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + M_TMEM);
+
+    // Fast variant: a chunk's raw k, v and q tiles arrive by tensor-map loads
+    // (128-byte swizzled, the layout of the MMA operands) straight into the
+    // regions where the gated operands are then computed in place: k -> Lk,
+    // v -> the fp16 copy of v, q -> Lq.  Consecutive chunks of a CTA alternate
+    // between two region layouts so that the next chunk's loads can be issued
+    // while this chunk's output tiles are still being staged (layout 0 / 1:
+    // Lq at 64K / 128K, R at 96K / 64K, the inverse at 128K / 96K).
+    const uint32_t rawbar = sbase + M_RAWB;
+    uint32_t rphase = 0;
+    bool raw_pending = false;   // a raw load was issued and not yet waited for
+    auto issue_raw = [&](const ChunkRef& cc, int hh, int lay_n) {   // thread 0
+        const uint32_t qo = lay_n ? 131072u : 65536u;
+        mbar_arrive_expect_tx(rawbar, 3u * 32768u);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tma_load_3d(sbase + (uint32_t)half * 16384u, &tm_k, half * 64, hh, (int)cc.tok0, rawbar);
+            tma_load_3d(sbase + 32768u + (uint32_t)half * 16384u, &tm_v, half * 64, hh, (int)cc.tok0, rawbar);
+            tma_load_3d(sbase + qo + (uint32_t)half * 16384u, &tm_q, half * 64, hh, (int)cc.tok0, rawbar);
+        }
+    };
+    int lay = 0;
+    if (FAST) {
+        if (tid == 0) issue_raw(c, h, 0);
+        raw_pending = true;
+    }
 
     // Bounded waits: once one has run out (flag set), later ones of this CTA
     // return at once, the item finishes on whatever the tensor memory holds
@@ -434,13 +471,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     };
 
 
-    // fast variant: a chunk's beta, gate rows and first k / q / v row are
-    // loaded at the end of the previous chunk, before its tile stores are
-    // queued, so that the read requests leave the SM ahead of 128 KB of
-    // store data
+    // fast variant: a chunk's beta and gate rows are loaded into registers
+    // during the previous chunk's epilogue
     const uint64_t efp = evict_first_policy();
     float4 gpre[4][2];
-    uint4 kpre = make_uint4(0u, 0u, 0u, 0u), qpre = kpre, vpre = kpre;
     float bpre = 0.f;
     auto load_g = [&](const ChunkRef& cc, int hh, int r) {
         const int d8 = (tid & 15) * 8;
@@ -452,23 +486,14 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             gpre[r][1] = ldg_ef_f4(p.g + off + 4, efp);
         }
     };
-    auto load_first = [&](const ChunkRef& cc, int hh) {   // row 0 of k / q / v, and beta
-        const int d8 = (tid & 15) * 8;
-        const int tg0 = (tid >> 4) * 4;
+    auto load_beta = [&](const ChunkRef& cc, int hh) {
         const size_t r0 = (size_t)cc.tok0 * H + hh;
-        kpre = qpre = vpre = make_uint4(0u, 0u, 0u, 0u);
-        if (tg0 < cc.len) {
-            const size_t off = (r0 + (size_t)tg0 * H) * KD + d8;
-            kpre = ldg_ef_u4(p.k + off, efp);
-            qpre = ldg_ef_u4(p.q + off, efp);
-            vpre = ldg_ef_u4(p.v + off, efp);
-        }
         bpre = (tid < BT && tid < cc.len) ? __ldg(p.beta + r0 + (size_t)tid * H) : 0.f;
     };
     auto load_rows = [&](const ChunkRef& cc, int hh) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) load_g(cc, hh, r);
-        load_first(cc, hh);
+        load_beta(cc, hh);
     };
     ChunkRef none{};   // zero rows: loads nothing, defines the registers
     none.len = 0;
@@ -481,6 +506,11 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
         const bool have_n = fetch_item<FAST>(p, nidx, nitem, cn, hn);
         const int len = c.len;
         const size_t row0 = (size_t)c.tok0 * H + h;
+        // region offsets of this chunk: the fast variant's alternating layout,
+        // or the wide variant's fixed map
+        const uint32_t oLQ = FAST ? (lay ? 131072u : 65536u) : MP::LQ;
+        const uint32_t oRR = FAST ? (lay ? 65536u : 98304u) : MP::RR;
+        const uint32_t oY = FAST ? (lay ? 98304u : 131072u) : MP::Y;
 
         // ------------------------------------------------------------------
         // Per-row scalars: beta, and the q / k scalings (scale, optional
@@ -530,19 +560,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             const int grp = tid >> 4;
             const int tg0 = grp * 4;
             float G[4][8];
-            // k, q, v rows are loaded one row ahead of their use (row 0 with
-            // the gate), so each row's loads are in flight before the
-            // previous row's shared-memory stores.
-            // the thread's second row of k, q, v into L1 while the prefix scan
-            // runs (the third and fourth as well would overflow the L1 left
-            // beside this kernel's shared memory)
-            if (tg0 + 1 < len) {
-                const size_t off = (row0 + (size_t)(tg0 + 1) * H) * KD + d8;
-                prefetch_l1(p.k + off);
-                prefetch_l1(p.q + off);
-                prefetch_l1(p.v + off);
-            }
-            uint4 kn = kpre, qn = qpre, vn = vpre;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const float4 ga = gpre[r][0], gb = gpre[r][1];
@@ -552,7 +569,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             // [32 groups][129]: the odd row stride keeps the column-wise
             // prefix scan free of shared-memory bank conflicts
             constexpr int TS = 129;
-            float* tot = reinterpret_cast<float*>(sm + RW);
+            float* tot = reinterpret_cast<float*>(sm + W_TOT);
             {
                 float acc[8];
 #pragma unroll
@@ -569,19 +586,22 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             }
             __syncthreads();
             {                           // exclusive prefix over the 32 row groups:
-                // warp w scans dimensions 8w .. 8w+7, lane = row group
+                // warp w scans dimensions 8w .. 8w+7, lane = row group; the
+                // eight scans are interleaved (all loads, then the shuffle
+                // steps, then all stores) rather than run one after another
+                float xs[8], incl[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int d = warp * 8 + j;
-                    const float x = tot[lane * TS + d];
-                    float incl = x;
+                for (int j = 0; j < 8; ++j) xs[j] = incl[j] = tot[lane * TS + warp * 8 + j];
 #pragma unroll
-                    for (int s2 = 1; s2 < 32; s2 <<= 1) {
-                        const float y = __shfl_up_sync(0xffffffffu, incl, s2);
-                        if (lane >= s2) incl += y;
+                for (int s2 = 1; s2 < 32; s2 <<= 1) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float y = __shfl_up_sync(0xffffffffu, incl[j], s2);
+                        if (lane >= s2) incl[j] += y;
                     }
-                    tot[lane * TS + d] = incl - x;
                 }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) tot[lane * TS + warp * 8 + j] = incl[j] - xs[j];
             }
             __syncthreads();
             {
@@ -614,20 +634,20 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
 #pragma unroll
                 for (int r = 0; r < 4; ++r) G[r][j] -= P;
             }
+            // this chunk's raw k, v, q tiles have landed (rows past the
+            // sequence's end hold other tokens or zeros: read as zero)
+            bounded_wait(rawbar, rphase);
+            rphase ^= 1;
+            raw_pending = false;
             float m = 0.f;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int t = tg0 + r;
-                const uint4 kc = kn, qc = qn, vc = vn;
-                if (r < 3) {
-                    kn = qn = vn = make_uint4(0u, 0u, 0u, 0u);
-                    if (t + 1 < len) {
-                        const size_t off = (row0 + (size_t)(t + 1) * H) * KD + d8;
-                        kn = ldg_ef_u4(p.k + off, efp);
-                        qn = ldg_ef_u4(p.q + off, efp);
-                        vn = ldg_ef_u4(p.v + off, efp);
-                    }
-                }
+                const uint32_t off = sw128_off(t, d8, 128);
+                uint4 kc = *reinterpret_cast<const uint4*>(sm + off);
+                uint4 vc = *reinterpret_cast<const uint4*>(sm + 32768 + off);
+                uint4 qc = *reinterpret_cast<const uint4*>(sm + oLQ + off);
+                if (t >= len) kc = vc = qc = make_uint4(0u, 0u, 0u, 0u);
                 float kf[8], qf[8], vf[8];
                 unpack8_bf16(kc, kf);
                 unpack8_bf16(qc, qf);
@@ -650,11 +670,12 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                     rk[j / 2] = pack_f16(c0, c1);
                     v16[j / 2] = pack_f16(vf[j], vf[j + 1]);
                 }
-                const uint32_t off = sw128_off(t, d8, 128);
-                sts_v4(sm, MP::LK + off, lk[0], lk[1], lk[2], lk[3]);
-                sts_v4(sm, MP::LK + 32768 + off, v16[0], v16[1], v16[2], v16[3]);
-                sts_v4(sm, MP::LQ + off, lqv[0], lqv[1], lqv[2], lqv[3]);
-                sts_v4(sm, MP::RR + off, rk[0], rk[1], rk[2], rk[3]);
+                // in place over the raw tiles (each thread rewrites the 16
+                // bytes it read), R into its own region
+                sts_v4(sm, off, lk[0], lk[1], lk[2], lk[3]);
+                sts_v4(sm, 32768 + off, v16[0], v16[1], v16[2], v16[3]);
+                sts_v4(sm, oLQ + off, lqv[0], lqv[1], lqv[2], lqv[3]);
+                sts_v4(sm, oRR + off, rk[0], rk[1], rk[2], rk[3]);
             }
             unsafe = !(m <= FP16_SAFE);
         } else {
@@ -768,15 +789,18 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             if (tid == 0) {
                 const uint32_t slot_i = atomicAdd(p.wide_count, 1u);
                 p.wide_list[slot_i] = (int32_t)item;
+                // the next chunk's raw tiles go to regions this chunk no
+                // longer needs (its operands are dropped)
+                if (FAST && have_n) issue_raw(cn, hn, lay ^ 1);
             }
+            if (FAST && have_n) raw_pending = true;
             if (have_n) prefetch_chunk(p, cn, hn, tid);
             if (FAST) load_rows(have_n ? cn : none, hn);
             __syncthreads();
         } else {
             if (tid == 0) {
                 const uint32_t id = idesc_f16(FAST ? T_F16 : T_BF16, 128, 128, false, false);
-                const Operand Lk{sbase + MP::LK, false, 128}, Lq{sbase + MP::LQ, false, 128},
-                    R{sbase + MP::RR, false, 128};
+                const Operand Lk{sbase + MP::LK, false, 128}, Lq{sbase + oLQ, false, 128}, R{sbase + oRR, false, 128};
                 mma_128(tmem + 0, Lk, R, id, 8);     // A_raw  -> cols [0,128)
                 mma_128(tmem + 128, Lq, R, id, 8);   // A2_raw -> cols [128,256)
                 mma_commit(bar);
@@ -825,7 +849,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                     if (trow >= 64 && col0 < 64) {
 #pragma unroll
                         for (int j = 0; j < 32; j += 8)
-                            sts_v4(sm, MP::YA + sw128_off(trow - 64, col0 + j, 64), pack_f16(x[j], x[j + 1]),
+                            sts_v4(sm, oY + sw128_off(trow - 64, col0 + j, 64), pack_f16(x[j], x[j + 1]),
                                    pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]),
                                    pack_f16(x[j + 6], x[j + 7]));
                     } else {
@@ -911,14 +935,14 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 const int r = e >> 5, c2 = (e & 31) * 2;
                 const float* Pp = Wd + r * DS + c2;
                 const float* Qp = Wd + 64 * DS + r * DS + c2;
-                sts_u32(sm, MP::YP + sw128_off(r, c2, 64),
+                sts_u32(sm, oY + 8192u + sw128_off(r, c2, 64),
                         pack_f16(Pp[0] + (r == c2 ? 1.f : 0.f), Pp[1] + (r == c2 + 1 ? 1.f : 0.f)));
-                sts_u32(sm, MP::YQ + sw128_off(r, c2, 64),
+                sts_u32(sm, oY + 16384u + sw128_off(r, c2, 64),
                         pack_f16(Qp[0] + (r == c2 ? 1.f : 0.f), Qp[1] + (r == c2 + 1 ? 1.f : 0.f)));
             }
             sync_for_mma();
             if (tid == 0) {
-                const Operand A10{sbase + MP::YA, false, 64}, Ph{sbase + MP::YP, true, 64};
+                const Operand A10{sbase + oY, false, 64}, Ph{sbase + oY + 8192u, true, 64};
                 mma_128(tmem + 0, A10, Ph, idesc_f16(T_F16, 128, 64, false, true), 4);   // T -> cols [0,64)
                 mma_commit(bar);
             }
@@ -934,7 +958,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             }
             sync_for_mma();
             if (tid == 0) {
-                const Operand Qh{sbase + MP::YQ, false, 64}, Th{sbase + W_TMP, true, 64};
+                const Operand Qh{sbase + oY + 16384u, false, 64}, Th{sbase + W_TMP, true, 64};
                 mma_128(tmem + 64, Qh, Th, idesc_f16(T_F16, 128, 64, false, true, /*neg_a=*/true), 4);  // L
                 mma_commit(bar);
             }
@@ -954,7 +978,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                     x[e] += (c0 + e == r) ? 1.f : 0.f;
                     if (FAST) x[e] *= sBeta[c0 + e];
                 }
-                sts_v4(sm, MP::Y + sw128_off(r, c0, 128), pack_f16(x[0], x[1]), pack_f16(x[2], x[3]),
+                sts_v4(sm, oY + sw128_off(r, c0, 128), pack_f16(x[0], x[1]), pack_f16(x[2], x[3]),
                        pack_f16(x[4], x[5]), pack_f16(x[6], x[7]));
             };
             for (int ch = tid; ch < 1024; ch += PREP_THREADS) {
@@ -972,12 +996,12 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
                 }
 #pragma unroll
                 for (int j = 0; j < 16; j += 8)
-                    sts_v4(sm, MP::Y + sw128_off(64 + trow, cg * 16 + j, 128), pack_f16(x[j], x[j + 1]),
+                    sts_v4(sm, oY + sw128_off(64 + trow, cg * 16 + j, 128), pack_f16(x[j], x[j + 1]),
                            pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]), pack_f16(x[j + 6], x[j + 7]));
             }
             if (tid < 512) {                 // zeros: rows 0..63, cols 64..127
                 const int r = tid >> 3, c0 = 64 + (tid & 7) * 8;
-                sts_v4(sm, MP::Y + sw128_off(r, c0, 128), 0u, 0u, 0u, 0u);
+                sts_v4(sm, oY + sw128_off(r, c0, 128), 0u, 0u, 0u, 0u);
             }
             sync_for_mma();
 
@@ -987,7 +1011,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             //   wide: Ainv [beta exp(G) k | beta v]
             // --------------------------------------------------------------
             if (tid == 0) {
-                const Operand Ai{sbase + MP::Y, false, 128}, Rh{sbase + MP::B2, true, 128};
+                const Operand Ai{sbase + oY, false, 128}, Rh{sbase + MP::B2, true, 128};
                 mma_128(tmem + 256, Ai, Rh, idesc_f16(T_F16, 128, 256, false, true), 8);
                 mma_commit(bar);
             }
@@ -1031,7 +1055,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             // epilogue of the first runs while the second computes.
             // --------------------------------------------------------------
             if (tid == 0) {
-                const Operand KgT{sbase + MP::KGT, true, 128}, A2h{sbase + RW, false, 128},
+                const Operand KgT{sbase + (FAST ? oRR : MP::KGT), true, 128}, A2h{sbase + RW, false, 128},
                     WU{sbase + MP::WU, true, 128};
                 mma_128(tmem + 256, A2h, WU, idesc_f16(T_F16, 128, 256, false, true), 8);
                 mma_commit(bar);
@@ -1041,30 +1065,128 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
             wait_mma();
 
             // --------------------------------------------------------------
-            // Phase 7: epilogue, straight from TMEM to the workspace tile.
-            //   warps 0-7:  lanes = d;  Nm = -cL (X^T w), Bc = cL X^T u
-            //               (cL = exp(G_last - P) for the fast variant, else 1)
-            //   warps 8-15: lanes = t;  Qe = qg - A2 w, Oi = A2 u
-            //               (fast: qg = Lq diag(exp(P)))
+            // Phase 7 (fast variant): epilogue through two 32 KB staging
+            // buffers, one product at a time, each bulk-stored as soon as it
+            // is staged; the buffer is reused once its store has read it.
+            //   Qe = Lq diag(exp(P)) - A2 w -> ST1 (the A2 operand's region)
+            //   [second product done: the next chunk's raw tiles are loaded
+            //    into this chunk's w | u and inverse / R regions]
+            //   Oi = A2 u -> ST0;  Nm = -cL R^T w -> ST1;  Bc = cL R^T u -> ST0
+            // Thread w%4 lane quarter = row (t or d), columns 32 (w / 4) ..
             // --------------------------------------------------------------
-            {
+            if constexpr (FAST) {
+                uint8_t* dst = tile_ptr(p, c.slot, h);
+                const ChunkRef& cx = have_n ? cn : none;
+                const int col0 = cg * 32;
+                float x[32];
+                // Qe (rows t): qg from Lq (fp16) times exp(P), minus A2 w
+                tmem_ld32(tmem + lane_off + 256u + (uint32_t)col0, x);
+                tmem_ld_wait();
+                load_g(cx, hn, 0);
+                load_g(cx, hn, 1);
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) {
+                    const uint4 qv = *reinterpret_cast<const uint4*>(sm + oLQ + sw128_off(trow, col0 + j, 128));
+                    float2 g0 = unpack_f16(qv.x), g1 = unpack_f16(qv.y), g2 = unpack_f16(qv.z), g3 = unpack_f16(qv.w);
+                    const float4 e0 = *reinterpret_cast<const float4*>(sEP + col0 + j);
+                    const float4 e1 = *reinterpret_cast<const float4*>(sEP + col0 + j + 4);
+                    g0.x *= e0.x; g0.y *= e0.y; g1.x *= e0.z; g1.y *= e0.w;
+                    g2.x *= e1.x; g2.y *= e1.y; g3.x *= e1.z; g3.y *= e1.w;
+                    sts_v4(sm, ST1 + sw128_off(trow, col0 + j, 128), pack_f16(g0.x - x[j], g0.y - x[j + 1]),
+                           pack_f16(g1.x - x[j + 2], g1.y - x[j + 3]), pack_f16(g2.x - x[j + 4], g2.y - x[j + 5]),
+                           pack_f16(g3.x - x[j + 6], g3.y - x[j + 7]));
+                }
+                fence_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+                    bulk_s2g(dst + TILE_QE, sbase + ST1, BT * KD * 2);
+                    bulk_commit();
+                }
+                load_g(cx, hn, 2);
+                load_g(cx, hn, 3);
+                // R^T [w | u] done: w | u, R and the inverse are free
+                bounded_wait(bar2, phase2);
+                phase2 ^= 1;
+                tc_fence_after();
+                if (tid == 0 && have_n) issue_raw(cn, hn, lay ^ 1);
+                if (have_n) raw_pending = true;
+                // Oi (rows t) -> its 32-column piece cg
+                tmem_ld32(tmem + lane_off + 384u + (uint32_t)col0, x);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; j += 8)
+                    sts_v4(sm, ST0 + (uint32_t)cg * OI_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
+                           pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]), pack_f16(x[j + 6], x[j + 7]));
+                fence_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+                    bulk_s2g(dst + TILE_OI, sbase + ST0, NVT * OI_PIECE);
+                    bulk_commit();
+                    bulk_wait_read1();   // the Qe store has read ST1
+                }
+                load_beta(cx, hn);
+                // Nm (rows d) = -cL R^T w
+                const float rs = sCL[trow];
+                tmem_ld32(tmem + lane_off + (uint32_t)col0, x);
+                tmem_ld_wait();
+                __syncthreads();
+                {
+                    const float ns = -rs;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8)
+                        sts_v4(sm, ST1 + sw128_off(trow, col0 + j, 128), pack_f16(ns * x[j], ns * x[j + 1]),
+                               pack_f16(ns * x[j + 2], ns * x[j + 3]), pack_f16(ns * x[j + 4], ns * x[j + 5]),
+                               pack_f16(ns * x[j + 6], ns * x[j + 7]));
+                }
+                fence_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+                    bulk_s2g(dst + TILE_NM, sbase + ST1, KD * KD * 2);
+                    bulk_commit();
+                    bulk_wait_read1();   // the Oi store has read ST0
+                }
+                // Bc (rows d) = cL R^T u -> its 32-column piece cg
+                tmem_ld32(tmem + lane_off + 128u + (uint32_t)col0, x);
+                tmem_ld_wait();
+                __syncthreads();
+#pragma unroll
+                for (int j = 0; j < 32; j += 8)
+                    sts_v4(sm, ST0 + (uint32_t)cg * BC_PIECE + sw64_off(trow, j), pack_f16(rs * x[j], rs * x[j + 1]),
+                           pack_f16(rs * x[j + 2], rs * x[j + 3]), pack_f16(rs * x[j + 4], rs * x[j + 5]),
+                           pack_f16(rs * x[j + 6], rs * x[j + 7]));
+                if (tid < 32) {
+                    float4 dg;
+                    dg.x = ex2(sGL[tid * 4 + 0]);
+                    dg.y = ex2(sGL[tid * 4 + 1]);
+                    dg.z = ex2(sGL[tid * 4 + 2]);
+                    dg.w = ex2(sGL[tid * 4 + 3]);
+                    *reinterpret_cast<float4*>(dst + TILE_DG + tid * 16) = dg;
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncthreads();
+                tc_fence_after();
+                if (tid == 0) {   // asynchronous: drains while the next chunk starts
+                    bulk_s2g(dst + TILE_BC, sbase + ST0, NVT * BC_PIECE);
+                    bulk_commit();
+                }
+            } else {
+                // ----------------------------------------------------------
+                // Phase 7 (wide variant): epilogue, straight from TMEM to the
+                // workspace tile.
+                //   warps 0-7:  lanes = d;  Nm = -cL (X^T w), Bc = cL X^T u
+                //               (cL = exp(G_last - P) for the fast variant, else 1)
+                //   warps 8-15: lanes = t;  Qe = qg - A2 w, Oi = A2 u
+                // ----------------------------------------------------------
                 uint8_t* dst = tile_ptr(p, c.slot, h);
                 // 32-column blocks of the four products (kind 0 Nm, 1 Bc, 2 Qe,
                 // 3 Oi; TMEM columns kind * 128 + vt * 32).  The four warps of a
                 // lane quarter each take one Qe block, one Oi block and two Nm
                 // or two Bc blocks: Qe costs about twice the others.
                 const int role = warp >> 2;
-                const float rs = FAST ? sCL[trow] : 1.f;   // rows d of Nm / Bc
-                const ChunkRef& cx = have_n ? cn : none;
+                const float rs = 1.f;   // rows d of Nm / Bc (kg already carries exp(G_last - G))
 #pragma unroll
                 for (int part = 0; part < 4; ++part) {
-                    // the next chunk's first loads, spread over the parts so
-                    // that their requests do not queue up behind each other
-                    if (FAST) {
-                        if (part == 0) { load_g(cx, hn, 0); load_g(cx, hn, 1); }
-                        if (part == 1) { load_g(cx, hn, 2); load_g(cx, hn, 3); }
-                        if (part == 2) load_first(cx, hn);
-                    }
                     if (part == 2) {   // Nm | Bc: the second product
                         bounded_wait(bar2, phase2);
                         phase2 ^= 1;
@@ -1152,10 +1274,14 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
         c = cn;
         h = hn;
         have = have_n;
+        lay ^= 1;
     }
     if (bulk_thread) bulk_wait0();
     if (tid == 0) {
         if (*sFlag != 0) atomicOr(p.status, STATUS_TIMEOUT);
+        // a chunk's raw tiles issued before the loop ended (after a timeout)
+        // have landed before the shared memory is released
+        if (FAST && raw_pending) mbar_wait(rawbar, rphase, DRAIN_LIMIT);
         // every product this thread issued has completed before TMEM is freed
         mma_commit(sbase + M_BARD);
         mbar_wait(sbase + M_BARD, 0, DRAIN_LIMIT);
@@ -1165,12 +1291,47 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) kda_prep_kernel(const FwdPara
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+namespace {
+
+// The driver's tensor-map encoder, found once through the runtime (no link
+// against the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// q, k or v ([tokens][H][128] bf16) as a 3-D tensor (dimension, head, token):
+// one load brings 64 dimensions of one head for 128 consecutive tokens, in
+// the 128-byte swizzled layout of the MMA operands; tokens past the end read
+// as zero.
+bool make_row_map(CUtensorMap* m, const void* base, int H, long long ntok) {
+    const PFN_cuTensorMapEncodeTiled_v12000 fn = tmap_encoder();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)KD, (cuuint64_t)H, (cuuint64_t)ntok};
+    const cuuint64_t strides[2] = {(cuuint64_t)KD * 2u, (cuuint64_t)H * KD * 2u};
+    const cuuint32_t box[3] = {64u, 1u, (cuuint32_t)BT};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 template <bool L2NORM, bool FAST>
-static cudaError_t launch_one(const FwdParams& p, unsigned grid, cudaStream_t stream) {
+static cudaError_t launch_one(const FwdParams& p, const CUtensorMap (&tm)[3], unsigned grid, cudaStream_t stream) {
     cudaError_t e =
         cudaFuncSetAttribute(kda_prep_kernel<L2NORM, FAST>, cudaFuncAttributeMaxDynamicSharedMemorySize, PREP_SMEM);
     if (e != cudaSuccess) return e;
-    kda_prep_kernel<L2NORM, FAST><<<grid, PREP_THREADS, PREP_SMEM, stream>>>(p);
+    kda_prep_kernel<L2NORM, FAST><<<grid, PREP_THREADS, PREP_SMEM, stream>>>(p, tm[0], tm[1], tm[2]);
     return cudaGetLastError();
 }
 
@@ -1186,9 +1347,15 @@ cudaError_t launch_prep(const FwdParams& p, bool l2norm, cudaStream_t stream) {
     const long long items = (long long)p.nslots * p.H;
     const unsigned grid = (unsigned)(items < sms ? items : sms);
     if (grid == 0) return cudaSuccess;
-    e = l2norm ? launch_one<true, true>(p, grid, stream) : launch_one<false, true>(p, grid, stream);
+    const long long ntok = p.cu != nullptr ? (long long)p.T : (long long)p.N * p.T;
+    if (ntok == 0) return cudaSuccess;   // no tokens: every chunk slot is empty
+    CUtensorMap tm[3];
+    if (!make_row_map(&tm[0], p.q, p.H, ntok) || !make_row_map(&tm[1], p.k, p.H, ntok) ||
+        !make_row_map(&tm[2], p.v, p.H, ntok))
+        return cudaErrorInvalidValue;
+    e = l2norm ? launch_one<true, true>(p, tm, grid, stream) : launch_one<false, true>(p, tm, grid, stream);
     if (e != cudaSuccess) return e;
-    return l2norm ? launch_one<true, false>(p, grid, stream) : launch_one<false, false>(p, grid, stream);
+    return l2norm ? launch_one<true, false>(p, tm, grid, stream) : launch_one<false, false>(p, tm, grid, stream);
 }
 
 }  // namespace kda
