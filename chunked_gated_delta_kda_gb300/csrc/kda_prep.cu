@@ -585,23 +585,29 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                 for (int j = 0; j < 8; ++j) tot[grp * TS + d8 + j] = acc[j];
             }
             __syncthreads();
-            {                           // exclusive prefix over the 32 row groups:
-                // warp w scans dimensions 8w .. 8w+7, lane = row group; the
-                // eight scans are interleaved (all loads, then the shuffle
-                // steps, then all stores) rather than run one after another
-                float xs[8], incl[8];
+            {   // exclusive prefix over the 32 row groups, four threads per
+                // dimension: thread (d = tid / 4, quarter qq = tid % 4) scans
+                // groups 8 qq .. 8 qq + 7 in order, then adds the totals of
+                // the lower quarters (two shuffle steps among its 4 lanes)
+                const int d = tid >> 2, qq = tid & 3;
+                float v[8], run = 0.f;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) xs[j] = incl[j] = tot[lane * TS + warp * 8 + j];
+                for (int i = 0; i < 8; ++i) v[i] = tot[(8 * qq + i) * TS + d];
 #pragma unroll
-                for (int s2 = 1; s2 < 32; s2 <<= 1) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float y = __shfl_up_sync(0xffffffffu, incl[j], s2);
-                        if (lane >= s2) incl[j] += y;
-                    }
+                for (int i = 0; i < 8; ++i) {
+                    const float x = v[i];
+                    v[i] = run;
+                    run += x;
                 }
+                float incl = run;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) tot[lane * TS + warp * 8 + j] = incl[j] - xs[j];
+                for (int s2 = 1; s2 < 4; s2 <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, incl, s2, 4);
+                    if (qq >= s2) incl += y;
+                }
+                const float base = incl - run;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) tot[(8 * qq + i) * TS + d] = base + v[i];
             }
             __syncthreads();
             {
@@ -647,7 +653,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                 uint4 kc = *reinterpret_cast<const uint4*>(sm + off);
                 uint4 vc = *reinterpret_cast<const uint4*>(sm + 32768 + off);
                 uint4 qc = *reinterpret_cast<const uint4*>(sm + oLQ + off);
-                if (t >= len) kc = vc = qc = make_uint4(0u, 0u, 0u, 0u);
+                if (len < BT && t >= len) kc = vc = qc = make_uint4(0u, 0u, 0u, 0u);   // tail chunks only
                 float kf[8], qf[8], vf[8];
                 unpack8_bf16(kc, kf);
                 unpack8_bf16(qc, qf);

@@ -35,6 +35,9 @@ namespace kda {
 namespace {
 
 constexpr int SCAN_THREADS = 352;
+// the loaders also prefetch the tiles this many chunks ahead into L2, so
+// that the stage loads (two chunks ahead) find them there rather than in DRAM
+constexpr int PF_AHEAD = 4;
 // stage: Nm | Bc piece | Dg
 constexpr uint32_t ST_NM = 0;
 constexpr uint32_t ST_BC = 32768;
@@ -347,6 +350,12 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
                 if (c >= 2 && !wait(sfree(s), (uint32_t)((c - 2) >> 1) & 1u)) break;
                 if (drop && c == 1) continue;   // failure-detection test: this stage never arrives
                 load_stage(p, chunk_slot(p, n, c), h, vt, sbase + (uint32_t)s * ST_STRIDE, full(s));
+                if (c + PF_AHEAD < nch) {   // the stage PF_AHEAD chunks on into L2
+                    const uint8_t* pf = tile_ptr(p, chunk_slot(p, n, c + PF_AHEAD), h);
+                    bulk_prefetch_l2(pf + TILE_NM, KD * KD * 2);
+                    bulk_prefetch_l2(pf + TILE_BC + vt * BC_PIECE, BC_PIECE);
+                    bulk_prefetch_l2(pf + TILE_DG, KD * 4);
+                }
                 if (s) last1 = c;
                 else last0 = c;
             }
@@ -360,6 +369,11 @@ __global__ void __launch_bounds__(SCAN_THREADS, 1) kda_scan_kernel(const FwdPara
                 if (c >= 2 && !wait(mmao(s), (uint32_t)((c - 2) >> 1) & 1u)) break;
                 load_piece(src + TILE_QE, BT * KD * 2, sbase + S_QE + (uint32_t)s * 32768u, qfull(s));
                 nq = c + 1;
+                if (c + PF_AHEAD < nch) {
+                    const uint8_t* pf = tile_ptr(p, chunk_slot(p, n, c + PF_AHEAD), h);
+                    bulk_prefetch_l2(pf + TILE_QE, BT * KD * 2);
+                    bulk_prefetch_l2(pf + TILE_OI + vt * OI_PIECE, OI_PIECE);
+                }
                 if (c >= 4 && !wait(oifree(r), (uint32_t)((c - 4) >> 2) & 1u)) break;
                 load_piece(src + TILE_OI + vt * OI_PIECE, OI_PIECE, sbase + S_OI + (uint32_t)r * OI_PIECE, oifull(r));
                 no = c + 1;
