@@ -1,7 +1,8 @@
 // kda_fwd_noalloc: the chunked KDA forward for callers that cannot allocate
-// device memory at all -- for example code running inside a CUDA graph
-// capture or a custom allocator's callback, a plug-in host that owns every
-// allocation itself, or an embedded runtime with a fixed memory budget.  It
+// device memory at all -- for example code running inside a custom
+// allocator's own callback (allocating there would re-enter the allocator),
+// a plug-in inside a host application that owns every allocation itself, or
+// an embedded runtime with a fixed memory budget decided up front.  It
 // runs the same kernels as kda_fwd, with the workspace taken from a static
 // device array that is part of this library (every GPU that loads the
 // library holds it until the process exits) instead of from the caller.

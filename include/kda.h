@@ -160,10 +160,12 @@ kda_status kda_get_status(const void* workspace, cudaStream_t stream);
 #define KDA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 
 /*
- * kda_fwd for callers that cannot allocate device memory (code running while
- * a stream is being captured into a CUDA graph, inside an allocator callback,
- * or under a host application that owns every allocation).  No counterpart
- * on the method's pages: it is a deployment convenience of this library.
+ * kda_fwd for callers that cannot allocate device memory: code running
+ * inside a custom allocator's own callback (allocating there would re-enter
+ * the allocator), a plug-in whose host application owns every allocation, or
+ * a runtime with a fixed device-memory budget decided up front.  No
+ * counterpart on the method's pages: it is a deployment convenience of this
+ * library.
  *
  * Same arguments, layouts and precision as kda_fwd, minus the workspace: the
  * library uses a static __device__ array of KDA_NOALLOC_SCRATCH_BYTES that

@@ -1,6 +1,6 @@
 """GPU test of kda_fwd_noalloc, the entry point for callers that cannot
-allocate device memory (stream capture, allocator callbacks, hosts that own
-every allocation).  It must give bit for bit the result of kda_fwd
+allocate device memory (code inside an allocator's own callback, plug-ins
+whose host owns every allocation, fixed memory budgets).  It must give bit for bit the result of kda_fwd
 with a caller-provided workspace (it runs the same kernels), call after call, and refuse problems that do not
 fit its static scratch.  This file is collected last on purpose."""
 
