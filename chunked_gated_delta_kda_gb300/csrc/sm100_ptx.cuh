@@ -114,6 +114,11 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Wait until at most two committed bulk store groups are still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read2() {
+    asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
+}
+
 // Wait until at most one committed bulk store group is still reading shared memory.
 __device__ __forceinline__ void bulk_wait_read1() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
