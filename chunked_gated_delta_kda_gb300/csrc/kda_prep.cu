@@ -1191,13 +1191,13 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                 // or two Bc blocks: Qe costs about twice the others.
                 const int role = warp >> 2;
                 const float rs = 1.f;   // rows d of Nm / Bc (kg already carries exp(G_last - G))
+                // Qe and Oi are staged over w | u, the operands of the second
+                // product: it has completed before the first part is staged
+                bounded_wait(bar2, phase2);
+                phase2 ^= 1;
+                tc_fence_after();
 #pragma unroll
                 for (int part = 0; part < 4; ++part) {
-                    if (part == 2) {   // Nm | Bc: the second product
-                        bounded_wait(bar2, phase2);
-                        phase2 ^= 1;
-                        tc_fence_after();
-                    }
                     float x[32];
                     int kind, vt;
                     if (part < 2) {
