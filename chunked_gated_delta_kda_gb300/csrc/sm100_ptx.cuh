@@ -114,11 +114,6 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-// Wait until at most two committed bulk store groups are still reading shared memory.
-__device__ __forceinline__ void bulk_wait_read2() {
-    asm volatile("cp.async.bulk.wait_group.read 2;" ::: "memory");
-}
-
 // Wait until at most one committed bulk store group is still reading shared memory.
 __device__ __forceinline__ void bulk_wait_read1() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -234,30 +229,6 @@ __device__ __forceinline__ void mma_f16_warp(uint32_t d_tmem, uint64_t a_desc, u
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-// Eight MMAs (one 128-deep product in K = 16 steps) issued by one elected
-// lane of a converged warp in a single block: D (+)= sum_k A_k B_k, with the
-// k-th descriptors a0 + a_step[k], b0 + b_step[k] (start-address offsets).
-// The first step overwrites D unless `accumulate`.
-__device__ __forceinline__ void mma_f16_warp_k8(uint32_t d_tmem, uint64_t a0, const uint64_t (&ast)[8], uint64_t b0,
-                                                const uint64_t (&bst)[8], uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
-        "elect.sync r|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %18, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %17, p;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %17, 1;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %17, 1;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %17, 1;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %17, 1;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %11, %12, %17, 1;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %13, %14, %17, 1;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %15, %16, %17, 1;\n\t}" ::"r"(d_tmem),
-        "l"(a0 + ast[0]), "l"(b0 + bst[0]), "l"(a0 + ast[1]), "l"(b0 + bst[1]), "l"(a0 + ast[2]), "l"(b0 + bst[2]),
-        "l"(a0 + ast[3]), "l"(b0 + bst[3]), "l"(a0 + ast[4]), "l"(b0 + bst[4]), "l"(a0 + ast[5]), "l"(b0 + bst[5]),
-        "l"(a0 + ast[6]), "l"(b0 + bst[6]), "l"(a0 + ast[7]), "l"(b0 + bst[7]), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\t"
