@@ -160,6 +160,22 @@ def test_l2norm_flag():
     assert (o_on.float() - o_off.float()).abs().max().item() > 1e-4
 
 
+def test_explicit_scale():
+    """A caller's scale multiplies q (operator page, section "算法原理", step
+    M1: q times scale) and matches the oracle with the same scale; the C ABI's
+    "scale <= 0 or NaN means K^-0.5" gives the default's bits."""
+    x = make_inputs(custom("sc", B=1, T=640, H=2, with_h0=True, seed=33))
+    xs = dict(x, scale=0.3)
+    o, ht = run_gpu(xs)
+    o_ref, ht_ref = run_oracle(xs)
+    assert_within(compare(o, ht, o_ref, ht_ref))
+    o_def, ht_def = run_gpu(x)
+    assert (o.float() - o_def.float()).abs().max().item() > 1e-4
+    for bad in (-1.0, 0.0, float("nan")):
+        o_b, ht_b = run_gpu(dict(x, scale=bad))
+        assert torch.equal(o_b, o_def) and torch.equal(ht_b, ht_def), bad
+
+
 # ---------------------------------------------------------------------------
 # Bitwise invariants
 # ---------------------------------------------------------------------------
