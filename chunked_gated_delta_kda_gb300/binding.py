@@ -28,6 +28,7 @@ KDA_FLAG_BWD_CHUNK_FP32 = 4
 KDA_FLAG_SAVE_FOR_BWD = 8
 KDA_FLAG_BWD_REUSE_FWD = 16
 KDA_FLAG_BWD_UMMA = 32
+KDA_FLAG_FWD_TOKEN_EXACT = 64
 
 KDA_DEBUG_WAIT_LIMIT = 1
 KDA_DEBUG_DROP_SCAN_LOAD = 2
@@ -178,8 +179,10 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
         scale: Optional[float] = None, initial_state: Optional[torch.Tensor] = None,
         output_final_state: bool = False, use_qk_l2norm_in_kernel: bool = False,
         cu_seqlens: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-        save_for_backward: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """Chunked KDA forward.  ``save_for_backward`` (training) also stores the
+        save_for_backward: bool = False, token_exact: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Chunked KDA forward.  ``token_exact`` computes every (sequence, head)
+    token by token with an fp32 state instead (``KDA_FLAG_FWD_TOKEN_EXACT``:
+    for very slowly decaying heads; slower).  ``save_for_backward`` (training) also stores the
     chunk states in ``workspace`` (which must then be a caller tensor of at
     least ``bwd_workspace_bytes`` bytes) for ``bwd(..., reuse_forward=True,
     workspace=<the same tensor>)``.  q, k: bf16 [B,T,H,K]; v: bf16 [B,T,H,V]; g: fp32
@@ -218,7 +221,8 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta
         if save_for_backward:
             raise ValueError("save_for_backward needs a workspace of at least bwd_workspace_bytes(...) bytes")
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
-    flags = (KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0) | (KDA_FLAG_SAVE_FOR_BWD if save_for_backward else 0)
+    flags = ((KDA_FLAG_QK_L2NORM if use_qk_l2norm_in_kernel else 0) | (KDA_FLAG_SAVE_FOR_BWD if save_for_backward else 0)
+             | (KDA_FLAG_FWD_TOKEN_EXACT if token_exact else 0))
     with torch.cuda.device(dev):
         kda_fwd(q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, N, flags, workspace)
     return o, ht

@@ -56,8 +56,11 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const fl
     if (!workspace) return KDA_ERR_INVALID_ARG;
     if (T > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
     if (B < 1 || T < 0 || H < 1 || N < 1 || H > 65535 || N > 65535) return KDA_ERR_INVALID_ARG;
-    if ((flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_SAVE_FOR_BWD)) != 0u) return KDA_ERR_INVALID_ARG;
+    if ((flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_SAVE_FOR_BWD | KDA_FLAG_FWD_TOKEN_EXACT)) != 0u)
+        return KDA_ERR_INVALID_ARG;
     const bool save = (flags & KDA_FLAG_SAVE_FOR_BWD) != 0u;
+    const bool token_exact = (flags & KDA_FLAG_FWD_TOKEN_EXACT) != 0u;
+    if (save && token_exact) return KDA_ERR_INVALID_ARG;
     if (cu_seqlens == nullptr) {
         if (N != B || T % kda::BT != 0) return KDA_ERR_INVALID_ARG;
     } else {
@@ -111,8 +114,17 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const fl
     }
 
     if (cudaMemsetAsync(workspace, 0, kda::WS_CLEAR, stream) != cudaSuccess) return KDA_ERR_CUDA;
-    if (cudaMemsetAsync(p.exact_flags, 0, (size_t)N * H * 4, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    // token-exact: every unit flagged (non-zero words), nothing chunked runs
+    if (cudaMemsetAsync(p.exact_flags, token_exact ? 1 : 0, (size_t)N * H * 4, stream) != cudaSuccess)
+        return KDA_ERR_CUDA;
     if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (token_exact) {
+        if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return KDA_ERR_CUDA;
+        if (kda::launch_exact(p, p.exact_flags, (flags & KDA_FLAG_QK_L2NORM) != 0u, stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return KDA_ERR_CUDA;
+        return KDA_OK;
+    }
     if (p.nslots > 0) {
         if (kda::launch_prep(p, (flags & KDA_FLAG_QK_L2NORM) != 0u, stream) != cudaSuccess) return KDA_ERR_CUDA;
     }

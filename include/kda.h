@@ -79,6 +79,15 @@ typedef enum {
  * KDA_FLAG_BWD_TOKEN_EXACT. */
 #define KDA_FLAG_BWD_REUSE_FWD 16u
 
+/* kda_fwd only: compute every (sequence, head) token by token with an fp32
+ * state (the recurrence itself, the exact kernel the chunked path already
+ * uses for units beyond its factoring range) instead of in chunked form.
+ * For heads whose gates decay so slowly that the chunked path's fp16 product
+ * operands exceed the final-state tolerance (about g/1000 per token and
+ * slower); one sequential chain per (sequence, head, 32 value rows), so it
+ * is much slower on long sequences.  Not with KDA_FLAG_SAVE_FOR_BWD. */
+#define KDA_FLAG_FWD_TOKEN_EXACT 64u
+
 /* kda_bwd only: evaluate the per-chunk chain rule with tcgen05 kind::tf32
  * products (operands staged K-major in shared memory, accumulators in TMEM)
  * instead of the default warp-level TF32 products.  Same results within the
@@ -110,7 +119,8 @@ size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int N);
  *   o           bf16 [B, T, H, V]   output (written for every valid token)
  *   ht          fp32 [N, H, V, K] final state, or NULL to skip it
  *   B, T, H, K, V, N  sizes (K == V == 128)
- *   flags       0, KDA_FLAG_QK_L2NORM, KDA_FLAG_SAVE_FOR_BWD (or both)
+ *   flags       0 or KDA_FLAG_QK_L2NORM, with KDA_FLAG_SAVE_FOR_BWD or
+ *               KDA_FLAG_FWD_TOKEN_EXACT
  *   workspace   device scratch of at least kda_fwd_workspace_bytes(...)
  *               bytes, 256-byte aligned; its contents need not be
  *               initialised.  Two calls that share a workspace must not

@@ -21,12 +21,12 @@ def to_np(t):
     return None if t is None else t.detach().float().cpu().numpy()
 
 
-def run_gpu(x, output_final_state=True, l2norm=False, device="cuda"):
+def run_gpu(x, output_final_state=True, l2norm=False, device="cuda", token_exact=False):
     from chunked_gated_delta_kda_gb300 import binding
     d = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     o, ht = binding.fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], scale=d.get("scale"),
                         initial_state=d["h0"], output_final_state=output_final_state,
-                        use_qk_l2norm_in_kernel=l2norm, cu_seqlens=d["cu_seqlens"])
+                        use_qk_l2norm_in_kernel=l2norm, cu_seqlens=d["cu_seqlens"], token_exact=token_exact)
     torch.cuda.synchronize()
     return o, ht
 

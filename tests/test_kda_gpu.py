@@ -264,6 +264,15 @@ def test_host_validation_on_device():
     with pytest.raises(binding.KdaError) as e:   # fixed length needs T % 128 == 0
         binding.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], None, None, None, o, None, 1, 0, ws)
     assert e.value.code == 1
+    o2 = torch.empty((1, 256, 1, 128), dtype=torch.bfloat16, device="cuda")
+    q2 = torch.zeros((1, 256, 1, 128), dtype=torch.bfloat16, device="cuda")
+    g2 = torch.zeros((1, 256, 1, 128), dtype=torch.float32, device="cuda")
+    b2 = torch.zeros((1, 256, 1), dtype=torch.float32, device="cuda")
+    big = torch.empty(binding.bwd_workspace_bytes(1, 256, 1, 1), dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.KdaError) as e:   # token-exact has no chunk states to save
+        binding.kda_fwd(q2, q2, q2, g2, b2, None, None, None, o2, None, 1,
+                        binding.KDA_FLAG_SAVE_FOR_BWD | binding.KDA_FLAG_FWD_TOKEN_EXACT, big)
+    assert e.value.code == 1
 
 
 def test_many_short_sequences():
@@ -311,3 +320,37 @@ def test_slow_decay_known_limit(gate_div):
     assert stats["o_tol_ratio"] <= 1.0 and stats["o_relnorm"] <= 1e-2, stats
     assert stats["S_tol_ratio"] <= 2.0, stats
     assert stats["S_tol_ratio"] <= 1.25 * {1000.0: 1.33, 4096.0: 1.45}[gate_div], stats
+
+
+@pytest.mark.parametrize("gate_div", [1000.0, 4096.0])
+def test_token_exact_slow_decay(gate_div):
+    """The same slow-decay inputs through KDA_FLAG_FWD_TOKEN_EXACT (every
+    (sequence, head) token by token with an fp32 state): output and final
+    state within the page's tolerances."""
+    w = custom("slow", B=1, T=8192, H=4, with_h0=True, seed=3, gate_div=gate_div)
+    x = make_inputs(w)
+    o, ht = run_gpu(x, token_exact=True)
+    o_ref, ht_ref = run_oracle(x)
+    stats = compare(o, ht, o_ref, ht_ref)
+    print(gate_div, stats)
+    assert_within(stats)
+
+
+@pytest.mark.parametrize("case", ["b2_t2048_h8", "varlen_mixed", "l2norm"])
+def test_token_exact_matches_oracle(case):
+    """KDA_FLAG_FWD_TOKEN_EXACT on a named workload with h0, on ragged varlen
+    packing with an empty and a one-row-tail sequence, and with the in-kernel
+    q/k normalisation."""
+    l2 = case == "l2norm"
+    if case == "b2_t2048_h8":
+        x = make_inputs(WORKLOADS["b2_t2048_h8"])
+    elif case == "varlen_mixed":
+        lens = [37, 0, 300, 129, 1]
+        x = make_inputs(custom(case, B=1, T=sum(lens), H=3, seqlens=lens, with_h0=True, seed=21))
+    else:
+        x = make_inputs(custom(case, B=1, T=640, H=2, with_h0=True, seed=31))
+        gen = torch.Generator().manual_seed(99)
+        x["q"] = (x["q"].float() * (0.5 + torch.rand(x["q"].shape[:3] + (1,), generator=gen) * 3)).bfloat16()
+    o, ht = run_gpu(x, token_exact=True, l2norm=l2)
+    o_ref, ht_ref = run_oracle(x, l2norm=l2)
+    assert_within(compare(o, ht, o_ref, ht_ref, cu=None if x["cu_seqlens"] is None else x["cu_seqlens"].numpy()))
