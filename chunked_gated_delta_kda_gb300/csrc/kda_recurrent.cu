@@ -14,9 +14,12 @@
 // (32 fp32 registers), and the two dot products per row are warp reductions.
 // A CTA of 4 warps covers 32 value rows of one (sequence, head); the grid is
 // (V / 32, H, N).  Over a sequence the token steps form one dependent chain
-// per warp, so each token's inputs are loaded REC_AHEAD tokens before its
-// step (four measured fastest: 51 ms against 82 without the lookahead and 56
-// with eight, for the exact forward of T=65536, H=32).  The state is read once and written once per call (once
+// per warp, so the exact recompute (long sequences) loads each token's
+// inputs four tokens before its step (51 ms against 82 without the lookahead
+// and 56 with eight, for the exact forward of T=65536, H=32); the decode
+// kernel, one or a few tokens per sequence and bound by the state traffic,
+// keeps the plain loop (the lookahead's registers cost it occupancy: 0.174
+// against 0.162 ms on the decode workload).  The state is read once and written once per call (once
 // per token in speculative mode), so the kernel is bound by HBM traffic on
 // the state, 2 x 64 KiB per (sequence, head).
 #include <cuda_bf16.h>
@@ -70,7 +73,7 @@ struct TokIn {
     float beta;
     uint4 v;        // 8 bf16: value rows v0 .. v0 + 7
 };
-constexpr int REC_AHEAD = 4;   // tokens in flight ahead of the one computed
+constexpr int EXACT_AHEAD = 4;   // exact recompute: tokens in flight ahead of the one computed
 
 __device__ __forceinline__ TokIn load_tok(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                                           const uint16_t* __restrict__ v, const float* __restrict__ g,
@@ -152,28 +155,37 @@ __device__ __forceinline__ void rec_token(const TokIn& in, uint16_t* __restrict_
 }
 
 // Tokens 0 .. len - 1 of one (sequence, head) starting at packed token bos:
-// a ring of REC_AHEAD loaded inputs (slot i holds token t0 + i of the
-// current group), each refilled with the token REC_AHEAD on as soon as it
-// is consumed; after(t) runs after token t's update.
-template <class After>
+// AHEAD = 0 loads each token's inputs right before its step; otherwise a
+// ring of AHEAD loaded inputs (slot i holds token t0 + i of the current
+// group), each refilled with the token AHEAD on as soon as it is consumed.
+// after(t) runs after token t's update.
+template <int AHEAD, class After>
 __device__ __forceinline__ void rec_tokens(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                                            const uint16_t* __restrict__ v, const float* __restrict__ g,
                                            const float* __restrict__ beta, uint16_t* __restrict__ o, float scale,
                                            bool l2norm, long long bos, int len, int H, int h, int v0, int lane,
                                            float (&s)[REC_ROWS][4], After after) {
-    TokIn ring[REC_AHEAD];
+    if constexpr (AHEAD == 0) {
+        for (int t = 0; t < len; ++t) {
+            const size_t tok = (size_t)(bos + t) * H + h;
+            rec_token(load_tok(q, k, v, g, beta, tok, v0, lane), o, scale, l2norm, tok, v0, lane, s);
+            after(t);
+        }
+    } else {
+        TokIn ring[AHEAD];
 #pragma unroll
-    for (int i = 0; i < REC_AHEAD; ++i)
-        if (i < len) ring[i] = load_tok(q, k, v, g, beta, (size_t)(bos + i) * H + h, v0, lane);
-    for (int t0 = 0; t0 < len; t0 += REC_AHEAD) {
+        for (int i = 0; i < AHEAD; ++i)
+            if (i < len) ring[i] = load_tok(q, k, v, g, beta, (size_t)(bos + i) * H + h, v0, lane);
+        for (int t0 = 0; t0 < len; t0 += AHEAD) {
 #pragma unroll
-        for (int i = 0; i < REC_AHEAD; ++i) {
-            const int t = t0 + i;
-            if (t < len) {
-                const TokIn cur = ring[i];
-                if (t + REC_AHEAD < len) ring[i] = load_tok(q, k, v, g, beta, (size_t)(bos + t + REC_AHEAD) * H + h, v0, lane);
-                rec_token(cur, o, scale, l2norm, (size_t)(bos + t) * H + h, v0, lane, s);
-                after(t);
+            for (int i = 0; i < AHEAD; ++i) {
+                const int t = t0 + i;
+                if (t < len) {
+                    const TokIn cur = ring[i];
+                    if (t + AHEAD < len) ring[i] = load_tok(q, k, v, g, beta, (size_t)(bos + t + AHEAD) * H + h, v0, lane);
+                    rec_token(cur, o, scale, l2norm, (size_t)(bos + t) * H + h, v0, lane, s);
+                    after(t);
+                }
             }
         }
     }
@@ -244,7 +256,7 @@ __global__ void __launch_bounds__(REC_THREADS) kda_recurrent_kernel(const RecPar
         }
     }
 
-    rec_tokens(p.q, p.k, p.v, p.g, p.beta, p.o, p.scale, p.l2norm != 0, bos, len, H, h, v0, lane, s, [&](int t) {
+    rec_tokens<0>(p.q, p.k, p.v, p.g, p.beta, p.o, p.scale, p.l2norm != 0, bos, len, H, h, v0, lane, s, [&](int t) {
         if (p.nacc != nullptr) {   // speculative mode: the state after token t goes to slot row[t]
             const int ws = row[t];
             if (ws >= 0) store_rows(p.pool + (((size_t)ws * H + h) * VD + v0) * KD, s, lane);
@@ -277,7 +289,8 @@ __global__ void __launch_bounds__(REC_THREADS) kda_exact_kernel(const FwdParams 
         if (p.h0 != nullptr) x = *reinterpret_cast<const float4*>(p.h0 + st + (size_t)r * KD + 4 * lane);
         s[r][0] = x.x; s[r][1] = x.y; s[r][2] = x.z; s[r][3] = x.w;
     }
-    rec_tokens(p.q, p.k, p.v, p.g, p.beta, p.o, p.scale, l2norm != 0, bos, len, H, h, v0, lane, s, [](int) {});
+    rec_tokens<EXACT_AHEAD>(p.q, p.k, p.v, p.g, p.beta, p.o, p.scale, l2norm != 0, bos, len, H, h, v0, lane, s,
+                            [](int) {});
     if (p.ht != nullptr) store_rows(p.ht + st, s, lane);
 }
 
