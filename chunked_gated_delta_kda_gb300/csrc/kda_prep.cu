@@ -17,8 +17,8 @@
 // Factoring.  With a pivot P (per dimension, the prefix sum at row 64),
 //   E = exp(G - P),  F = exp(P - G),
 //   Lk = k E, Lq = (scale q) E, R = k F,  so that A_raw = Lk R^T, A2_raw = Lq R^T.
-// Two variants of the kernel share everything after the gated products:
-//   * fast (fp16 gated operands): when every Lk, Lq, R, v of the chunk fits
+// Two kernels of one template share everything after the gated products:
+//   * fast (fp16 gated operands): when every Lk, Lq, R of the chunk fits
 //     comfortably in fp16, the other operands are exact column / row
 //     rescalings of these tiles and need no tiles of their own:
 //       exp(G) k = Lk diag(exp(P))      ->  w = ((I+A)^-1 diag(beta) Lk) diag(exp(P))
@@ -27,14 +27,20 @@
 //     with beta folded into the columns of the inverse.
 //   * wide (bf16 gated operands): chunks whose factors would overflow fp16
 //     (strong decay inside the chunk) are queued by the fast kernel and
-//     redone by this variant, which builds exp(G) k, kg, qg and beta v as
-//     separate fp16 tiles.  A chunk whose decay from the pivot row exceeds
-//     the factor cap is flagged: its (sequence, head) is then recomputed
-//     exactly, token by token, after the scan.
+//     redone by this one, which builds exp(G) k, kg, qg and beta v as
+//     separate fp16 tiles.  The fast kernel queues a chunk as soon as its
+//     gate prefix alone shows a move from the pivot row that fp16 factors
+//     cannot hold, before any fp16 gating, and otherwise after the exact
+//     range check of its fp16 operands.  A chunk whose decay from the pivot
+//     row exceeds the factor cap is flagged: its (sequence, head) is then
+//     recomputed exactly, token by token, after the scan.
+// Both kernels load a chunk's raw q, k, v tiles by tensor-map copies and
+// compute the gate prefix with the same thread mapping; each has its own
+// register allocation, so the wide code costs the fast kernel nothing.
 //
 // GB300 mapping.  Persistent kernels: one 512-thread CTA per SM walks the
 // work items.  The 128-wide contractions run on tcgen05 tensor cores with
-// fp16 operands (bf16 for the wide variant's gated operands) and fp32
+// fp16 operands (bf16 for the wide kernel's gated operands) and fp32
 // accumulators in TMEM.  The prefix sum, the gated operands and the 16x16
 // diagonal blocks of the inverse run on CUDA cores in fp32; the 16 -> 32 and
 // 32 -> 64 merges of the inverse on warp-level TF32 tensor-core products
@@ -57,35 +63,38 @@ constexpr float LOG2E = 1.4426950408889634f;
 // exp2 argument cap: 2^115 ~ e^80, the page's decay cap; keeps every factor
 // finite so that a zero operand never meets an infinite one.
 constexpr float EXP2_CAP = 115.0f;
-// The fast variant keeps a chunk only if every gated operand is below this
-// (fp16 max is 65504; the margin keeps products and sums finite).
+// The fast kernel keeps a chunk only if every gated operand (Lk, Lq, R) is
+// below this (fp16 max is 65504; the margin keeps products and sums finite).
+// v is not checked: it is an fp16 operand in both kernels.
 constexpr float FP16_SAFE = 16384.0f;
 
 // Shared-memory regions (bytes from the 1024-aligned base).
-//                  fast variant (layout 0 | layout 1)          wide variant
+//                  fast kernel (layout 0 | layout 1)           wide kernel
 //   0    .. 64K :  raw k | raw v -> Lk | v16 -> w | u          Lk | Lq -> qg | kg
 //   64K  .. 96K :  raw q -> Lq    | R                          R -> merge tiles -> Ainv
 //   96K  .. 128K:  R              | merge tiles -> Ainv        RHS (k part) -> w
 //   128K .. 160K:  merge tiles -> Ainv | raw q -> Lq           RHS (v part) -> u
 //   160K .. 208K:  fp32 diag blocks -> A2 (160K .. 192K)       qg stash -> fp32
 //                  -> output staging 1; prefix totals at 192K  diag blocks -> A2
-// Fast variant: chunks alternate between the two layouts, so that the next
-// chunk's raw q (in place of this chunk's inverse, or of its R) and raw k, v
-// (in place of w | u) can be loaded while this chunk's output tiles are
-// staged in 96K .. 128K and 160K .. 192K.
+// Chunks alternate between the two fast layouts, so that the next chunk's
+// raw q (in place of this chunk's inverse, or of its R) and raw k, v (in
+// place of w | u) can be loaded while this chunk's output tiles are staged
+// in 96K .. 128K and 160K .. 192K.  The wide kernel's raw tiles sit where
+// the same alternation puts them (k at 0, v at 32K, q at 64K or 128K); its
+// gating reads each 16-byte piece before it writes the same piece of any
+// region, so the wide operands can be written over them.
 constexpr uint32_t RM = 213248;            // misc
 constexpr uint32_t M_G64 = RM;             // f32[128]  G at the pivot row (log2 units)
 constexpr uint32_t M_GL = RM + 512;        // f32[128]  G at the last row (log2 units)
 constexpr uint32_t M_BETA = RM + 1024;     // f32[128]
 constexpr uint32_t M_INVQ = RM + 1536;     // f32[128]  scale / ||q|| (or scale)
 constexpr uint32_t M_INVK = RM + 2048;     // f32[128]  1 / ||k|| (or 1)
-constexpr uint32_t M_EP = RM + 2560;       // f32[128]  exp(P)          (fast)
-constexpr uint32_t M_CL = RM + 3072;       // f32[128]  exp(G_last - P) (fast)
-constexpr uint32_t M_TOT = RM + 3584;      // f32[8][128] row-block sums (wide)
+constexpr uint32_t M_EP = RM + 2560;       // f32[128]  exp(P)
+constexpr uint32_t M_CL = RM + 3072;       // f32[128]  exp(G_last - P), capped
 constexpr uint32_t M_BAR = RM + 7680;      // mbarrier
 constexpr uint32_t M_BAR2 = RM + 7688;     // mbarrier of the second transition product
 constexpr uint32_t M_BARD = RM + 7696;     // mbarrier: every issued product done (before TMEM is freed)
-constexpr uint32_t M_RAWB = RM + 7704;     // mbarrier: a chunk's raw q / k / v tiles landed (fast variant)
+constexpr uint32_t M_RAWB = RM + 7704;     // mbarrier: a chunk's raw q / k / v tiles landed
 constexpr uint32_t M_TMEM = RM + 7744;     // TMEM base address
 constexpr uint32_t M_FLAG = RM + 7748;     // failure flag
 constexpr uint32_t SMEM_USED = RM + 7808;
@@ -98,37 +107,38 @@ constexpr int DS = 68;
 constexpr uint32_t W_DIAG = RW;                          // 2 x 64 x 68 floats = 34816 B
 constexpr uint32_t W_TMP = RW + 2 * 64 * DS * 4;         // merge temps, up to 10 KB
 static_assert(W_TMP + 2 * 1280 * 4 <= RM, "merge temps overlap the misc block");
-// fast variant: the gate prefix-scan totals ([32 row groups][129] fp32), clear
+// the gate prefix-scan totals ([32 row groups][129] fp32), clear
 // of the output staging buffers that may still be draining when they are written
 constexpr uint32_t W_TOT = 196608;
 static_assert(W_TOT + 32 * 129 * 4 <= RM, "prefix totals overlap the misc block");
-// fast variant: the two 32 KB staging buffers of the output tiles
+// fast kernel: the two 32 KB staging buffers of the output tiles
 constexpr uint32_t ST0 = 98304;
 constexpr uint32_t ST1 = RW;
 static_assert(PREP_SMEM <= 232448, "shared memory above the 227 KB limit");
 
-// Fixed region map of the wide variant (the fast variant uses LK, B2 and WU
-// from it and takes Lq, R and the inverse's region from its chunk's layout).
-template <bool FAST>
-struct Map {
-    static constexpr uint32_t LK = 0;
-    static constexpr uint32_t LQ = FAST ? 65536 : 32768;
-    static constexpr uint32_t RR = FAST ? 98304 : 65536;      // R
-    static constexpr uint32_t Y = FAST ? 131072 : 65536;      // merge tiles, then Ainv
-    static constexpr uint32_t B2 = FAST ? 0 : 98304;          // B operand of the WY product (N = 256)
-    static constexpr uint32_t WU = FAST ? 0 : 98304;          // w | u (N = 256)
-    static constexpr uint32_t KGT = FAST ? 98304 : 32768;     // A operand (MN-major) of the Nm | Bc product
-    static constexpr uint32_t QS = FAST ? 65536 : 0;          // Lq (fast) or qg (wide) for the Qe epilogue
-    // level-3 merge tiles inside the Ainv region (A10, P, Q), T in the merge
-    // temps (free by then), so that Ainv's P and Q parts can be written
-    // while the last merge product runs
-    static constexpr uint32_t YA = Y, YP = Y + 8192, YQ = Y + 16384;
-    // staging of the output tile for the bulk store (regions free by then)
-    static constexpr uint32_t ST_NM = FAST ? 0 : 65536;
-    static constexpr uint32_t ST_BC = 32768;
-    static constexpr uint32_t ST_QE = FAST ? 131072 : 98304;
-    static constexpr uint32_t ST_OI = FAST ? 98304 : 131072;
-};
+// Fixed region map of the wide kernel (the fast kernel takes Lq, R and the
+// inverse's region from its chunk's layout, and has Lk, the WY product's
+// right-hand side and w | u at 0).
+namespace wide_map {
+constexpr uint32_t LQ = 32768;
+constexpr uint32_t RR = 65536;     // R
+constexpr uint32_t Y = 65536;      // merge tiles, then Ainv (over R)
+constexpr uint32_t B2 = 98304;     // B operand of the WY product (N = 256): [beta exp(G) k | beta v]
+constexpr uint32_t WU = 98304;     // w | u (N = 256), over B2
+constexpr uint32_t KGT = 32768;    // kg: A operand (MN-major) of the Nm | Bc product, over Lq
+constexpr uint32_t QS = 0;         // qg for the Qe epilogue, over Lk
+// staging of the output tiles for the bulk stores (regions free by then)
+constexpr uint32_t ST_NM = 65536;
+constexpr uint32_t ST_BC = 32768;
+constexpr uint32_t ST_QE = 98304;
+constexpr uint32_t ST_OI = 131072;
+}  // namespace wide_map
+// The fast kernel's gate-only check: a chunk whose gate prefix moves more
+// than this (log2 units) between the pivot row and the chunk's first or last
+// row in some dimension needs a factor above 2^18, which the fp16 range
+// check passes only for |k| or |q| below 2^-4 there; such chunks are queued
+// for the wide kernel without fp16 gating.
+constexpr float WIDE_SPAN = 18.0f;
 
 // max that propagates NaN (an operand 0 * inf must not pass the range check)
 __device__ __forceinline__ float fmax_nan(float a, float b) {
@@ -335,8 +345,9 @@ __device__ __forceinline__ void prefetch_chunk(const FwdParams& p, const ChunkRe
     }
 }
 
-// Work iteration.  Fast: every (slot, head) item, grid-stride, skipping
-// empty slots.  Wide: the entries of the queue the fast kernel filled.
+// Work iteration.  Fast kernel: every (slot, head) item, grid-stride,
+// skipping empty slots.  Wide kernel: the entries of the queue the fast
+// kernel filled.
 template <bool FAST>
 __device__ __forceinline__ bool fetch_item(const FwdParams& p, long long& idx, long long& item, ChunkRef& c,
                                            int& h) {
@@ -367,13 +378,68 @@ __device__ __forceinline__ bool fetch_item(const FwdParams& p, long long& idx, l
     }
 }
 
+// Wide-kernel gating of one thread's 4 rows x 8 dimensions (G: the gate
+// prefix minus the pivot, log2 units).  Lk, Lq, R bf16
+// (capped factors) over the raw tiles; RHS = [beta exp(G) k | beta v] fp16
+// and qg fp16 in their own regions; kg fp16 parked in tensor memory columns
+// 256 .. 319 (free until the WY product), 16 per warp of a lane quarter,
+// until the region of Lq is free.  exp(G) = E exp(P) <= 1.
+template <bool L2NORM>
+__device__ __forceinline__ void wide_gating(uint8_t* sm, const float (&G)[4][8], int tg0, int d8, int len,
+                                            uint32_t oRawQ, uint32_t kg_col) {
+    const float* sBeta = reinterpret_cast<const float*>(sm + M_BETA);
+    const float* sInvQ = reinterpret_cast<const float*>(sm + M_INVQ);
+    const float* sInvK = reinterpret_cast<const float*>(sm + M_INVK);
+    const float* sEP = reinterpret_cast<const float*>(sm + M_EP);
+    const float* sCL = reinterpret_cast<const float*>(sm + M_CL);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int t = tg0 + r;
+        const uint32_t off = sw128_off(t, d8, 128);
+        uint4 kc = *reinterpret_cast<const uint4*>(sm + off);
+        uint4 vc = *reinterpret_cast<const uint4*>(sm + 32768 + off);
+        uint4 qc = *reinterpret_cast<const uint4*>(sm + oRawQ + off);
+        if (len < BT && t >= len) kc = vc = qc = make_uint4(0u, 0u, 0u, 0u);   // tail chunks only
+        float kf[8], qf[8], vf[8];
+        unpack8_bf16(kc, kf);
+        unpack8_bf16(qc, qf);
+        unpack8_bf16(vc, vf);
+        const float ik = L2NORM ? sInvK[t] : 1.f, iq = sInvQ[t], b = sBeta[t];
+        uint32_t lk[4], lqv[4], rk[4], bk[4], bv[4], qg[4], kg[4];
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+            const float g0 = G[r][j], g1 = G[r][j + 1];
+            const float E0 = ex2(fminf(g0, EXP2_CAP)), E1 = ex2(fminf(g1, EXP2_CAP));
+            const float F0 = ex2(fminf(-g0, EXP2_CAP)), F1 = ex2(fminf(-g1, EXP2_CAP));
+            const float k0 = kf[j] * ik, k1 = kf[j + 1] * ik;
+            const float q0 = qf[j] * iq, q1 = qf[j + 1] * iq;
+            const float eg0 = E0 * sEP[d8 + j], eg1 = E1 * sEP[d8 + j + 1];
+            lk[j / 2] = pack_bf16(k0 * E0, k1 * E1);
+            lqv[j / 2] = pack_bf16(q0 * E0, q1 * E1);
+            rk[j / 2] = pack_bf16(k0 * F0, k1 * F1);
+            bk[j / 2] = pack_f16(b * k0 * eg0, b * k1 * eg1);
+            bv[j / 2] = pack_f16(b * vf[j], b * vf[j + 1]);
+            qg[j / 2] = pack_f16(q0 * eg0, q1 * eg1);
+            kg[j / 2] = pack_f16(k0 * F0 * sCL[d8 + j], k1 * F1 * sCL[d8 + j + 1]);
+        }
+        // every raw piece of this row was read above: its own pieces of the
+        // regions below may now be overwritten
+        sts_v4(sm, off, lk[0], lk[1], lk[2], lk[3]);
+        sts_v4(sm, wide_map::LQ + off, lqv[0], lqv[1], lqv[2], lqv[3]);
+        sts_v4(sm, wide_map::RR + off, rk[0], rk[1], rk[2], rk[3]);
+        sts_v4(sm, wide_map::B2 + off, bk[0], bk[1], bk[2], bk[3]);
+        sts_v4(sm, wide_map::B2 + 32768u + off, bv[0], bv[1], bv[2], bv[3]);
+        sts_v4(sm, RW + off, qg[0], qg[1], qg[2], qg[3]);
+        tmem_st4(kg_col + (uint32_t)(4 * r), kg[0], kg[1], kg[2], kg[3]);
+    }
+}
+
 }  // namespace
 
 template <bool L2NORM, bool FAST>
 __global__ void __launch_bounds__(PREP_THREADS, 1)
     kda_prep_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v) {
-    using MP = Map<FAST>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -385,10 +451,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
     const int cg = warp >> 2;             // column group (0..3) for TMEM read-backs
     const uint32_t lane_off = (uint32_t)(lq * 32) << 16;
     const int trow = lq * 32 + lane;      // TMEM lane = matrix row of this thread
-    // fast: thread 0 issues (and waits for) every bulk tile store and tensor
-    // load; wide: one thread in each 128-thread group issues one of the four
-    // bulk tile stores
-    const bool bulk_thread = FAST ? tid == 0 : (tid & 127) == 0;
+    // thread 0 issues (and waits for) every bulk tile store and tensor load
+    const bool bulk_thread = tid == 0;
 
     float* sG64 = reinterpret_cast<float*>(sm + M_G64);
     float* sGL = reinterpret_cast<float*>(sm + M_GL);
@@ -429,10 +493,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + M_TMEM);
 
-    // Fast variant: a chunk's raw k, v and q tiles arrive by tensor-map loads
-    // (128-byte swizzled, the layout of the MMA operands) straight into the
-    // regions where the gated operands are then computed in place: k -> Lk,
-    // v -> the fp16 copy of v, q -> Lq.  Consecutive chunks of a CTA alternate
+    // A chunk's raw k, v and q tiles arrive by tensor-map loads (128-byte
+    // swizzled, the layout of the MMA operands) straight into the regions
+    // where the gated operands are then computed in place (fast kernel: k -> Lk,
+    // v -> the fp16 copy of v, q -> Lq).  Consecutive chunks of a CTA alternate
     // between two region layouts so that the next chunk's loads can be issued
     // while this chunk's output tiles are still being staged (layout 0 / 1:
     // Lq at 64K / 128K, R at 96K / 64K, the inverse at 128K / 96K).
@@ -450,10 +514,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
         }
     };
     int lay = 0;
-    if (FAST) {
-        if (tid == 0) issue_raw(c, h, 0);
-        raw_pending = true;
-    }
+    if (tid == 0) issue_raw(c, h, 0);
+    raw_pending = true;
 
     // Bounded waits: once one has run out (flag set), later ones of this CTA
     // return at once, the item finishes on whatever the tensor memory holds
@@ -469,10 +531,19 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
         phase ^= 1;
         tc_fence_after();
     };
+    // a chunk's raw tiles have landed; after a wait that ran out the load
+    // stays pending and is drained before the CTA exits
+    auto wait_raw = [&]() {
+        bounded_wait(rawbar, rphase);
+        if (*sFlag == 0) {
+            rphase ^= 1;
+            raw_pending = false;
+        }
+    };
 
 
-    // fast variant: a chunk's beta and gate rows are loaded into registers
-    // during the previous chunk's epilogue
+    // a chunk's beta and gate rows are loaded into registers during the
+    // previous chunk's epilogue
     const uint64_t efp = evict_first_policy();
     float4 gpre[4][2];
     float bpre = 0.f;
@@ -497,7 +568,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
     };
     ChunkRef none{};   // zero rows: loads nothing, defines the registers
     none.len = 0;
-    if (FAST) load_rows(c, h);
+    load_rows(c, h);
 
     while (have && *sFlag == 0) {
         long long nidx = idx + gridDim.x, nitem = 0;
@@ -506,18 +577,18 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
         const bool have_n = fetch_item<FAST>(p, nidx, nitem, cn, hn);
         const int len = c.len;
         const size_t row0 = (size_t)c.tok0 * H + h;
-        // region offsets of this chunk: the fast variant's alternating layout,
-        // or the wide variant's fixed map
-        const uint32_t oLQ = FAST ? (lay ? 131072u : 65536u) : MP::LQ;
-        const uint32_t oRR = FAST ? (lay ? 65536u : 98304u) : MP::RR;
-        const uint32_t oY = FAST ? (lay ? 98304u : 131072u) : MP::Y;
+        // region offsets of this chunk's alternating layout (the raw q tile
+        // lands at oRawQ in both kernels; the wide kernel's other regions are
+        // fixed)
+        const uint32_t oRawQ = lay ? 131072u : 65536u;   // fast kernel: Lq
+        const uint32_t oRf = lay ? 65536u : 98304u;       // fast kernel: R
 
         // ------------------------------------------------------------------
         // Per-row scalars: beta, and the q / k scalings (scale, optional
         // L2 normalisation x / sqrt(sum x^2 + 1e-6)).
         // ------------------------------------------------------------------
         if (tid < BT) {
-            sBeta[tid] = FAST ? bpre : (tid < len ? __ldg(p.beta + row0 + (size_t)tid * H) : 0.f);
+            sBeta[tid] = bpre;
             if (!L2NORM) {
                 sInvQ[tid] = p.scale;
                 sInvK[tid] = 1.f;
@@ -550,101 +621,112 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
 
         // ------------------------------------------------------------------
         // Phase 1: gate prefix sum (log2 units), pivot row 64, gated operands.
+        // thread = 8 consecutive dimensions x 4 consecutive rows
         // ------------------------------------------------------------------
-        bool unsafe = false;
-        uint32_t kgr[16];   // wide variant: kg held until region 0 is free
-        (void)kgr;
-        if constexpr (FAST) {
-            // thread = 8 consecutive dimensions x 4 consecutive rows
-            const int d8 = (tid & 15) * 8;
-            const int grp = tid >> 4;
-            const int tg0 = grp * 4;
-            float G[4][8];
+        const int d8 = (tid & 15) * 8;
+        const int grp = tid >> 4;
+        const int tg0 = grp * 4;
+        float G[4][8];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const float4 ga = gpre[r][0], gb = gpre[r][1];
-                G[r][0] = ga.x; G[r][1] = ga.y; G[r][2] = ga.z; G[r][3] = ga.w;
-                G[r][4] = gb.x; G[r][5] = gb.y; G[r][6] = gb.z; G[r][7] = gb.w;
-            }
-            // [32 groups][129]: the odd row stride keeps the column-wise
-            // prefix scan free of shared-memory bank conflicts
-            constexpr int TS = 129;
-            float* tot = reinterpret_cast<float*>(sm + W_TOT);
-            {
-                float acc[8];
+        for (int r = 0; r < 4; ++r) {
+            const float4 ga = gpre[r][0], gb = gpre[r][1];
+            G[r][0] = ga.x; G[r][1] = ga.y; G[r][2] = ga.z; G[r][3] = ga.w;
+            G[r][4] = gb.x; G[r][5] = gb.y; G[r][6] = gb.z; G[r][7] = gb.w;
+        }
+        float span = 0.f;   // fast kernel: the gate's move from the pivot row
+        // [32 groups][129]: the odd row stride keeps the column-wise
+        // prefix scan free of shared-memory bank conflicts
+        constexpr int TS = 129;
+        float* tot = reinterpret_cast<float*>(sm + W_TOT);
+        {
+            float acc[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+            for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        acc[j] = fmaf(G[r][j], LOG2E, acc[j]);
-                        G[r][j] = acc[j];
-                    }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) tot[grp * TS + d8 + j] = acc[j];
-            }
-            __syncthreads();
-            {   // exclusive prefix over the 32 row groups, four threads per
-                // dimension: thread (d = tid / 4, quarter qq = tid % 4) scans
-                // groups 8 qq .. 8 qq + 7 in order, then adds the totals of
-                // the lower quarters (two shuffle steps among its 4 lanes)
-                const int d = tid >> 2, qq = tid & 3;
-                float v[8], run = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = tot[(8 * qq + i) * TS + d];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float x = v[i];
-                    v[i] = run;
-                    run += x;
-                }
-                float incl = run;
-#pragma unroll
-                for (int s2 = 1; s2 < 4; s2 <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, incl, s2, 4);
-                    if (qq >= s2) incl += y;
-                }
-                const float base = incl - run;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) tot[(8 * qq + i) * TS + d] = base + v[i];
-            }
-            __syncthreads();
-            {
+            for (int r = 0; r < 4; ++r)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const float o = tot[grp * TS + d8 + j];
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) G[r][j] += o;
+                    acc[j] = fmaf(G[r][j], LOG2E, acc[j]);
+                    G[r][j] = acc[j];
                 }
-                if (grp == 16) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) sG64[d8 + j] = G[0][j];
-                }
-                if (grp == 31) {
+            for (int j = 0; j < 8; ++j) tot[grp * TS + d8 + j] = acc[j];
+        }
+        __syncthreads();
+        {   // exclusive prefix over the 32 row groups, four threads per
+            // dimension: thread (d = tid / 4, quarter qq = tid % 4) scans
+            // groups 8 qq .. 8 qq + 7 in order, then adds the totals of
+            // the lower quarters (two shuffle steps among its 4 lanes)
+            const int d = tid >> 2, qq = tid & 3;
+            float v[8], run = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) sGL[d8 + j] = G[3][j];
-                }
+            for (int i = 0; i < 8; ++i) v[i] = tot[(8 * qq + i) * TS + d];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float x = v[i];
+                v[i] = run;
+                run += x;
             }
-            if (bulk_thread) bulk_wait_read0();   // previous tile's bulk stores have read their staging
+            float incl = run;
+#pragma unroll
+            for (int s2 = 1; s2 < 4; s2 <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, s2, 4);
+                if (qq >= s2) incl += y;
+            }
+            const float base = incl - run;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) tot[(8 * qq + i) * TS + d] = base + v[i];
+            if (FAST) {   // the gate prefix at rows 63 and 127 (quarter totals)
+                const float g63 = __shfl_sync(0xffffffffu, incl, 1, 4);
+                const float g127 = __shfl_sync(0xffffffffu, incl, 3, 4);
+                span = fmax_nan(fabsf(g63), fabsf(g127 - g63));
+            }
+        }
+        // Fast kernel: the gate-only check, on this barrier.  A chunk whose
+        // gate prefix moves plainly beyond what fp16 factors hold between
+        // the pivot row (taken as row 63 here) and the chunk's first or last
+        // row is queued for the wide kernel without fp16 gating.
+        bool handoff_gate = false;
+        if constexpr (FAST)
+            handoff_gate = __syncthreads_or(!(span <= WIDE_SPAN)) != 0;
+        else
             __syncthreads();
-            if (tid < 128) {
-                const float P = sG64[tid];
-                sEP[tid] = ex2(P);
-                sCL[tid] = ex2(fminf(sGL[tid] - P, EXP2_CAP));
-            }
-            // only G - P is needed from here on: fold the pivot in once
+        {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const float P = sG64[d8 + j];
+                const float o = tot[grp * TS + d8 + j];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) G[r][j] -= P;
+                for (int r = 0; r < 4; ++r) G[r][j] += o;
             }
-            // this chunk's raw k, v, q tiles have landed (rows past the
-            // sequence's end hold other tokens or zeros: read as zero)
-            bounded_wait(rawbar, rphase);
-            rphase ^= 1;
-            raw_pending = false;
+            if (grp == 16) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) sG64[d8 + j] = G[0][j];
+            }
+            if (grp == 31) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) sGL[d8 + j] = G[3][j];
+            }
+        }
+        if (bulk_thread) bulk_wait_read0();   // previous tile's bulk stores have read their staging
+        __syncthreads();
+        if (tid < 128) {
+            const float P = sG64[tid];
+            sEP[tid] = ex2(P);
+            sCL[tid] = ex2(fminf(sGL[tid] - P, EXP2_CAP));
+        }
+        // only G - P is needed from here on: fold the pivot in once
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float P = sG64[d8 + j];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) G[r][j] -= P;
+        }
+        bool handoff = handoff_gate;   // fast kernel: the chunk goes to the wide kernel's queue
+        if constexpr (!FAST) __syncthreads();   // sEP / sCL are written
+        // this chunk's raw k, v, q tiles have landed (rows past the
+        // sequence's end hold other tokens or zeros: read as zero)
+        wait_raw();
+        if (FAST && !handoff) {
             float m = 0.f;
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
@@ -652,7 +734,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                 const uint32_t off = sw128_off(t, d8, 128);
                 uint4 kc = *reinterpret_cast<const uint4*>(sm + off);
                 uint4 vc = *reinterpret_cast<const uint4*>(sm + 32768 + off);
-                uint4 qc = *reinterpret_cast<const uint4*>(sm + oLQ + off);
+                uint4 qc = *reinterpret_cast<const uint4*>(sm + oRawQ + off);
                 if (len < BT && t >= len) kc = vc = qc = make_uint4(0u, 0u, 0u, 0u);   // tail chunks only
                 float kf[8], qf[8], vf[8];
                 unpack8_bf16(kc, kf);
@@ -663,14 +745,14 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < 8; j += 2) {
                     // uncapped: a factor that overflows makes an operand
-                    // infinite, which the range check sends to the wide variant
+                    // infinite, which the range check sends to the wide kernel
                     const float E0 = ex2(G[r][j]), E1 = ex2(G[r][j + 1]);
                     const float F0 = ex2(-G[r][j]), F1 = ex2(-G[r][j + 1]);
                     const float k0 = kf[j] * ik, k1 = kf[j + 1] * ik;
                     const float q0 = qf[j] * iq, q1 = qf[j + 1] * iq;
                     const float a0 = k0 * E0, a1 = k1 * E1, b0 = q0 * E0, b1 = q1 * E1, c0 = k0 * F0, c1 = k1 * F1;
                     m = fmax_nan(m, fmax_nan(fmax_nan(fabsf(a0), fabsf(a1)), fmax_nan(fabsf(b0), fabsf(b1))));
-                    m = fmax_nan(m, fmax_nan(fmax_nan(fabsf(c0), fabsf(c1)), fmax_nan(fabsf(vf[j]), fabsf(vf[j + 1]))));
+                    m = fmax_nan(m, fmax_nan(fabsf(c0), fabsf(c1)));
                     lk[j / 2] = pack_f16(a0, a1);
                     lqv[j / 2] = pack_f16(b0, b1);
                     rk[j / 2] = pack_f16(c0, c1);
@@ -680,133 +762,50 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                 // bytes it read), R into its own region
                 sts_v4(sm, off, lk[0], lk[1], lk[2], lk[3]);
                 sts_v4(sm, 32768 + off, v16[0], v16[1], v16[2], v16[3]);
-                sts_v4(sm, oLQ + off, lqv[0], lqv[1], lqv[2], lqv[3]);
-                sts_v4(sm, oRR + off, rk[0], rk[1], rk[2], rk[3]);
+                sts_v4(sm, oRawQ + off, lqv[0], lqv[1], lqv[2], lqv[3]);
+                sts_v4(sm, oRf + off, rk[0], rk[1], rk[2], rk[3]);
             }
-            unsafe = !(m <= FP16_SAFE);
-        } else {
-            // thread = dimension pair x 16 consecutive rows
-            const int d0 = (tid & 63) * 2;
-            const int rb = tid >> 6;
-            const int t0 = rb * 16;
-            float* sTot = reinterpret_cast<float*>(sm + M_TOT);
-            float G0[16], G1[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const int t = t0 + r;
-                float2 gv = make_float2(0.f, 0.f);
-                if (t < len) gv = ldg_f2(p.g + (row0 + (size_t)t * H) * KD + d0);
-                G0[r] = gv.x;
-                G1[r] = gv.y;
-            }
-            {
-                float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    a0 += G0[r] * LOG2E;
-                    a1 += G1[r] * LOG2E;
-                    G0[r] = a0;
-                    G1[r] = a1;
-                }
-                sTot[rb * 128 + d0] = a0;
-                sTot[rb * 128 + d0 + 1] = a1;
-            }
-            __syncthreads();
-            {
-                float o0 = 0.f, o1 = 0.f;
-                for (int b2 = 0; b2 < rb; ++b2) {
-                    o0 += sTot[b2 * 128 + d0];
-                    o1 += sTot[b2 * 128 + d0 + 1];
-                }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    G0[r] += o0;
-                    G1[r] += o1;
-                }
-                if (rb == 4) {
-                    sG64[d0] = G0[0];
-                    sG64[d0 + 1] = G1[0];
-                }
-                if (rb == 7) {
-                    sGL[d0] = G0[15];
-                    sGL[d0 + 1] = G1[15];
-                }
-            }
-            if (bulk_thread) bulk_wait_read0();   // previous tile's bulk stores have read their staging
-            __syncthreads();
-            const float P0 = sG64[d0], P1 = sG64[d0 + 1];
-            {   // beyond |G - P| = EXP2_CAP the capped factors no longer
-                // multiply back to exp(G_c - G_i): this (sequence, head) is
-                // recomputed token by token after the scan
-                bool far = false;
-#pragma unroll
-                for (int r = 0; r < 16; ++r)
-                    far = far || fabsf(G0[r] - P0) > EXP2_CAP || fabsf(G1[r] - P1) > EXP2_CAP;
-                if (__any_sync(0xffffffffu, far) && lane == 0) p.exact_flags[(size_t)c.n * H + h] = 1u;
-            }
-            const float eP0 = ex2(P0), eP1 = ex2(P1);
-            const float cL0 = ex2(fminf(sGL[d0] - P0, EXP2_CAP)), cL1 = ex2(fminf(sGL[d0 + 1] - P1, EXP2_CAP));
-            // Lk, Lq, R bf16; RHS = [beta exp(G) k | beta v] fp16; qg fp16
-            // stashed in region W; kg fp16 in registers.
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                asm volatile("" ::: "memory");
-                uint32_t kr[8], qr[8], vr[8];
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int t = t0 + half * 8 + r;
-                    kr[r] = qr[r] = vr[r] = 0u;
-                    if (t < len) {
-                        const size_t off = (row0 + (size_t)t * H) * KD + d0;
-                        kr[r] = ldg_u32(p.k + off);
-                        qr[r] = ldg_u32(p.q + off);
-                        vr[r] = ldg_u32(p.v + off);
-                    }
-                }
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int rr = half * 8 + r;
-                    const int t = t0 + rr;
-                    float2 kf = unpack_bf16(kr[r]), qf = unpack_bf16(qr[r]), vf = unpack_bf16(vr[r]);
-                    const float ik = sInvK[t], iq = sInvQ[t], b = sBeta[t];
-                    kf.x *= ik; kf.y *= ik;
-                    qf.x *= iq; qf.y *= iq;
-                    const float E0 = ex2(fminf(G0[rr] - P0, EXP2_CAP)), E1 = ex2(fminf(G1[rr] - P1, EXP2_CAP));
-                    const float F0 = ex2(fminf(P0 - G0[rr], EXP2_CAP)), F1 = ex2(fminf(P1 - G1[rr], EXP2_CAP));
-                    const uint32_t off = sw128_off(t, d0, 128);
-                    sts_u32(sm, MP::LK + off, pack_bf16(kf.x * E0, kf.y * E1));
-                    sts_u32(sm, MP::LQ + off, pack_bf16(qf.x * E0, qf.y * E1));
-                    sts_u32(sm, MP::RR + off, pack_bf16(kf.x * F0, kf.y * F1));
-                    const float eg0 = E0 * eP0, eg1 = E1 * eP1;                      // exp(G_t) <= 1
-                    sts_u32(sm, MP::B2 + off, pack_f16(b * kf.x * eg0, b * kf.y * eg1));
-                    sts_u32(sm, MP::B2 + sw128_off(t, 128 + d0, 128), pack_f16(b * vf.x, b * vf.y));
-                    sts_u32(sm, RW + off, pack_f16(qf.x * eg0, qf.y * eg1));        // qg stash
-                    kgr[rr] = pack_f16(kf.x * F0 * cL0, kf.y * F1 * cL1);
-                }
-            }
+            // the range check; the same barrier hands the operands to the
+            // tensor core
+            fence_async_smem();
+            tc_fence_before();
+            handoff = __syncthreads_or(!(m <= FP16_SAFE)) != 0;
+            tc_fence_after();
         }
-        // The fast variant hands chunks it cannot hold in fp16 to the wide
-        // one.  The same barrier hands the operands to the tensor core.
-        fence_async_smem();
-        tc_fence_before();
-        const bool to_wide = __syncthreads_or(FAST && unsafe) != 0;
-        tc_fence_after();
-        if (to_wide) {
+        if constexpr (!FAST) {
+            // beyond |G - P| = EXP2_CAP the capped factors no longer multiply
+            // back to exp(G_c - G_i): this (sequence, head) is recomputed
+            // token by token after the scan
+            bool far = false;
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) far = far || fabsf(G[r][j]) > EXP2_CAP;
+            if (__any_sync(0xffffffffu, far) && lane == 0) p.exact_flags[(size_t)c.n * H + h] = 1u;
+            wide_gating<L2NORM>(sm, G, tg0, d8, len, oRawQ, tmem + lane_off + 256u + (uint32_t)(cg * 16));
+            tmem_st_wait();
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+        }
+        if (handoff) {
             if (tid == 0) {
                 const uint32_t slot_i = atomicAdd(p.wide_count, 1u);
                 p.wide_list[slot_i] = (int32_t)item;
                 // the next chunk's raw tiles go to regions this chunk no
-                // longer needs (its operands are dropped)
-                if (FAST && have_n) issue_raw(cn, hn, lay ^ 1);
+                // longer needs (its operands, if any, are dropped)
+                if (have_n) issue_raw(cn, hn, lay ^ 1);
             }
-            if (FAST && have_n) raw_pending = true;
+            if (have_n) raw_pending = true;
             if (have_n) prefetch_chunk(p, cn, hn, tid);
-            if (FAST) load_rows(have_n ? cn : none, hn);
+            load_rows(have_n ? cn : none, hn);
             __syncthreads();
         } else {
             if (tid == 0) {
                 const uint32_t id = idesc_f16(FAST ? T_F16 : T_BF16, 128, 128, false, false);
-                const Operand Lk{sbase + MP::LK, false, 128}, Lq{sbase + oLQ, false, 128}, R{sbase + oRR, false, 128};
+                const Operand Lk{sbase, false, 128}, Lq{sbase + (FAST ? oRawQ : wide_map::LQ), false, 128},
+                    R{sbase + (FAST ? oRf : wide_map::RR), false, 128};
                 mma_128(tmem + 0, Lk, R, id, 8);     // A_raw  -> cols [0,128)
                 mma_128(tmem + 128, Lq, R, id, 8);   // A2_raw -> cols [128,256)
                 mma_commit(bar);
@@ -815,20 +814,28 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
             if (have_n) prefetch_chunk(p, cn, hn, tid);
             wait_mma();
 
+            // the inverse's region (merge tiles, then Ainv)
+            const uint32_t oY = FAST ? (lay ? 98304u : 131072u) : wide_map::Y;
             // --------------------------------------------------------------
             // Phase 2: A (strictly lower, times beta_row) from TMEM: diagonal
-            // 64-blocks to fp32 (W), A10 to fp16 (YA).  The wide variant
-            // first moves kg and qg into region 0.
+            // 64-blocks to fp32 (W), A10 to fp16 (YA).  The wide kernel first
+            // moves kg and qg into regions 0 .. 64K (Lk and Lq are free).
             // --------------------------------------------------------------
             if constexpr (!FAST) {
-                const int d0 = (tid & 63) * 2;
-                const int t0 = (tid >> 6) * 16;
+                {
+                    float kf[16];
+                    tmem_ld16(tmem + lane_off + 256u + (uint32_t)(cg * 16), kf);
+                    tmem_ld_wait();
+                    const uint32_t* kg = reinterpret_cast<const uint32_t*>(kf);
 #pragma unroll
-                for (int r = 0; r < 16; ++r) sts_u32(sm, 32768 + sw128_off(t0 + r, d0, 128), kgr[r]);
+                    for (int r = 0; r < 4; ++r)
+                        sts_v4(sm, wide_map::KGT + sw128_off((tid >> 4) * 4 + r, (tid & 15) * 8, 128), kg[4 * r], kg[4 * r + 1], kg[4 * r + 2],
+                               kg[4 * r + 3]);
+                }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint32_t off = (uint32_t)(tid + i * PREP_THREADS) * 16u;
-                    *reinterpret_cast<uint4*>(sm + off) = *reinterpret_cast<const uint4*>(sm + RW + off);
+                    *reinterpret_cast<uint4*>(sm + wide_map::QS + off) = *reinterpret_cast<const uint4*>(sm + RW + off);
                 }
                 __syncthreads();
             }
@@ -1017,7 +1024,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
             //   wide: Ainv [beta exp(G) k | beta v]
             // --------------------------------------------------------------
             if (tid == 0) {
-                const Operand Ai{sbase + oY, false, 128}, Rh{sbase + MP::B2, true, 128};
+                const Operand Ai{sbase + oY, false, 128}, Rh{sbase + (FAST ? 0u : wide_map::B2), true, 128};
                 mma_128(tmem + 256, Ai, Rh, idesc_f16(T_F16, 128, 256, false, true), 8);
                 mma_commit(bar);
             }
@@ -1050,7 +1057,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                 }
 #pragma unroll
                 for (int j = 0; j < 32; j += 8)
-                    sts_v4(sm, MP::WU + sw128_off(trow, col0 + j, 128), pack_f16(x[j], x[j + 1]),
+                    sts_v4(sm, (FAST ? 0u : wide_map::WU) + sw128_off(trow, col0 + j, 128), pack_f16(x[j], x[j + 1]),
                            pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]), pack_f16(x[j + 6], x[j + 7]));
             }
             sync_for_mma();
@@ -1061,8 +1068,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
             // epilogue of the first runs while the second computes.
             // --------------------------------------------------------------
             if (tid == 0) {
-                const Operand KgT{sbase + (FAST ? oRR : MP::KGT), true, 128}, A2h{sbase + RW, false, 128},
-                    WU{sbase + MP::WU, true, 128};
+                const Operand KgT{sbase + (FAST ? oRf : wide_map::KGT), true, 128}, A2h{sbase + RW, false, 128},
+                    WU{sbase + (FAST ? 0u : wide_map::WU), true, 128};
                 mma_128(tmem + 256, A2h, WU, idesc_f16(T_F16, 128, 256, false, true), 8);
                 mma_commit(bar);
                 mma_128(tmem + 0, KgT, WU, idesc_f16(T_F16, 128, 256, true, true), 8);
@@ -1071,7 +1078,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
             wait_mma();
 
             // --------------------------------------------------------------
-            // Phase 7 (fast variant): epilogue through two 32 KB staging
+            // Phase 7 (fast kernel): epilogue through two 32 KB staging
             // buffers, one product at a time, each bulk-stored as soon as it
             // is staged; the buffer is reused once its store has read it.
             //   Qe = Lq diag(exp(P)) - A2 w -> ST1 (the A2 operand's region)
@@ -1092,7 +1099,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                 load_g(cx, hn, 1);
 #pragma unroll
                 for (int j = 0; j < 32; j += 8) {
-                    const uint4 qv = *reinterpret_cast<const uint4*>(sm + oLQ + sw128_off(trow, col0 + j, 128));
+                    const uint4 qv = *reinterpret_cast<const uint4*>(sm + oRawQ + sw128_off(trow, col0 + j, 128));
                     float2 g0 = unpack_f16(qv.x), g1 = unpack_f16(qv.y), g2 = unpack_f16(qv.z), g3 = unpack_f16(qv.w);
                     const float4 e0 = *reinterpret_cast<const float4*>(sEP + col0 + j);
                     const float4 e1 = *reinterpret_cast<const float4*>(sEP + col0 + j + 4);
@@ -1178,10 +1185,9 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                 }
             } else {
                 // ----------------------------------------------------------
-                // Phase 7 (wide variant): epilogue, straight from TMEM to the
-                // workspace tile.
+                // Phase 7 (wide kernel): epilogue, all four tiles staged at once
+                // in the regions free by then, then bulk-stored.
                 //   warps 0-7:  lanes = d;  Nm = -cL (X^T w), Bc = cL X^T u
-                //               (cL = exp(G_last - P) for the fast variant, else 1)
                 //   warps 8-15: lanes = t;  Qe = qg - A2 w, Oi = A2 u
                 // ----------------------------------------------------------
                 uint8_t* dst = tile_ptr(p, c.slot, h);
@@ -1190,7 +1196,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                 // lane quarter each take one Qe block, one Oi block and two Nm
                 // or two Bc blocks: Qe costs about twice the others.
                 const int role = warp >> 2;
-                const float rs = 1.f;   // rows d of Nm / Bc (kg already carries exp(G_last - G))
                 // Qe and Oi are staged over w | u, the operands of the second
                 // product: it has completed before the first part is staged
                 bounded_wait(bar2, phase2);
@@ -1211,41 +1216,36 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                     tmem_ld32(tmem + lane_off + (uint32_t)(kind * 128 + col0), x);
                     tmem_ld_wait();
                     if (kind < 2) {
+                        // kg already carries exp(G_last - G): no row scale
                         if (kind == 0) {
-                            const float ns = -rs;
 #pragma unroll
                             for (int j = 0; j < 32; j += 8)
-                                sts_v4(sm, MP::ST_NM + sw128_off(trow, col0 + j, 128), pack_f16(ns * x[j], ns * x[j + 1]),
-                                       pack_f16(ns * x[j + 2], ns * x[j + 3]), pack_f16(ns * x[j + 4], ns * x[j + 5]),
-                                       pack_f16(ns * x[j + 6], ns * x[j + 7]));
+                                sts_v4(sm, wide_map::ST_NM + sw128_off(trow, col0 + j, 128), pack_f16(-x[j], -x[j + 1]),
+                                       pack_f16(-x[j + 2], -x[j + 3]), pack_f16(-x[j + 4], -x[j + 5]),
+                                       pack_f16(-x[j + 6], -x[j + 7]));
                         } else {
 #pragma unroll
                             for (int j = 0; j < 32; j += 8)
-                                sts_v4(sm, MP::ST_BC + vt * BC_PIECE + sw64_off(trow, j), pack_f16(rs * x[j], rs * x[j + 1]),
-                                       pack_f16(rs * x[j + 2], rs * x[j + 3]), pack_f16(rs * x[j + 4], rs * x[j + 5]),
-                                       pack_f16(rs * x[j + 6], rs * x[j + 7]));
+                                sts_v4(sm, wide_map::ST_BC + vt * BC_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
+                                       pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]),
+                                       pack_f16(x[j + 6], x[j + 7]));
                         }
                     } else {
                         if (kind == 2) {
 #pragma unroll
                             for (int j = 0; j < 32; j += 8) {
-                                const uint4 qv = *reinterpret_cast<const uint4*>(sm + MP::QS + sw128_off(trow, col0 + j, 128));
-                                float2 g0 = unpack_f16(qv.x), g1 = unpack_f16(qv.y), g2 = unpack_f16(qv.z),
-                                       g3 = unpack_f16(qv.w);
-                                if (FAST) {
-                                    const float4 e0 = *reinterpret_cast<const float4*>(sEP + col0 + j);
-                                    const float4 e1 = *reinterpret_cast<const float4*>(sEP + col0 + j + 4);
-                                    g0.x *= e0.x; g0.y *= e0.y; g1.x *= e0.z; g1.y *= e0.w;
-                                    g2.x *= e1.x; g2.y *= e1.y; g3.x *= e1.z; g3.y *= e1.w;
-                                }
-                                sts_v4(sm, MP::ST_QE + sw128_off(trow, col0 + j, 128), pack_f16(g0.x - x[j], g0.y - x[j + 1]),
+                                const uint4 qv =
+                                    *reinterpret_cast<const uint4*>(sm + wide_map::QS + sw128_off(trow, col0 + j, 128));
+                                const float2 g0 = unpack_f16(qv.x), g1 = unpack_f16(qv.y), g2 = unpack_f16(qv.z),
+                                             g3 = unpack_f16(qv.w);
+                                sts_v4(sm, wide_map::ST_QE + sw128_off(trow, col0 + j, 128), pack_f16(g0.x - x[j], g0.y - x[j + 1]),
                                        pack_f16(g1.x - x[j + 2], g1.y - x[j + 3]), pack_f16(g2.x - x[j + 4], g2.y - x[j + 5]),
                                        pack_f16(g3.x - x[j + 6], g3.y - x[j + 7]));
                             }
                         } else {
 #pragma unroll
                             for (int j = 0; j < 32; j += 8)
-                                sts_v4(sm, MP::ST_OI + vt * OI_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
+                                sts_v4(sm, wide_map::ST_OI + vt * OI_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
                                        pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]),
                                        pack_f16(x[j + 6], x[j + 7]));
                         }
@@ -1259,22 +1259,28 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                     dg.w = ex2(sGL[tid * 4 + 3]);
                     *reinterpret_cast<float4*>(dst + TILE_DG + tid * 16) = dg;
                 }
+                // the next chunk's gate rows and beta, as the fast epilogue loads them
+                load_rows(have_n ? cn : none, hn);
                 fence_async_smem();
                 tc_fence_before();
                 __syncthreads();
                 tc_fence_after();
-                if (bulk_thread) {   // asynchronous: drains while the next chunk loads
-                    switch (tid >> 7) {
-                        case 0: bulk_s2g(dst + TILE_NM, sbase + MP::ST_NM, KD * KD * 2); break;
-                        case 1: bulk_s2g(dst + TILE_QE, sbase + MP::ST_QE, BT * KD * 2); break;
-                        case 2: bulk_s2g(dst + TILE_BC, sbase + MP::ST_BC, NVT * BC_PIECE); break;
-                        default: bulk_s2g(dst + TILE_OI, sbase + MP::ST_OI, NVT * OI_PIECE); break;
-                    }
+                if (bulk_thread) {
+                    bulk_s2g(dst + TILE_NM, sbase + wide_map::ST_NM, KD * KD * 2);
+                    bulk_s2g(dst + TILE_QE, sbase + wide_map::ST_QE, BT * KD * 2);
+                    bulk_s2g(dst + TILE_BC, sbase + wide_map::ST_BC, NVT * BC_PIECE);
+                    bulk_s2g(dst + TILE_OI, sbase + wide_map::ST_OI, NVT * OI_PIECE);
                     bulk_commit();
+                    // the next chunk's raw tiles land where this one was staged:
+                    // issued once the stores have read it
+                    if (have_n) {
+                        bulk_wait_read0();
+                        issue_raw(cn, hn, lay ^ 1);
+                    }
                 }
+                if (have_n) raw_pending = true;
             }
         }
-
         idx = nidx;
         item = nitem;
         c = cn;
@@ -1287,7 +1293,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
         if (*sFlag != 0) atomicOr(p.status, STATUS_TIMEOUT);
         // a chunk's raw tiles issued before the loop ended (after a timeout)
         // have landed before the shared memory is released
-        if (FAST && raw_pending) mbar_wait(rawbar, rphase, DRAIN_LIMIT);
+        if (raw_pending) mbar_wait(rawbar, rphase, DRAIN_LIMIT);
         // every product this thread issued has completed before TMEM is freed
         mma_commit(sbase + M_BARD);
         mbar_wait(sbase + M_BARD, 0, DRAIN_LIMIT);
@@ -1341,8 +1347,8 @@ static cudaError_t launch_one(const FwdParams& p, const CUtensorMap (&tm)[3], un
     return cudaGetLastError();
 }
 
-// Host-side launcher: the fast variant over every work item, then the wide
-// variant over whatever the fast one queued (usually nothing; its CTAs then
+// Host-side launcher: the fast kernel over every work item, then the wide
+// kernel over whatever the fast one queued (usually nothing; its CTAs then
 // exit at once).  One persistent CTA per SM, fewer if there is less work.
 cudaError_t launch_prep(const FwdParams& p, bool l2norm, cudaStream_t stream) {
     int dev = 0, sms = 0;

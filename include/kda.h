@@ -130,7 +130,9 @@ size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int N);
  * Precision: bf16 inputs, fp32 gate prefix sums, fp32 (I+A)^-1 and fp32
  * state; tensor-core products take fp16 operands with fp32 accumulation
  * (bf16 operands for the gated q.k / k.k products of chunks whose in-chunk
- * decay is too strong for fp16 factors).
+ * decay is too strong for fp16 factors).  v, and u = (I+A)^-1 diag(beta) v,
+ * enter those products as fp16 in every chunk: they must stay below 65504
+ * (fp16's largest value) in magnitude.
  * The gated products are factored around the chunk's middle row with
  * factors capped at e^80, exact (up to rounding) while the gate decay between
  * that row and the chunk's first or last row stays below 80 in each

@@ -132,7 +132,7 @@ def test_unscaled_gates_wide_path():
 
 def test_mixed_fast_and_wide_chunks():
     """Chunks alternate between weak and strong gates inside one sequence, so
-    one call runs both prep variants; outputs and state still match."""
+    one call runs both prep modes; outputs and state still match."""
     w = custom("mixed_gates", B=1, T=1024, H=3, with_h0=True, seed=23)
     x = make_inputs(w)
     boost = torch.ones(1024)
@@ -141,6 +141,65 @@ def test_mixed_fast_and_wide_chunks():
             boost[j * 128:(j + 1) * 128] = 16.0
     x["g"] = x["g"] * boost[None, :, None, None]
     o, ht = run_gpu(x)
+    o_ref, ht_ref = run_oracle(x)
+    assert_within(compare(o, ht, o_ref, ht_ref))
+
+
+def _fwd_wide_record(x):
+    """Forward through the C ABI on a fresh workspace.  Returns o, ht and the
+    work items (slot * H + head) queued for the wide (bf16) prep kernel: word 1
+    of the workspace header counts them, the list starts at byte 256."""
+    from chunked_gated_delta_kda_gb300 import binding
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    B, T, H, _ = d["q"].shape
+    N = x["N"]
+    o = torch.empty((B, T, H, 128), dtype=torch.bfloat16, device="cuda")
+    ht = torch.empty((N, H, 128, 128), dtype=torch.float32, device="cuda")
+    ws = torch.empty(binding.workspace_bytes(B, T, H, N), dtype=torch.uint8, device="cuda")
+    binding.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d.get("scale"), d["h0"], d["cu_seqlens"],
+                    o, ht, N, 0, ws)
+    torch.cuda.synchronize()
+    n = int(ws[4:8].view(torch.int32).item())
+    items = sorted(ws[256:256 + 4 * n].view(torch.int32).tolist())
+    return o, ht, items
+
+
+def test_wide_mode_chunks_recorded():
+    """Which chunks go to the wide kernel: none at the named workloads'
+    gates; exactly the boosted ones (16x stronger gates, decided from the
+    gate prefix alone) when strong and weak chunks alternate."""
+    H = 3
+    w = custom("mode_record", B=1, T=1024, H=H, with_h0=True, seed=24)
+    x = make_inputs(w)
+    _, _, items = _fwd_wide_record(x)
+    assert items == []
+    boost = torch.ones(1024)
+    for j in (1, 3, 6):
+        boost[j * 128:(j + 1) * 128] = 16.0
+    x["g"] = x["g"] * boost[None, :, None, None]
+    o, ht, items = _fwd_wide_record(x)
+    assert items == sorted(j * H + h for j in (1, 3, 6) for h in range(H))
+    o_ref, ht_ref = run_oracle(x)
+    assert_within(compare(o, ht, o_ref, ht_ref))
+
+
+@pytest.mark.parametrize("row", [0, 127])
+def test_fp16_range_redo(row):
+    """A chunk that passes the gate-only check (largest move from the pivot
+    row ~15.7 in log2 units, below the check's 18) but whose fp16 operands
+    overflow the safe range: dimension 7 of head 1 decays 0.17 per token
+    in chunk 2, and k at its first row (factor exp(G - P) ~ 2^15.7) or last
+    row (exp(P - G) ~ 2^15.4) is 0.9 there.  The chunk is gated in fp16,
+    fails the range check and is redone by the wide kernel; only that
+    (chunk, head) is queued, and the outputs match the oracle."""
+    H = 2
+    x = make_inputs(custom("redo", B=1, T=640, H=H, with_h0=True, seed=25))
+    g, k = x["g"].clone(), x["k"].clone()
+    g[0, 256:384, 1, 7] = -0.17
+    k[0, 256 + row, 1, 7] = 0.9
+    x["g"], x["k"] = g, k
+    o, ht, items = _fwd_wide_record(x)
+    assert items == [2 * H + 1]
     o_ref, ht_ref = run_oracle(x)
     assert_within(compare(o, ht, o_ref, ht_ref))
 
