@@ -69,20 +69,21 @@ constexpr float EXP2_CAP = 115.0f;
 constexpr float FP16_SAFE = 16384.0f;
 
 // Shared-memory regions (bytes from the 1024-aligned base).
-//                  fast kernel (layout 0 | layout 1)           wide kernel
-//   0    .. 64K :  raw k | raw v -> Lk | v16 -> w | u          Lk | Lq -> qg | kg
-//   64K  .. 96K :  raw q -> Lq    | R                          R -> merge tiles -> Ainv
-//   96K  .. 128K:  R              | merge tiles -> Ainv        RHS (k part) -> w
-//   128K .. 160K:  merge tiles -> Ainv | raw q -> Lq           RHS (v part) -> u
-//   160K .. 208K:  fp32 diag blocks -> A2 (160K .. 192K)       qg stash -> fp32
-//                  -> output staging 1; prefix totals at 192K  diag blocks -> A2
-// Chunks alternate between the two fast layouts, so that the next chunk's
-// raw q (in place of this chunk's inverse, or of its R) and raw k, v (in
-// place of w | u) can be loaded while this chunk's output tiles are staged
-// in 96K .. 128K and 160K .. 192K.  The wide kernel's raw tiles sit where
-// the same alternation puts them (k at 0, v at 32K, q at 64K or 128K); its
-// gating reads each 16-byte piece before it writes the same piece of any
-// region, so the wide operands can be written over them.
+//                  fast kernel (layout 0 | layout 1)          wide kernel (layout 0)
+//   0    .. 64K :  raw k | raw v -> Lk | v16 -> w | u         raw k | raw v -> Lk | Lq -> qg | kg
+//   64K  .. 96K :  raw q -> Lq    | R                         raw q -> R -> merge tiles -> Ainv
+//                                                              -> Qe staging
+//   96K  .. 128K:  R              | merge tiles -> Ainv       RHS (k part) -> w -> Nm staging
+//   128K .. 160K:  merge tiles -> Ainv | raw q -> Lq          RHS (v part) -> u -> Bc staging
+//   160K .. 208K:  fp32 diag blocks -> A2 (160K .. 192K)      qg stash -> fp32 diag blocks -> A2
+//                  -> output staging 1; prefix totals at 192K -> Oi staging; prefix totals at 192K
+// The fast kernel's chunks alternate between its two layouts, so that the
+// next chunk's raw q (in place of this chunk's inverse, or of its R) and raw
+// k, v (in place of w | u) can be loaded while this chunk's output tiles are
+// staged in 96K .. 128K and 160K .. 192K.  The wide kernel keeps layout 0
+// (raw q at 64K, requested once the Qe staging there has been stored); its
+// gating reads each 16-byte piece of the raw tiles before it writes the same
+// piece of any region, so the wide operands can be written over them.
 constexpr uint32_t RM = 213248;            // misc
 constexpr uint32_t M_G64 = RM;             // f32[128]  G at the pivot row (log2 units)
 constexpr uint32_t M_GL = RM + 512;        // f32[128]  G at the last row (log2 units)
@@ -127,11 +128,13 @@ constexpr uint32_t B2 = 98304;     // B operand of the WY product (N = 256): [be
 constexpr uint32_t WU = 98304;     // w | u (N = 256), over B2
 constexpr uint32_t KGT = 32768;    // kg: A operand (MN-major) of the Nm | Bc product, over Lq
 constexpr uint32_t QS = 0;         // qg for the Qe epilogue, over Lk
-// staging of the output tiles for the bulk stores (regions free by then)
-constexpr uint32_t ST_NM = 65536;
-constexpr uint32_t ST_BC = 32768;
-constexpr uint32_t ST_QE = 98304;
-constexpr uint32_t ST_OI = 131072;
+// staging of the output tiles for the bulk stores: Qe and Oi once the first
+// transition product is done (over Ainv and A2), Nm and Bc once the second
+// is (over w | u)
+constexpr uint32_t ST_QE = 65536;
+constexpr uint32_t ST_OI = RW;
+constexpr uint32_t ST_NM = 98304;
+constexpr uint32_t ST_BC = 131072;
 }  // namespace wide_map
 // The fast kernel's gate-only check: a chunk whose gate prefix moves more
 // than this (log2 units) between the pivot row and the chunk's first or last
@@ -177,10 +180,6 @@ __device__ __forceinline__ float2 unpack_f16(uint32_t u) {
     __half2 h = *reinterpret_cast<__half2*>(&u);
     return __half22float2(h);
 }
-__device__ __forceinline__ uint32_t ldg_u32(const uint16_t* p) {
-    return __ldg(reinterpret_cast<const unsigned int*>(p));
-}
-__device__ __forceinline__ float2 ldg_f2(const float* p) { return __ldg(reinterpret_cast<const float2*>(p)); }
 
 // Read-once input rows (one head's rows of one chunk): loaded with an L2
 // evict-first policy so that they leave L2 ahead of the prefetched rows of
@@ -1185,71 +1184,72 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                 }
             } else {
                 // ----------------------------------------------------------
-                // Phase 7 (wide kernel): epilogue, all four tiles staged at once
-                // in the regions free by then, then bulk-stored.
-                //   warps 0-7:  lanes = d;  Nm = -cL (X^T w), Bc = cL X^T u
-                //   warps 8-15: lanes = t;  Qe = qg - A2 w, Oi = A2 u
+                // Phase 7 (wide kernel): epilogue in two stages.
+                //   1. (first product done, the second still running)
+                //      Qe = qg - A2 w -> ST_QE (Ainv's region),
+                //      Oi = A2 u      -> ST_OI (A2's region); bulk-stored.
+                //   2. (second product done)
+                //      Nm = -kg^T w -> ST_NM, Bc = kg^T u -> ST_BC (over
+                //      w | u); bulk-stored.  The next chunk's raw tiles
+                //      (k over qg, v over kg, q over ST_QE) are requested
+                //      once the Qe store has read its staging.
+                // Lanes are rows (t for Qe / Oi, d for Nm / Bc); the four warps
+                // of a lane quarter take one 32-column block of each product
+                // (TMEM columns: Nm 0, Bc 128, Qe 256, Oi 384, + 32 role).
                 // ----------------------------------------------------------
                 uint8_t* dst = tile_ptr(p, c.slot, h);
-                // 32-column blocks of the four products (kind 0 Nm, 1 Bc, 2 Qe,
-                // 3 Oi; TMEM columns kind * 128 + vt * 32).  The four warps of a
-                // lane quarter each take one Qe block, one Oi block and two Nm
-                // or two Bc blocks: Qe costs about twice the others.
                 const int role = warp >> 2;
-                // Qe and Oi are staged over w | u, the operands of the second
-                // product: it has completed before the first part is staged
+                const int col0 = role * 32;
+                {
+                    float x[32];
+                    tmem_ld32(tmem + lane_off + 256u + (uint32_t)col0, x);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        const uint4 qv =
+                            *reinterpret_cast<const uint4*>(sm + wide_map::QS + sw128_off(trow, col0 + j, 128));
+                        const float2 g0 = unpack_f16(qv.x), g1 = unpack_f16(qv.y), g2 = unpack_f16(qv.z),
+                                     g3 = unpack_f16(qv.w);
+                        sts_v4(sm, wide_map::ST_QE + sw128_off(trow, col0 + j, 128),
+                               pack_f16(g0.x - x[j], g0.y - x[j + 1]), pack_f16(g1.x - x[j + 2], g1.y - x[j + 3]),
+                               pack_f16(g2.x - x[j + 4], g2.y - x[j + 5]), pack_f16(g3.x - x[j + 6], g3.y - x[j + 7]));
+                    }
+                    tmem_ld32(tmem + lane_off + 384u + (uint32_t)col0, x);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8)
+                        sts_v4(sm, wide_map::ST_OI + role * OI_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
+                               pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]),
+                               pack_f16(x[j + 6], x[j + 7]));
+                }
+                fence_async_smem();
+                __syncthreads();
+                if (bulk_thread) {
+                    bulk_s2g(dst + TILE_QE, sbase + wide_map::ST_QE, BT * KD * 2);
+                    bulk_s2g(dst + TILE_OI, sbase + wide_map::ST_OI, NVT * OI_PIECE);
+                    bulk_commit();
+                }
+                // the second product has read w | u and kg
                 bounded_wait(bar2, phase2);
                 phase2 ^= 1;
                 tc_fence_after();
-#pragma unroll
-                for (int part = 0; part < 4; ++part) {
+                {
                     float x[32];
-                    int kind, vt;
-                    if (part < 2) {
-                        kind = 2 + part;
-                        vt = role;
-                    } else {
-                        kind = role & 1;
-                        vt = (role & 2) + (part - 2);
-                    }
-                    const int col0 = vt * 32;
-                    tmem_ld32(tmem + lane_off + (uint32_t)(kind * 128 + col0), x);
+                    // kg already carries exp(G_last - G): no row scale
+                    tmem_ld32(tmem + lane_off + (uint32_t)col0, x);
                     tmem_ld_wait();
-                    if (kind < 2) {
-                        // kg already carries exp(G_last - G): no row scale
-                        if (kind == 0) {
 #pragma unroll
-                            for (int j = 0; j < 32; j += 8)
-                                sts_v4(sm, wide_map::ST_NM + sw128_off(trow, col0 + j, 128), pack_f16(-x[j], -x[j + 1]),
-                                       pack_f16(-x[j + 2], -x[j + 3]), pack_f16(-x[j + 4], -x[j + 5]),
-                                       pack_f16(-x[j + 6], -x[j + 7]));
-                        } else {
+                    for (int j = 0; j < 32; j += 8)
+                        sts_v4(sm, wide_map::ST_NM + sw128_off(trow, col0 + j, 128), pack_f16(-x[j], -x[j + 1]),
+                               pack_f16(-x[j + 2], -x[j + 3]), pack_f16(-x[j + 4], -x[j + 5]),
+                               pack_f16(-x[j + 6], -x[j + 7]));
+                    tmem_ld32(tmem + lane_off + 128u + (uint32_t)col0, x);
+                    tmem_ld_wait();
 #pragma unroll
-                            for (int j = 0; j < 32; j += 8)
-                                sts_v4(sm, wide_map::ST_BC + vt * BC_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
-                                       pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]),
-                                       pack_f16(x[j + 6], x[j + 7]));
-                        }
-                    } else {
-                        if (kind == 2) {
-#pragma unroll
-                            for (int j = 0; j < 32; j += 8) {
-                                const uint4 qv =
-                                    *reinterpret_cast<const uint4*>(sm + wide_map::QS + sw128_off(trow, col0 + j, 128));
-                                const float2 g0 = unpack_f16(qv.x), g1 = unpack_f16(qv.y), g2 = unpack_f16(qv.z),
-                                             g3 = unpack_f16(qv.w);
-                                sts_v4(sm, wide_map::ST_QE + sw128_off(trow, col0 + j, 128), pack_f16(g0.x - x[j], g0.y - x[j + 1]),
-                                       pack_f16(g1.x - x[j + 2], g1.y - x[j + 3]), pack_f16(g2.x - x[j + 4], g2.y - x[j + 5]),
-                                       pack_f16(g3.x - x[j + 6], g3.y - x[j + 7]));
-                            }
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 32; j += 8)
-                                sts_v4(sm, wide_map::ST_OI + vt * OI_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
-                                       pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]),
-                                       pack_f16(x[j + 6], x[j + 7]));
-                        }
-                    }
+                    for (int j = 0; j < 32; j += 8)
+                        sts_v4(sm, wide_map::ST_BC + role * BC_PIECE + sw64_off(trow, j), pack_f16(x[j], x[j + 1]),
+                               pack_f16(x[j + 2], x[j + 3]), pack_f16(x[j + 4], x[j + 5]),
+                               pack_f16(x[j + 6], x[j + 7]));
                 }
                 if (tid < 32) {
                     float4 dg;
@@ -1267,15 +1267,11 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                 tc_fence_after();
                 if (bulk_thread) {
                     bulk_s2g(dst + TILE_NM, sbase + wide_map::ST_NM, KD * KD * 2);
-                    bulk_s2g(dst + TILE_QE, sbase + wide_map::ST_QE, BT * KD * 2);
                     bulk_s2g(dst + TILE_BC, sbase + wide_map::ST_BC, NVT * BC_PIECE);
-                    bulk_s2g(dst + TILE_OI, sbase + wide_map::ST_OI, NVT * OI_PIECE);
                     bulk_commit();
-                    // the next chunk's raw tiles land where this one was staged:
-                    // issued once the stores have read it
                     if (have_n) {
-                        bulk_wait_read0();
-                        issue_raw(cn, hn, lay ^ 1);
+                        bulk_wait_read1();   // the Qe / Oi stores have read their staging
+                        issue_raw(cn, hn, 0);
                     }
                 }
                 if (have_n) raw_pending = true;
@@ -1286,7 +1282,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
         c = cn;
         h = hn;
         have = have_n;
-        lay ^= 1;
+        if (FAST) lay ^= 1;   // the wide kernel keeps layout 0 (raw q at 64K)
     }
     if (bulk_thread) bulk_wait0();
     if (tid == 0) {
