@@ -14,6 +14,7 @@ this method exists to run).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -592,6 +593,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--gate-div", type=float, default=None,
+                    help="forward: divide logsigmoid(N(0,1)) by this for g instead of the workload's 16 "
+                         "(1 = the pages' unscaled stable-input gates, whose chunks take the wide prep kernel)")
     ap.add_argument("--op", choices=["fwd", "decode", "bwd"], default="fwd",
                     help="fwd: the chunked forward (default); decode: the token-by-token entry point; "
                          "bwd: the chunked backward")
@@ -600,6 +604,9 @@ def main():
 
     world, rank, local = rank_env()
     w = WORKLOADS[args.workload]
+    if args.gate_div is not None:
+        assert args.op == "fwd", "--gate-div applies to the forward"
+        w = dataclasses.replace(w, gate_div=args.gate_div)
 
     if args.op == "decode":
         return run_decode(args, rank, world, local)
@@ -660,6 +667,9 @@ def main():
     scan_ms = sum(ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)) / args.steps
     st = binding.get_status(ws)
     assert st == 0, f"device status {st}"
+    # chunks the last step queued for the wide (bf16) prep kernel: word 1 of
+    # the workspace header
+    wide_chunks = int(ws[4:8].view(torch.int32).item())
 
     ms_per_step = max_over_ranks(total_ms, dev, world) / args.steps
 
@@ -691,7 +701,8 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 in/out; fp16 MMA operands, fp32 accumulate, fp32 state", "data": "synthetic",
         "config": {"workload": w.name, "B": B, "T": T, "H": H, "K": w.K, "V": w.V, "chunk": 128,
-                   "h0": h0 is not None, "output_final_state": True,
+                   "h0": h0 is not None, "output_final_state": True, "gate_div": w.gate_div,
+                   "wide_chunks": wide_chunks,
                    "l2_between_steps": "inputs (2.7 GB per step) larger than L2 (129 MB); no flush",
                    "inputs": "seeded synthetic, drawn on device with the workload's recipe"},
         "tflops_alg": alg_flop / (ms_per_step * 1e-3) / 1e12,
