@@ -688,7 +688,9 @@ def main():
     dom = max(stages, key=lambda s: stages[s]["ms"])
     d = stages[dom]
     achieved = d["alg_bytes"] / (d["ms"] * 1e-3) / 1e9
-    tr = traffic.get(dom)
+    # the committed traffic row is the fast prep kernel's: it does not
+    # describe a step whose chunks went to the wide kernel
+    tr = traffic.get(dom) if (dom != "kda_prep_kernel" or wide_chunks == 0) else None
     roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"],
                 "traffic": (tr * th if tr is not None else None),
