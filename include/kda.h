@@ -188,11 +188,10 @@ kda_status kda_get_status(const void* workspace, cudaStream_t stream);
  * cudaFree, no allocating library routine.
  *
  * The first call on each device looks up the array's device address with
- * cudaGetSymbolAddress (with that device current); make that first call
- * before any stream capture begins.  Every call on a device shares the one
- * array: calls whose GPU work overlaps in time (on different streams, or
- * from different host threads) race on it and give undefined results, so
- * serialise them.  kda_get_status() is not available for this entry point
+ * cudaGetSymbolAddress (with that device current).  Every call on a device
+ * shares the one array: calls whose GPU work overlaps in time (on different
+ * streams, or from different host threads) race on it and give undefined
+ * results, so serialise them.  kda_get_status() is not available for this entry point
  * (the status word lives in the shared array).
  */
 kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, const float* g, const float* beta,
