@@ -183,6 +183,45 @@ def test_wide_mode_chunks_recorded():
     assert_within(compare(o, ht, o_ref, ht_ref))
 
 
+@pytest.mark.parametrize("case", ["varlen_tails", "l2norm"])
+def test_wide_kernel_variants(case):
+    """The wide prep kernel on ragged varlen tails (every sequence's last
+    chunk partial, one sequence shorter than a chunk) and with in-kernel q/k
+    normalisation: the pages' unscaled gates send every chunk to it, and
+    the results match the oracle."""
+    if case == "varlen_tails":
+        lens = [300, 77, 513, 129]
+        x = make_inputs(custom(case, B=1, T=sum(lens), H=2, seqlens=lens, with_h0=True, seed=26, gate_div=1.0))
+        o, ht, items = _fwd_wide_record(x)
+        # every chunk whose gate prefix moves more than 18 (log2 units)
+        # between row 63 and the chunk's first or last row is queued (the
+        # short tails may stay in the fast kernel); varlen slot of chunk j of
+        # sequence n: floor(cu[n] / 128) + n + j
+        g = x["g"].numpy()[0].astype(np.float64) * np.log2(np.e)
+        cu = np.cumsum([0] + lens)
+        must = set()
+        for n_, L_seq in enumerate(lens):
+            for j in range((L_seq + 127) // 128):
+                rows = g[cu[n_] + 128 * j: cu[n_] + min(128 * (j + 1), L_seq)]
+                G = np.cumsum(rows, axis=0)
+                g63 = G[min(63, len(G) - 1)]
+                span = np.maximum(np.abs(g63), np.abs(G[-1] - g63)).max(axis=-1)
+                for h in range(2):
+                    if span[h] > 18.0:
+                        must.add((cu[n_] // 128 + n_ + j) * 2 + h)
+        assert len(must) >= 12 and must <= set(items)
+        o_ref, ht_ref = run_oracle(x)
+        assert_within(compare(o, ht, o_ref, ht_ref, cu=x["cu_seqlens"].numpy()))
+    else:
+        x = make_inputs(custom(case, B=1, T=640, H=2, with_h0=True, seed=27, gate_div=1.0))
+        gen = torch.Generator().manual_seed(98)
+        x["q"] = (x["q"].float() * (0.5 + torch.rand(x["q"].shape[:3] + (1,), generator=gen) * 3)).bfloat16()
+        x["k"] = (x["k"].float() * (0.5 + torch.rand(x["k"].shape[:3] + (1,), generator=gen) * 3)).bfloat16()
+        o, ht = run_gpu(x, l2norm=True)
+        o_ref, ht_ref = run_oracle(x, l2norm=True)
+        assert_within(compare(o, ht, o_ref, ht_ref))
+
+
 @pytest.mark.parametrize("row", [0, 127])
 def test_fp16_range_redo(row):
     """A chunk that passes the gate-only check (largest move from the pivot
