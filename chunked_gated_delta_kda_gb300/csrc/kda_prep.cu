@@ -976,7 +976,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
             }
             // Assemble (I + A)^-1 as fp16, K-major [c][i], in region Y:
             //   rows 0..63:  [P | 0],   rows 64..127: [L | Q]   (unit diagonal)
-            // The fast variant folds diag(beta) into its columns.  P (over A10,
+            // The fast kernel folds diag(beta) into its columns.  P (over A10,
             // read by the finished first merge product) and Q (over nothing)
             // are written while the second product runs; the zeros (over its
             // Q operand) and L (its result) after it.

@@ -15,13 +15,15 @@
 // A CTA of 4 warps covers 32 value rows of one (sequence, head); the grid is
 // (V / 32, H, N).  Over a sequence the token steps form one dependent chain
 // per warp, so the exact recompute (long sequences) loads each token's
-// inputs four tokens before its step (51 ms against 82 without the lookahead
-// and 56 with eight, for the exact forward of T=65536, H=32); the decode
-// kernel, one or a few tokens per sequence and bound by the state traffic,
-// keeps the plain loop (the lookahead's registers cost it occupancy: 0.174
-// against 0.162 ms on the decode workload).  The state is read once and written once per call (once
-// per token in speculative mode), so the kernel is bound by HBM traffic on
-// the state, 2 x 64 KiB per (sequence, head).
+// inputs ahead of its step, four tokens ahead with eight rows per warp and
+// one four-token window ahead with two (51 ms against 82 without the
+// lookahead and 56 with eight, for the exact forward of T=65536, H=32); the
+// decode kernel, one or a few tokens per sequence and bound by the state
+// traffic, keeps the plain loop (the lookahead's registers cost it
+// occupancy: 0.174 against 0.162 ms on the decode workload).  The state is
+// read once and written once per call (once per token in speculative mode),
+// so the kernel is bound by HBM traffic on the state, 2 x 64 KiB per
+// (sequence, head).
 #include <cuda_bf16.h>
 
 #include "kda.h"
@@ -37,8 +39,10 @@ constexpr int REC_ROWS_CTA = REC_ROWS * (REC_THREADS / 32);
 // The exact recompute gives each warp two value rows when there are few
 // units (with eight, 32 or fewer units put less than one warp on each SM
 // sub-partition: 4.2 -> 2.9 ms for 4 units of 8192 tokens, 51 -> 49 ms for
-// 32 units of 65536), eight otherwise (with two, each token's q / k / g
-// rows are loaded four times as often: 6.7 -> 11.6 ms for 64 units of 8192).
+// 32 units of 65536), stepped four tokens at a time with one warp reduction
+// per window (2.9 -> 2.15 ms and 48.9 -> 47.7 ms); eight rows and one token
+// at a time otherwise (with two, each token's q / k / g rows are loaded four
+// times as often: 6.7 -> 11.6 ms for 64 units of 8192).
 constexpr int EXACT_FEW_UNITS = 32;
 
 struct RecParams {
@@ -102,18 +106,6 @@ __device__ __forceinline__ TokIn<ROWS> load_tok(const uint16_t* __restrict__ q, 
     return in;
 }
 
-// All-reduce two per-lane partial sums over the warp: one exchange on lane
-// bit 4 leaves each half-warp with one row's pair sums, a butterfly over the
-// other four bits completes it, then both totals are fetched.
-__device__ __forceinline__ void warp_sum2(float (&a)[2], int lane) {
-    const bool h16 = lane & 16;
-    float b = (h16 ? a[1] : a[0]) + __shfl_xor_sync(0xffffffffu, h16 ? a[0] : a[1], 16);
-#pragma unroll
-    for (int m = 8; m > 0; m >>= 1) b += __shfl_xor_sync(0xffffffffu, b, m);
-    a[0] = __shfl_sync(0xffffffffu, b, 0);
-    a[1] = __shfl_sync(0xffffffffu, b, 16);
-}
-
 // One token of the recurrence on this warp's ROWS value rows (row v0 + r in
 // s[r], lane owning K entries 4 lane .. 4 lane + 3): decay, delta update,
 // read-out; lane 0 writes the ROWS bf16 outputs.  `tok` indexes (token, head).
@@ -148,10 +140,8 @@ __device__ __forceinline__ void rec_token(const TokIn<ROWS>& in, uint16_t* __res
     }
     const float e[4] = {__expf(gv.x), __expf(gv.y), __expf(gv.z), __expf(gv.w)};
 
-    auto reduce = [&](float (&d)[ROWS]) {
-        if constexpr (ROWS == 8) warp_sum8(d, lane);
-        else warp_sum2(d, lane);
-    };
+    static_assert(ROWS == 8, "eight value rows per warp");
+    auto reduce = [&](float (&d)[ROWS]) { warp_sum8(d, lane); };
     // decay, then k . s_v
     float dot[ROWS];
 #pragma unroll
@@ -182,64 +172,8 @@ __device__ __forceinline__ void rec_token(const TokIn<ROWS>& in, uint16_t* __res
         __nv_bfloat162 o2[ROWS / 2];
 #pragma unroll
         for (int j = 0; j < ROWS / 2; ++j) o2[j] = __floats2bfloat162_rn(dot[2 * j], dot[2 * j + 1]);
-        if constexpr (ROWS == 8) *reinterpret_cast<uint4*>(o + tok * VD + v0) = *reinterpret_cast<const uint4*>(o2);
-        else *reinterpret_cast<__nv_bfloat162*>(o + tok * VD + v0) = o2[0];
+        *reinterpret_cast<uint4*>(o + tok * VD + v0) = *reinterpret_cast<const uint4*>(o2);
     }
-}
-
-// The same token step for two value rows with one warp reduction instead of
-// two: with s_d the decayed state and delta = beta (v - k.s_d), the read-out
-// of the updated state is q.s_d + delta (q.k), so k.s_d, q.s_d (both rows)
-// and q.k are reduced together.  The exact recompute's chain per token is
-// then one reduction long.
-__device__ __forceinline__ void rec_token_one_reduction(const TokIn<2>& in, uint16_t* __restrict__ o, float scale,
-                                                        bool l2norm, size_t tok, int v0, int lane, float (&s)[2][4]) {
-    float qv[4], kv[4];
-    qv[0] = __uint_as_float(in.q.x << 16); qv[1] = __uint_as_float(in.q.x & 0xffff0000u);
-    qv[2] = __uint_as_float(in.q.y << 16); qv[3] = __uint_as_float(in.q.y & 0xffff0000u);
-    kv[0] = __uint_as_float(in.k.x << 16); kv[1] = __uint_as_float(in.k.x & 0xffff0000u);
-    kv[2] = __uint_as_float(in.k.y << 16); kv[3] = __uint_as_float(in.k.y & 0xffff0000u);
-    const float vv[2] = {__uint_as_float(in.v[0] << 16), __uint_as_float(in.v[0] & 0xffff0000u)};
-    float qs = scale, ks = 1.f;
-    if (l2norm) {   // x / sqrt(sum x^2 + 1e-6), section "测试与验证体系"
-        const float sq = warp_sum(qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3]);
-        const float sk = warp_sum(kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3]);
-        qs *= rsqrtf(sq + 1e-6f);
-        ks = rsqrtf(sk + 1e-6f);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        qv[i] *= qs;
-        kv[i] *= ks;
-    }
-    const float e[4] = {__expf(in.g.x), __expf(in.g.y), __expf(in.g.z), __expf(in.g.w)};
-    // [k.s_d row 0, row 1, q.s_d row 0, row 1, q.k, -, -, -]
-    float d[8];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        float ak = 0.f, aq = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            s[r][i] *= e[i];
-            ak = fmaf(kv[i], s[r][i], ak);
-            aq = fmaf(qv[i], s[r][i], aq);
-        }
-        d[r] = ak;
-        d[2 + r] = aq;
-    }
-    d[4] = qv[0] * kv[0] + qv[1] * kv[1] + qv[2] * kv[2] + qv[3] * kv[3];
-    d[5] = d[6] = d[7] = 0.f;
-    warp_sum8(d, lane);
-    float out[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const float delta = in.beta * (vv[r] - d[r]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) s[r][i] = fmaf(kv[i], delta, s[r][i]);
-        out[r] = fmaf(delta, d[4], d[2 + r]);
-    }
-    if (lane == 0)
-        *reinterpret_cast<__nv_bfloat162*>(o + tok * VD + v0) = __floats2bfloat162_rn(out[0], out[1]);
 }
 
 // Tokens 0 .. len - 1 of one (sequence, head) starting at packed token bos:
@@ -272,15 +206,188 @@ __device__ __forceinline__ void rec_tokens(const uint16_t* __restrict__ q, const
                     const TokIn<ROWS> cur = ring[i];
                     if (t + AHEAD < len)
                         ring[i] = load_tok<ROWS>(q, k, v, g, beta, (size_t)(bos + t + AHEAD) * H + h, v0, lane);
-                    if constexpr (ROWS == 2)
-                        rec_token_one_reduction(cur, o, scale, l2norm, (size_t)(bos + t) * H + h, v0, lane, s);
-                    else
-                        rec_token<ROWS>(cur, o, scale, l2norm, (size_t)(bos + t) * H + h, v0, lane, s);
+                    rec_token<ROWS>(cur, o, scale, l2norm, (size_t)(bos + t) * H + h, v0, lane, s);
                     after(t);
                 }
             }
         }
     }
+}
+
+// Four tokens at once on this warp's two value rows (the exact recompute).
+// With S the state before the window, D_i the decay from there through token
+// i (the product of exp(g) over tokens 0 .. i) and F_ij = D_i / D_j (the
+// product over tokens j+1 .. i, so no division and no range limit), the
+// per-token rule unrolls to
+//   delta_i = beta_i (v_i - (k_i D_i).S - sum_{j<i} c_ij delta_j),
+//   o_i     = (q_i D_i).S + sum_{j<=i} d_ij delta_j,
+//   S'      = D_3 S + sum_j (k_j F_3j) delta_j^T,
+// c_ij = sum k_i k_j F_ij, d_ij = sum q_i k_j F_ij.  All 32 dot products of
+// the window go through one warp reduction (a reduce-scatter, then the totals
+// through shared memory) instead of one reduction per token.  Tokens n .. 3
+// of a last partial window are inert (beta = 0, no decay, no output).
+__device__ __forceinline__ void rec_window4(const TokIn<2> (&in)[4], int n, uint16_t* __restrict__ o, float scale,
+                                            bool l2norm, size_t tok0, int H, int v0, int lane, float (&s)[2][4],
+                                            float* red) {
+    float qv[4][4], kv[4][4], e[4][4], bt[4], vv[4][2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const bool ok = i < n;
+        qv[i][0] = __uint_as_float(in[i].q.x << 16); qv[i][1] = __uint_as_float(in[i].q.x & 0xffff0000u);
+        qv[i][2] = __uint_as_float(in[i].q.y << 16); qv[i][3] = __uint_as_float(in[i].q.y & 0xffff0000u);
+        kv[i][0] = __uint_as_float(in[i].k.x << 16); kv[i][1] = __uint_as_float(in[i].k.x & 0xffff0000u);
+        kv[i][2] = __uint_as_float(in[i].k.y << 16); kv[i][3] = __uint_as_float(in[i].k.y & 0xffff0000u);
+        e[i][0] = ok ? __expf(in[i].g.x) : 1.f;
+        e[i][1] = ok ? __expf(in[i].g.y) : 1.f;
+        e[i][2] = ok ? __expf(in[i].g.z) : 1.f;
+        e[i][3] = ok ? __expf(in[i].g.w) : 1.f;
+        bt[i] = ok ? in[i].beta : 0.f;
+        vv[i][0] = ok ? __uint_as_float(in[i].v[0] << 16) : 0.f;
+        vv[i][1] = ok ? __uint_as_float(in[i].v[0] & 0xffff0000u) : 0.f;
+        if (!ok) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) qv[i][x] = kv[i][x] = 0.f;
+        }
+    }
+    float ks[4] = {1.f, 1.f, 1.f, 1.f}, qs[4] = {scale, scale, scale, scale};
+    if (l2norm) {   // x / sqrt(sum x^2 + 1e-6), section "测试与验证体系"
+        float nr[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            nr[i] = kv[i][0] * kv[i][0] + kv[i][1] * kv[i][1] + kv[i][2] * kv[i][2] + kv[i][3] * kv[i][3];
+            nr[4 + i] = qv[i][0] * qv[i][0] + qv[i][1] * qv[i][1] + qv[i][2] * qv[i][2] + qv[i][3] * qv[i][3];
+        }
+        warp_sum8(nr, lane);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ks[i] = rsqrtf(nr[i] + 1e-6f);
+            qs[i] = scale * rsqrtf(nr[4 + i] + 1e-6f);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            kv[i][x] *= ks[i];
+            qv[i][x] *= qs[i];
+        }
+    // decays: D_i (from the window start), F_ij (j < i)
+    float D[4][4], F10[4], F20[4], F21[4], F30[4], F31[4], F32[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        D[0][x] = e[0][x];
+        D[1][x] = D[0][x] * e[1][x];
+        D[2][x] = D[1][x] * e[2][x];
+        D[3][x] = D[2][x] * e[3][x];
+        F10[x] = e[1][x];
+        F21[x] = e[2][x];
+        F32[x] = e[3][x];
+        F20[x] = e[1][x] * e[2][x];
+        F31[x] = e[2][x] * e[3][x];
+        F30[x] = F20[x] * e[3][x];
+    }
+    // this lane's parts of the 32 dot products:
+    //   [2i + r] (k_i D_i).s_r, [8 + 2i + r] (q_i D_i).s_r,
+    //   [16 ..] c_10 c_20 c_21 c_30 c_31 c_32, [22 ..] d_00 d_10 d_11 d_20 d_21 d_22 d_30 d_31 d_32 d_33
+    float a[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            float ak = 0.f, aq = 0.f;
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                ak = fmaf(kv[i][x] * D[i][x], s[r][x], ak);
+                aq = fmaf(qv[i][x] * D[i][x], s[r][x], aq);
+            }
+            a[2 * i + r] = ak;
+            a[8 + 2 * i + r] = aq;
+        }
+    auto dot3 = [&](const float (&u)[4], const float (&w)[4], const float (&f)[4]) {
+        return u[0] * w[0] * f[0] + u[1] * w[1] * f[1] + u[2] * w[2] * f[2] + u[3] * w[3] * f[3];
+    };
+    auto dot2 = [&](const float (&u)[4], const float (&w)[4]) {
+        return u[0] * w[0] + u[1] * w[1] + u[2] * w[2] + u[3] * w[3];
+    };
+    a[16] = dot3(kv[1], kv[0], F10);
+    a[17] = dot3(kv[2], kv[0], F20);
+    a[18] = dot3(kv[2], kv[1], F21);
+    a[19] = dot3(kv[3], kv[0], F30);
+    a[20] = dot3(kv[3], kv[1], F31);
+    a[21] = dot3(kv[3], kv[2], F32);
+    a[22] = dot2(qv[0], kv[0]);
+    a[23] = dot3(qv[1], kv[0], F10);
+    a[24] = dot2(qv[1], kv[1]);
+    a[25] = dot3(qv[2], kv[0], F20);
+    a[26] = dot3(qv[2], kv[1], F21);
+    a[27] = dot2(qv[2], kv[2]);
+    a[28] = dot3(qv[3], kv[0], F30);
+    a[29] = dot3(qv[3], kv[1], F31);
+    a[30] = dot3(qv[3], kv[2], F32);
+    a[31] = dot2(qv[3], kv[3]);
+    // reduce-scatter by halving: after the five exchanges lane l holds the
+    // warp total of entry l
+    {
+        float b16[16], b8[8], b4[4], b2[2];
+        const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2, h1 = lane & 1;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            b16[j] = (h16 ? a[j + 16] : a[j]) + __shfl_xor_sync(0xffffffffu, h16 ? a[j] : a[j + 16], 16);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            b8[j] = (h8 ? b16[j + 8] : b16[j]) + __shfl_xor_sync(0xffffffffu, h8 ? b16[j] : b16[j + 8], 8);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            b4[j] = (h4 ? b8[j + 4] : b8[j]) + __shfl_xor_sync(0xffffffffu, h4 ? b8[j] : b8[j + 4], 4);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            b2[j] = (h2 ? b4[j + 2] : b4[j]) + __shfl_xor_sync(0xffffffffu, h2 ? b4[j] : b4[j + 2], 2);
+        const float t = (h1 ? b2[1] : b2[0]) + __shfl_xor_sync(0xffffffffu, h1 ? b2[0] : b2[1], 1);
+        red[lane] = t;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        const float4 t = *reinterpret_cast<const float4*>(red + j);
+        a[j] = t.x; a[j + 1] = t.y; a[j + 2] = t.z; a[j + 3] = t.w;
+    }
+    __syncwarp();   // every lane has read the totals before the next window writes them
+    // the four deltas and outputs per value row
+    float dl[4][2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        dl[0][r] = bt[0] * (vv[0][r] - a[r]);
+        dl[1][r] = bt[1] * (vv[1][r] - a[2 + r] - a[16] * dl[0][r]);
+        dl[2][r] = bt[2] * (vv[2][r] - a[4 + r] - a[17] * dl[0][r] - a[18] * dl[1][r]);
+        dl[3][r] = bt[3] * (vv[3][r] - a[6 + r] - a[19] * dl[0][r] - a[20] * dl[1][r] - a[21] * dl[2][r]);
+    }
+    if (lane == 0) {
+        float ov[4][2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            ov[0][r] = a[8 + r] + a[22] * dl[0][r];
+            ov[1][r] = a[10 + r] + a[23] * dl[0][r] + a[24] * dl[1][r];
+            ov[2][r] = a[12 + r] + a[25] * dl[0][r] + a[26] * dl[1][r] + a[27] * dl[2][r];
+            ov[3][r] = a[14 + r] + a[28] * dl[0][r] + a[29] * dl[1][r] + a[30] * dl[2][r] + a[31] * dl[3][r];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (i < n)
+                *reinterpret_cast<__nv_bfloat162*>(o + (tok0 + (size_t)i * H) * VD + v0) =
+                    __floats2bfloat162_rn(ov[i][0], ov[i][1]);
+    }
+    // state after the window
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            float y = D[3][x] * s[r][x];
+            y = fmaf(kv[0][x] * F30[x], dl[0][r], y);
+            y = fmaf(kv[1][x] * F31[x], dl[1][r], y);
+            y = fmaf(kv[2][x] * F32[x], dl[2][r], y);
+            y = fmaf(kv[3][x], dl[3][r], y);
+            s[r][x] = y;
+        }
 }
 
 }  // namespace
@@ -362,7 +469,9 @@ __global__ void __launch_bounds__(REC_THREADS) kda_recurrent_kernel(const RecPar
 // some chunk's in-chunk decay exceeded the range of exact factored products
 // (flagged by the chunk-parallel kernel) are recomputed here token by token,
 // from h0, overwriting the chunked result's o and final state.  The
-// recurrence is the same per-token rule, so it is exact for any decay.
+// recurrence is the same per-token rule (with two rows per warp, unrolled
+// over windows of four tokens with exact pairwise decays), so it is exact
+// for any decay.
 template <int ROWS>
 __global__ void __launch_bounds__(REC_THREADS) kda_exact_kernel(const FwdParams p, const uint32_t* flags,
                                                                 int l2norm) {
@@ -382,8 +491,29 @@ __global__ void __launch_bounds__(REC_THREADS) kda_exact_kernel(const FwdParams 
         if (p.h0 != nullptr) x = *reinterpret_cast<const float4*>(p.h0 + st + (size_t)r * KD + 4 * lane);
         s[r][0] = x.x; s[r][1] = x.y; s[r][2] = x.z; s[r][3] = x.w;
     }
-    rec_tokens<ROWS, EXACT_AHEAD>(p.q, p.k, p.v, p.g, p.beta, p.o, p.scale, l2norm != 0, bos, len, H, h, v0, lane, s,
-                                  [](int) {});
+    if constexpr (ROWS == 2) {
+        // windows of four tokens, the next window's inputs loaded while the
+        // current one is computed
+        __shared__ __align__(16) float red_all[REC_THREADS];
+        float* red = red_all + warp * 32;
+        TokIn<2> cur[4], nxt[4];
+        auto load_window = [&](TokIn<2> (&w)[4], int t0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (t0 + i < len) w[i] = load_tok<2>(p.q, p.k, p.v, p.g, p.beta, (size_t)(bos + t0 + i) * H + h, v0, lane);
+        };
+        load_window(cur, 0);
+        for (int t0 = 0; t0 < len; t0 += 4) {
+            if (t0 + 4 < len) load_window(nxt, t0 + 4);
+            rec_window4(cur, len - t0 < 4 ? len - t0 : 4, p.o, p.scale, l2norm != 0, (size_t)(bos + t0) * H + h, H, v0,
+                        lane, s, red);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+        }
+    } else {
+        rec_tokens<ROWS, EXACT_AHEAD>(p.q, p.k, p.v, p.g, p.beta, p.o, p.scale, l2norm != 0, bos, len, H, h, v0, lane, s,
+                                      [](int) {});
+    }
     if (p.ht != nullptr) store_rows(p.ht + st, s, lane);
 }
 
