@@ -33,11 +33,14 @@ def _run_both(x):
 @pytest.mark.parametrize("w", [
     custom("noalloc_fixed", B=2, T=1024, H=4, with_h0=True, seed=61),
     custom("noalloc_varlen", B=1, T=612, H=3, seqlens=[100, 300, 0, 212], with_h0=True, seed=62),
+    # unscaled gates: every chunk through the wide prep kernel's queue, which
+    # lives in the shared scratch too
+    custom("noalloc_wide", B=1, T=1024, H=3, with_h0=True, seed=65, gate_div=1.0),
 ], ids=lambda w: w.name)
 def test_noalloc_matches_kda_fwd_on_consecutive_calls(w):
     for call in range(2):
         x = _device_inputs(custom(w.name, B=w.B, T=w.T, H=w.H, seqlens=w.seqlens, with_h0=w.with_h0,
-                                  seed=w.seed + 100 * call))
+                                  seed=w.seed + 100 * call, gate_div=w.gate_div))
         o, ht, o_ref, ht_ref = _run_both(x)
         assert torch.isfinite(o.float()).all() and torch.isfinite(ht).all()
         # the same kernels on the same inputs: bit-identical, not just close
