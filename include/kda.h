@@ -3,7 +3,7 @@
  * NVIDIA GB300 (sm_103a).
  *
  * The operation (page "PyPTO-Gym chunk_kda operator: an NPU forward of chunked
- * gated delta-rule linear attention", lpnh.cn/news/2283126):
+ * gated delta-rule linear attention"):
  *   per sequence n and head h, with the K x V state S starting at h0[n,h]^T
  *   (or zero) and, for every token t in order,
  *       S <- diag(exp(g_t)) S                       (per-dimension gate decay)

@@ -4,8 +4,7 @@ TEST INFRASTRUCTURE ONLY.  Nothing under ``oracle/`` is used by the product
 path; only tests, the smoke check and the benchmark's CPU-baseline leg call it.
 
 This restates the four steps M1-M4 of the page "PyPTO-Gym chunk_kda operator:
-an NPU forward of chunked gated delta-rule linear attention"
-(lpnh.cn/news/2283126), section "算法原理" (algorithm), literally and without
+an NPU forward of chunked gated delta-rule linear attention", section "算法原理" (algorithm), literally and without
 blocking or fusion, so that it can be compared with the per-token recurrence
 (``oracle.kda_recurrent``), which it must equal up to rounding order:
 

@@ -7,7 +7,7 @@
  * tests, the smoke check and the benchmark's CPU-baseline leg do.
  *
  * What it computes (page "PyPTO-Gym chunk_kda operator: an NPU forward of
- * chunked gated delta-rule linear attention", lpnh.cn/news/2283126):
+ * chunked gated delta-rule linear attention"):
  *   - section "算子定位与算法背景" (operator placement and background): per
  *     token, first the per-dimension gate decay S <- S * exp(g), then the
  *     delta update S <- S + outer(beta*k, v - k.S), then the read-out

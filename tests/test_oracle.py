@@ -11,7 +11,7 @@ set fails for a family of plausible mistakes planted in a small numpy copy of
 the recurrence.
 
 Page cited throughout: "PyPTO-Gym chunk_kda operator: an NPU forward of
-chunked gated delta-rule linear attention" (lpnh.cn/news/2283126).
+chunked gated delta-rule linear attention".
 """
 
 import json
