@@ -21,7 +21,10 @@
 // entering each token of the chunk into a per-CTA scratch, then steps the
 // token rule above backwards.  The sums over value rows (dq, dk, dg, dbeta)
 // are reduced across warps through shared memory, one barrier per token.
-// With q/k normalisation the kernel produces the gradients with respect to
+// Each warp stages the inputs of its next token (and in the backward walk
+// the state entering it) in shared memory by asynchronous copies while it
+// computes the current one, so the dependent chain does not wait on global
+// memory.  With q/k normalisation the kernel produces the gradients with respect to
 // the normalised q and k; kda_l2norm_bwd_kernel applies the normalisation's
 // chain rule afterwards.
 #include <cuda_bf16.h>
@@ -29,6 +32,7 @@
 #include "kda.h"
 #include "kda_common.cuh"
 #include "kda_bwd.cuh"
+#include "sm100_ptx.cuh"
 
 namespace kda {
 
@@ -38,7 +42,14 @@ constexpr int XB_THREADS = 512;
 constexpr int XB_WARPS = XB_THREADS / 32;
 constexpr int XB_ROWS = 8;                        // value rows per warp
 constexpr int XB_RED = 3 * KD + 4;                // dq, dk, dg partials + dbeta (padded)
-constexpr uint32_t XB_SMEM = 2u * XB_WARPS * XB_RED * 4u;
+constexpr uint32_t XB_RED_BYTES = 2u * XB_WARPS * XB_RED * 4u;
+// One token's staging slot per warp (bytes): q, k (8 B per lane), g (16 B
+// per lane), the warp's 8 value entries of v and of dout, beta, then the
+// state entering the token (8 rows x 32 lanes x 16 B; backward walk only).
+constexpr uint32_t SL_Q = 0, SL_K = 256, SL_G = 512, SL_V = 1024, SL_DO = 1040, SL_BETA = 1056, SL_S = 1152;
+constexpr uint32_t SLOT_BYTES = SL_S + XB_ROWS * 32 * 16;   // 5248
+constexpr uint32_t XB_SMEM = XB_RED_BYTES + 2u * XB_WARPS * SLOT_BYTES;
+static_assert(XB_SMEM <= 232448, "shared memory above the 227 KB limit");
 
 struct TokenIn {
     float q[4], k[4], e[4];   // this lane's K entries: scaled (normalised) q, (normalised) k, exp(g)
@@ -54,12 +65,47 @@ __device__ __forceinline__ void load_rows8_bf16(const uint16_t* p, float (&x)[XB
     x[6] = __uint_as_float(u.w << 16); x[7] = __uint_as_float(u.w & 0xffff0000u);
 }
 
-__device__ __forceinline__ void load_token(const BwdParams& p, size_t tok, int v0, int lane, TokenIn& in) {
-    load4_bf16(p.q + tok * KD + 4 * lane, in.q);
-    load4_bf16(p.k + tok * KD + 4 * lane, in.k);
-    const float4 gv = *reinterpret_cast<const float4*>(p.g + tok * KD + 4 * lane);
-    in.beta = p.beta[tok];
-    load_rows8_bf16(p.v + tok * VD + v0, in.v);
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Stage token tok's inputs (and, with state != null, the warp's rows of the
+// state entering it) into a slot: one commit group per call.
+__device__ __forceinline__ void stage_token(const BwdParams& p, size_t tok, int v0, int lane, uint32_t slot,
+                                            bool with_dout, const float* state) {
+    cp_async8(slot + SL_Q + 8u * lane, p.q + tok * KD + 4 * lane);
+    cp_async8(slot + SL_K + 8u * lane, p.k + tok * KD + 4 * lane);
+    cp_async16(slot + SL_G + 16u * lane, p.g + tok * KD + 4 * lane);
+    if (lane == 0) {
+        cp_async16(slot + SL_V, p.v + tok * VD + v0);
+        if (with_dout) cp_async16(slot + SL_DO, p.dout + tok * VD + v0);
+        cp_async4(slot + SL_BETA, p.beta + tok);
+    }
+    if (state != nullptr) {
+#pragma unroll
+        for (int r = 0; r < XB_ROWS; ++r) cp_async16(slot + SL_S + (uint32_t)(r * 32 + lane) * 16u, state + (size_t)r * KD + 4 * lane);
+    }
+    cp_commit();
+}
+
+// A staged token's inputs: unpacked, scaled (and normalised), exp(g)
+__device__ __forceinline__ void read_token(const BwdParams& p, const uint8_t* slot, int lane, TokenIn& in) {
+    load4_bf16(reinterpret_cast<const uint16_t*>(slot + SL_Q + 8 * lane), in.q);
+    load4_bf16(reinterpret_cast<const uint16_t*>(slot + SL_K + 8 * lane), in.k);
+    const float4 gv = *reinterpret_cast<const float4*>(slot + SL_G + 16 * lane);
+    in.beta = *reinterpret_cast<const float*>(slot + SL_BETA);
+    load_rows8_bf16(reinterpret_cast<const uint16_t*>(slot + SL_V), in.v);
     float qs = p.scale, ks = 1.f;
     if (p.l2norm) {   // x / sqrt(sum x^2 + 1e-6), section "测试与验证体系"
         const float sq = warp_sum(in.q[0] * in.q[0] + in.q[1] * in.q[1] + in.q[2] * in.q[2] + in.q[3] * in.q[3]);
@@ -115,8 +161,10 @@ __device__ __forceinline__ void store_state(float* dst, int lane, const float (&
 
 __global__ void __launch_bounds__(XB_THREADS, 1)
 kda_bwd_exact_kernel(const BwdParams p, const uint32_t* only) {
-    extern __shared__ __align__(16) float red[];   // [2][XB_WARPS][XB_RED]
+    extern __shared__ __align__(16) float red[];   // [2][XB_WARPS][XB_RED], then the staging slots
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* slots = reinterpret_cast<uint8_t*>(red) + XB_RED_BYTES + (size_t)warp * 2 * SLOT_BYTES;
+    const uint32_t slots_s = smem_u32(slots);
     const int v0 = warp * XB_ROWS;
     const int H = p.H;
     const int units = p.N * H;
@@ -151,15 +199,31 @@ kda_bwd_exact_kernel(const BwdParams p, const uint32_t* only) {
 #pragma unroll
             for (int r = 0; r < XB_ROWS; ++r) s[r][0] = s[r][1] = s[r][2] = s[r][3] = 0.f;
         }
-        for (int j = 0; j < nch; ++j) {
+        auto ckpt_of = [&](int j) {
             const int slot = p.cu == nullptr ? n * p.NT + j : p.cu[n] / BT + n + j;
-            store_state(p.ckpt + (((size_t)slot * H + h) * VD + v0) * KD, lane, s);
-            if (j == nch - 1) break;   // the last chunk's tokens are replayed in pass 2
-            for (int t = j * BT; t < (j + 1) * BT; ++t) {
+            return p.ckpt + (((size_t)slot * H + h) * VD + v0) * KD;
+        };
+        {
+            // the tokens of every chunk but the last (replayed in pass 2),
+            // each staged one token ahead
+            const int tend = nch > 0 ? (nch - 1) * BT : 0;
+            if (tend > 0) stage_token(p, (size_t)bos * H + h, v0, lane, slots_s, false, nullptr);
+            for (int t = 0; t < tend; ++t) {
+                if (t % BT == 0) store_state(ckpt_of(t / BT), lane, s);
+                if (t + 1 < tend) {
+                    stage_token(p, (size_t)(bos + t + 1) * H + h, v0, lane, slots_s + (uint32_t)((t + 1) & 1) * SLOT_BYTES,
+                                false, nullptr);
+                    cp_wait<1>();
+                } else {
+                    cp_wait<0>();
+                }
+                __syncwarp();
                 TokenIn in;
-                load_token(p, (size_t)(bos + t) * H + h, v0, lane, in);
+                read_token(p, slots + (size_t)(t & 1) * SLOT_BYTES, lane, in);
                 forward_token(in, lane, s);
+                __syncwarp();   // the slot is read before the next stage overwrites it
             }
+            if (nch > 0) store_state(ckpt_of(nch - 1), lane, s);
         }
 
         // pass 2: backward, chunk by chunk from the last
@@ -175,20 +239,52 @@ kda_bwd_exact_kernel(const BwdParams p, const uint32_t* only) {
             const int t0 = j * BT;
             const int t1 = min(len, t0 + BT);
             load_state(p.ckpt + (((size_t)slot * H + h) * VD + v0) * KD, lane, s);
+            stage_token(p, (size_t)(bos + t0) * H + h, v0, lane, slots_s, false, nullptr);
             for (int t = t0; t < t1; ++t) {   // states entering each token of the chunk
                 store_state(scratch + ((size_t)(t - t0) * VD + v0) * KD, lane, s);
+                if (t + 1 < t1) {
+                    stage_token(p, (size_t)(bos + t + 1) * H + h, v0, lane,
+                                slots_s + (uint32_t)((t + 1 - t0) & 1) * SLOT_BYTES, false, nullptr);
+                    cp_wait<1>();
+                } else {
+                    cp_wait<0>();
+                }
+                __syncwarp();
                 TokenIn in;
-                load_token(p, (size_t)(bos + t) * H + h, v0, lane, in);
+                read_token(p, slots + (size_t)((t - t0) & 1) * SLOT_BYTES, lane, in);
                 forward_token(in, lane, s);
+                __syncwarp();
             }
+            // the scratch states stored above are read back below by copies
+            // this thread issues: its stores are ordered before them
+            __threadfence_block();
+            auto stage_back = [&](int t, int k) {   // token t with its state and dout, into slot k
+                stage_token(p, (size_t)(bos + t) * H + h, v0, lane, slots_s + (uint32_t)k * SLOT_BYTES, true,
+                            scratch + ((size_t)(t - t0) * VD + v0) * KD);
+            };
+            stage_back(t1 - 1, 0);
             for (int t = t1 - 1; t >= t0; --t) {
                 const size_t tok = (size_t)(bos + t) * H + h;
+                const int k = (t1 - 1 - t) & 1;
+                if (t - 1 >= t0) {
+                    stage_back(t - 1, k ^ 1);
+                    cp_wait<1>();
+                } else {
+                    cp_wait<0>();
+                }
+                __syncwarp();
+                const uint8_t* sl = slots + (size_t)k * SLOT_BYTES;
                 TokenIn in;
-                load_token(p, tok, v0, lane, in);
+                read_token(p, sl, lane, in);
                 float dov[XB_ROWS];
-                load_rows8_bf16(p.dout + tok * VD + v0, dov);
+                load_rows8_bf16(reinterpret_cast<const uint16_t*>(sl + SL_DO), dov);
                 float a[XB_ROWS][4];
-                load_state(scratch + ((size_t)(t - t0) * VD + v0) * KD, lane, a);
+#pragma unroll
+                for (int r = 0; r < XB_ROWS; ++r) {
+                    const float4 x = *reinterpret_cast<const float4*>(sl + SL_S + (r * 32 + lane) * 16);
+                    a[r][0] = x.x; a[r][1] = x.y; a[r][2] = x.z; a[r][3] = x.w;
+                }
+                __syncwarp();   // the slot is read before the next stage overwrites it
 
                 float rr[XB_ROWS], gk[XB_ROWS];
 #pragma unroll
