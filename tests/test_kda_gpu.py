@@ -120,6 +120,20 @@ def test_strong_gates_within_range():
     assert_within(compare(o, ht, o_ref, ht_ref))
 
 
+@pytest.mark.parametrize("gate_div", [8.0, 6.0])
+def test_fast_path_near_its_range(gate_div):
+    """Gates just inside the fp16 factoring's range (at g/8 no chunk and at
+    g/6 a few leave the fast kernel on the large workload): the fp16 operands
+    are near their largest values on one side of the pivot row and near the
+    subnormal range on the other; the result must still match the oracle."""
+    x = make_inputs(custom("edge", B=1, T=2048, H=4, with_h0=True, seed=28, gate_div=gate_div))
+    o, ht = run_gpu(x)
+    o_ref, ht_ref = run_oracle(x)
+    stats = compare(o, ht, o_ref, ht_ref)
+    print(gate_div, stats)
+    assert_within(stats)
+
+
 def test_unscaled_gates_wide_path():
     """Unscaled log-sigmoid gates (about -0.8 per token, tens of nats per
     chunk): the fp16 factoring cannot hold these chunks, so they take the
