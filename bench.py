@@ -370,6 +370,115 @@ def run_decode(args, rank, world, local):
 
 
 # ---------------------------------------------------------------------------
+# KCP forward with the ranks simulated on one GPU
+# ---------------------------------------------------------------------------
+
+KCP_METRIC = "KDA KCP forward (ranks simulated on one GPU) token*heads/s at T=64K H=32 K=V=128"
+
+
+def run_kcp(args, rank, world, local, w):
+    """The KCP forward of the workload packed as one batch of sequences, with
+    --kcp-world ranks simulated on this GPU (per rank: the pre-process of its
+    last piece, the merge, its local forward; all on one stream, so the
+    ranks run one after another), beside the unsplit forward of the same
+    inputs.  The C entry point is called with preallocated buffers."""
+    import ctypes
+    from chunked_gated_delta_kda_gb300 import binding
+    W = args.kcp_world
+    name = f"{w.name}_kcp{W}"
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the forward "
+                              "(bench.py --impl reference); the KCP simulator has no separate one"}), flush=True)
+        return 0
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = binding.load_library()
+    x = make_inputs(w, device=str(dev), draw_on_device=True, seed_offset=rank)
+    q, k, v, g, beta, h0 = (x[nn] for nn in ("q", "k", "v", "g", "beta", "h0"))
+    B, T, H = w.B, w.T, w.H
+    # packed: B fixed-length sequences become one batch of B sequences (a
+    # varlen workload is packed already)
+    q, k, v, g, beta = (t.reshape((1, B * T) + tuple(t.shape[2:])) for t in (q, k, v, g, beta))
+    N = w.N
+    cu_host = torch.tensor([i * T for i in range(N + 1)], dtype=torch.int32) if w.seqlens is None else \
+        torch.tensor([0] + list(np.cumsum(w.seqlens)), dtype=torch.int32)
+    Tp = int(cu_host[-1])
+    o = torch.empty((1, Tp, H, w.V), dtype=torch.bfloat16, device=dev)
+    ht = torch.empty((N, H, w.V, w.K), dtype=torch.float32, device=dev)
+    nbytes = int(lib.kda_kcp_workspace_bytes(Tp, H, w.K, w.V, N, W))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+    def step():
+        rc = lib.kda_kcp_fwd(ptr(q), ptr(k), ptr(v), ptr(g), ptr(beta), -1.0, ptr(h0), ctypes.c_void_p(cu_host.data_ptr()),
+                             ptr(o), ptr(ht), Tp, H, w.K, w.V, N, W, 0, ptr(ws), nbytes,
+                             ctypes.c_void_p(stream.cuda_stream))
+        assert rc == 0, f"kda_kcp_fwd: {rc}"
+
+    cu_dev = cu_host.to(dev)
+    fws = torch.empty(binding.workspace_bytes(1, Tp, H, N), dtype=torch.uint8, device=dev)
+
+    def unsplit():
+        binding.kda_fwd(q, k, v, g, beta, None, h0, cu_dev, o, ht, N, 0, fws)
+
+    def timed(fn, steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / steps
+
+    for _ in range(args.warmup):
+        step()
+        unsplit()
+    assert binding.get_status(ws) == 0
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start = time.time()
+    ms = max_over_ranks(timed(step, args.steps), dev, world)
+    t_end = time.time()
+    clocks.stop()
+    ms_unsplit = timed(unsplit, args.steps)
+    th, alg_bytes, _, _ = algorithmic(w, N)
+    peaks = load_peaks()
+    # the simulated ranks run in series: local forwards over every token, plus
+    # for every rank whose last piece continues two forwards of that piece
+    n_carry = sum(1 for r in range(W - 1) if (r + 1) * Tp // W not in set(cu_host.tolist()))
+    line = {"metric": KCP_METRIC, "value": job_rate(th, world, ms), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in/out; fp16 MMA operands, fp32 accumulate, fp32 state",
+            "data": "synthetic",
+            "config": {"workload": name, "T": Tp, "H": H, "sequences": N, "world_size_simulated": W,
+                       "ranks_carrying_state": n_carry,
+                       "l2_between_steps": "inputs (2.7 GB per step at T=64K H=32) larger than L2; no flush"},
+            "unsplit_forward_ms": ms_unsplit,
+            "path_roofline": {"bound": "hbm", "alg_bytes": alg_bytes, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "achieved": alg_bytes / (ms * 1e-3) / 1e9,
+                              "frac": alg_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                              "note": "the simulator replays each carrying rank's last piece twice (pre-process) "
+                                      "and runs the ranks in series"},
+            # per forward: fast prep, wide prep, scan, exact recompute; plus the
+            # identity kernel and one merge per carrying rank
+            "gpu_launches": args.steps * (4 * (W + 2 * n_carry) + (1 + n_carry if n_carry else 0)),
+            "clocks": clocks.summary(t_start, t_end)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+# ---------------------------------------------------------------------------
 # Backward (gradients of <do, o> + <dht, ht>)
 # ---------------------------------------------------------------------------
 
@@ -596,9 +705,11 @@ def main():
     ap.add_argument("--gate-div", type=float, default=None,
                     help="forward: divide logsigmoid(N(0,1)) by this for g instead of the workload's 16 "
                          "(1 = the pages' unscaled stable-input gates, whose chunks take the wide prep kernel)")
-    ap.add_argument("--op", choices=["fwd", "decode", "bwd"], default="fwd",
+    ap.add_argument("--op", choices=["fwd", "decode", "bwd", "kcp"], default="fwd",
                     help="fwd: the chunked forward (default); decode: the token-by-token entry point; "
-                         "bwd: the chunked backward")
+                         "bwd: the chunked backward; kcp: the KCP forward with --kcp-world ranks simulated "
+                         "on this GPU")
+    ap.add_argument("--kcp-world", type=int, default=4, help="simulated ranks for --op kcp")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
@@ -612,6 +723,8 @@ def main():
         return run_decode(args, rank, world, local)
     if args.op == "bwd":
         return run_bwd(args, rank, world, local, w)
+    if args.op == "kcp":
+        return run_kcp(args, rank, world, local, w)
     if args.impl == "reference":
         return run_reference(args, w, rank, world)
 
