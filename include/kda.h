@@ -98,8 +98,11 @@ typedef enum {
 /*
  * Bytes of device workspace kda_fwd needs for these sizes (an upper bound
  * that covers both fixed-length and varlen packing).  0 on invalid sizes.
- * Layout: a 256-byte status header, then one 131584-byte tile per
- * (128-token chunk slot, head), then one flag word per (sequence, head).
+ * Layout: a 256-byte header (word 0 the device status; word 1 the number
+ * of chunks the fast prep kernel queued for the wide one), the queue (one
+ * int32 work item, slot * H + head, per queued chunk; room for every (chunk
+ * slot, head), padded to 256 bytes), one 131584-byte tile per (128-token
+ * chunk slot, head), then one flag word per (sequence, head).
  */
 size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int N);
 
