@@ -45,6 +45,20 @@ def test_named_workload_every_unit(name):
     assert torch.isfinite(o.float()).all() and torch.isfinite(ht).all()
 
 
+def test_large_workload_unscaled_gates_every_unit():
+    """The large workload's sizes (B=1, T=65536, H=32) with the pages'
+    unscaled gates: all 16384 (chunk, head) items go through the wide prep
+    kernel's queue; every unit against the oracle."""
+    w = custom("t65536_h32_g1", B=1, T=65536, H=32, seed=4, gate_div=1.0)
+    x = make_inputs(w)
+    o, ht, items = _fwd_wide_record(x)
+    assert len(items) == 16384
+    o_ref, ht_ref = run_oracle(x)
+    stats = compare(o, ht, o_ref, ht_ref)
+    print(stats)
+    assert_within(stats)
+
+
 # ---------------------------------------------------------------------------
 # Ragged tails, varlen edge cases, sizes spanning several chunks
 # ---------------------------------------------------------------------------
